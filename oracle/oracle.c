@@ -1,0 +1,263 @@
+/*
+ * CPU oracle for submanifold sparse 3D convolution — TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the plain, slow, obviously-correct statement of what the GPU
+ * library computes.  Only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark may load it; the product path never does.
+ * It shares no code, header, table or helper with the CUDA sources.
+ *
+ * Sources (the web pages this method is described on):
+ *  - "Contribution Tasks — JeffreyXiang/FlexGEMM", §一 (positioning) and §二
+ *    (architecture map, "how one call flows through the modules", key types
+ *    and functions table): the operator sparse_submanifold_conv3d(feats,
+ *    coords, shape, weight, bias) computes outputs only at the active input
+ *    sites; a neighbour map is built from a coordinate hash map
+ *    (hashmap_insert_3d_idx_as_val, subm_neighbor_map) and reused by the
+ *    forward and the backward pass (neighbor_cache).
+ *  - "From CUDA to Triton: Triton JIT and autotuning", §六 6.2: the masked
+ *    implicit GEMM kernel takes (input, weight, bias, neighbor, sorted_idx,
+ *    output) with V = 27 taps, a uint32 neighbour table, and a contraction
+ *    dimension of V * Ci.
+ *
+ * The pages do not write the sum out.  The reading taken here (the standard
+ * submanifold convolution) is:
+ *   tap k <-> offset o_k = (dx,dy,dz) in {-1,0,1}^3, k = 9(dx+1)+3(dy+1)+(dz+1)
+ *   nbr[i][k] = j  if voxel j has coordinate coord_i + o_k in the same batch
+ *               element, else 0xFFFFFFFF (outside the grid counts as absent)
+ *   mask[i]   = sum_k [nbr[i][k] valid] * 2^k
+ *   out[i][co]  = bias[co] + sum_k sum_ci W[k][ci][co] * f[nbr[i][k]][ci]
+ *   dX[j][ci]   = sum over (i,k) with nbr[i][k] = j of sum_co W[k][ci][co] dY[i][co]
+ *   dW[k][ci][co] = sum_i [nbr[i][k] valid] f[nbr[i][k]][ci] * dY[i][co]
+ *   db[co]      = sum_i dY[i][co]
+ * All floating point is accumulated in double precision from the (already
+ * dtype-rounded) inputs.
+ *
+ * The neighbour lookup is a dictionary: a sorted array of (key, row) pairs
+ * built with qsort and searched with bsearch from the C library.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_NONE 0xFFFFFFFFu
+
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_OUT_OF_RANGE = 2, ORACLE_DUPLICATE = 3,
+       ORACLE_NO_MEMORY = 4 };
+
+/* Tap index k -> offset (dx, dy, dz). */
+static void tap_offset(int k, int* dx, int* dy, int* dz)
+{
+    *dx = k / 9 - 1;
+    *dy = (k / 3) % 3 - 1;
+    *dz = k % 3 - 1;
+}
+
+/* Linear address of (b,x,y,z) in a B x X x Y x Z grid. */
+static uint64_t linear_key(int64_t b, int64_t x, int64_t y, int64_t z,
+                           int64_t X, int64_t Y, int64_t Z)
+{
+    return (uint64_t)(((b * X + x) * Y + y) * Z + z);
+}
+
+typedef struct { uint64_t key; int64_t row; } dict_entry;
+
+static int cmp_entry(const void* a, const void* b)
+{
+    const dict_entry* p = (const dict_entry*)a;
+    const dict_entry* q = (const dict_entry*)b;
+    if (p->key < q->key) return -1;
+    if (p->key > q->key) return 1;
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * Neighbour map (the subm_neighbor_map step).  coords is [N][4] = (b,x,y,z).
+ * Returns ORACLE_OUT_OF_RANGE if a coordinate lies outside [0,B)x[0,X)x[0,Y)x[0,Z),
+ * ORACLE_DUPLICATE if two rows share a coordinate; nbr/mask are then unspecified.
+ */
+int oracle_nbrmap(const int32_t* coords, int64_t N, int B, int X, int Y, int Z,
+                  uint32_t* nbr, uint32_t* mask)
+{
+    if (N < 0 || B <= 0 || X <= 0 || Y <= 0 || Z <= 0) return ORACLE_BAD_ARG;
+    if (N == 0) return ORACLE_OK;
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        if (c[0] < 0 || c[0] >= B || c[1] < 0 || c[1] >= X ||
+            c[2] < 0 || c[2] >= Y || c[3] < 0 || c[3] >= Z)
+            return ORACLE_OUT_OF_RANGE;
+    }
+    dict_entry* dict = (dict_entry*)malloc((size_t)N * sizeof(dict_entry));
+    if (!dict) return ORACLE_NO_MEMORY;
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        dict[i].key = linear_key(c[0], c[1], c[2], c[3], X, Y, Z);
+        dict[i].row = i;
+    }
+    qsort(dict, (size_t)N, sizeof(dict_entry), cmp_entry);
+    for (int64_t i = 1; i < N; ++i) {
+        if (dict[i].key == dict[i - 1].key) {
+            free(dict);
+            return ORACLE_DUPLICATE;
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        uint32_t m = 0;
+        for (int k = 0; k < 27; ++k) {
+            int dx, dy, dz;
+            tap_offset(k, &dx, &dy, &dz);
+            int64_t x = (int64_t)c[1] + dx, y = (int64_t)c[2] + dy, z = (int64_t)c[3] + dz;
+            uint32_t j = ORACLE_NONE;
+            if (x >= 0 && x < X && y >= 0 && y < Y && z >= 0 && z < Z) {
+                dict_entry probe;
+                probe.key = linear_key(c[0], x, y, z, X, Y, Z);
+                probe.row = 0;
+                const dict_entry* hit = (const dict_entry*)bsearch(
+                    &probe, dict, (size_t)N, sizeof(dict_entry), cmp_entry);
+                if (hit) j = (uint32_t)hit->row;
+            }
+            nbr[i * 27 + k] = j;
+            if (j != ORACLE_NONE) m |= 1u << k;
+        }
+        mask[i] = m;
+    }
+    free(dict);
+    return ORACLE_OK;
+}
+
+/*
+ * Forward: out[i][co] = bias[co] + sum_k sum_ci W[k][ci][co] * f[nbr[i][k]][ci]
+ * for the R rows whose neighbour lists are given in nbr ([R][27], indices into
+ * the Nf rows of f).  W is [27][Cin][Cout]; bias may be NULL (zero).
+ */
+void oracle_fwd(const uint32_t* nbr, int64_t R, const double* f, int64_t Nf,
+                const double* W, const double* bias, int Cin, int Cout, double* out)
+{
+    (void)Nf;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < R; ++i) {
+        double* o = out + i * Cout;
+        for (int co = 0; co < Cout; ++co) o[co] = bias ? bias[co] : 0.0;
+        for (int k = 0; k < 27; ++k) {
+            uint32_t j = nbr[i * 27 + k];
+            if (j == ORACLE_NONE) continue;
+            const double* fj = f + (int64_t)j * Cin;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const double a = fj[ci];
+                const double* w = W + ((int64_t)k * Cin + ci) * Cout;
+                for (int co = 0; co < Cout; ++co) o[co] += w[co] * a;
+            }
+        }
+    }
+}
+
+/*
+ * Input gradient by its definition (the adjoint of the forward): every valid
+ * pair (i,k) with j = nbr[i][k] adds W_k dY[i] to dX[j].  nbr is [N][27] over
+ * the N rows of dY and dX.  Sequential: the scatter is written out plainly.
+ */
+void oracle_dgrad_scatter(const uint32_t* nbr, int64_t N, const double* dY,
+                          const double* W, int Cin, int Cout, double* dX)
+{
+    memset(dX, 0, (size_t)N * Cin * sizeof(double));
+    for (int64_t i = 0; i < N; ++i) {
+        const double* g = dY + i * Cout;
+        for (int k = 0; k < 27; ++k) {
+            uint32_t j = nbr[i * 27 + k];
+            if (j == ORACLE_NONE) continue;
+            double* d = dX + (int64_t)j * Cin;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const double* w = W + ((int64_t)k * Cin + ci) * Cout;
+                double s = 0.0;
+                for (int co = 0; co < Cout; ++co) s += w[co] * g[co];
+                d[ci] += s;
+            }
+        }
+    }
+}
+
+/*
+ * Input gradient for R chosen rows, gathered form: since o_{26-k} = -o_k,
+ * nbr[i][k] = j holds exactly when nbr[j][26-k] = i, so
+ *   dX[j][ci] = sum_k' sum_co W[26-k'][ci][co] * dY[nbr[j][k']][co].
+ * nbr is [R][27] (indices into the rows of dY).  The tests check this form
+ * against oracle_dgrad_scatter.
+ */
+void oracle_dgrad_rows(const uint32_t* nbr, int64_t R, const double* dY, int64_t Ny,
+                       const double* W, int Cin, int Cout, double* dX)
+{
+    (void)Ny;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < R; ++r) {
+        double* d = dX + r * Cin;
+        for (int ci = 0; ci < Cin; ++ci) d[ci] = 0.0;
+        for (int kp = 0; kp < 27; ++kp) {
+            uint32_t i = nbr[r * 27 + kp];
+            if (i == ORACLE_NONE) continue;
+            const double* g = dY + (int64_t)i * Cout;
+            const int k = 26 - kp;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const double* w = W + ((int64_t)k * Cin + ci) * Cout;
+                double s = 0.0;
+                for (int co = 0; co < Cout; ++co) s += w[co] * g[co];
+                d[ci] += s;
+            }
+        }
+    }
+}
+
+/*
+ * Weight and bias gradient:
+ *   dW[k][ci][co] = sum_i [nbr[i][k] valid] f[nbr[i][k]][ci] * dY[i][co]
+ *   db[co]        = sum_i dY[i][co]      (db may be NULL)
+ * nbr is [N][27]; f has Nf rows; dY has N rows.  Parallel over taps only, so
+ * every output entry is one plain sum in row order.
+ */
+void oracle_wgrad(const uint32_t* nbr, int64_t N, const double* f, int64_t Nf,
+                  const double* dY, int Cin, int Cout, double* dW, double* db)
+{
+    (void)Nf;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int k = 0; k < 27; ++k) {
+        double* w = dW + (int64_t)k * Cin * Cout;
+        memset(w, 0, (size_t)Cin * Cout * sizeof(double));
+        for (int64_t i = 0; i < N; ++i) {
+            uint32_t j = nbr[i * 27 + k];
+            if (j == ORACLE_NONE) continue;
+            const double* fj = f + (int64_t)j * Cin;
+            const double* g = dY + i * Cout;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const double a = fj[ci];
+                double* wr = w + (int64_t)ci * Cout;
+                for (int co = 0; co < Cout; ++co) wr[co] += a * g[co];
+            }
+        }
+    }
+    if (db) {
+        for (int co = 0; co < Cout; ++co) db[co] = 0.0;
+        for (int64_t i = 0; i < N; ++i)
+            for (int co = 0; co < Cout; ++co) db[co] += dY[i * Cout + co];
+    }
+}
