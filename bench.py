@@ -1,0 +1,386 @@
+"""Benchmark: one step = the whole submanifold-conv hot path on one batch of
+seeded synthetic voxels, through the C ABI:
+    neighbour-map build (hash, probe, Morton sort, tile masks)
+    -> forward -> input gradient -> weight and bias gradient.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``value`` = voxels/s over all ranks (each rank
+runs its own independent replica of the workload: weak scaling, no data-path
+collective).  Per-step device time comes from CUDA events on the launch
+stream; L2 is flushed (256 MiB write) between steps, outside the events.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "submanifold conv3d fwd+bwd voxels/s & TFLOP/s (valid pairs), % of GB300 roofline"
+DEFAULT_WORKLOAD = "b4_r64_spheres_c64_f16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ------------------------------------------------------------------ work model
+def pass_work(N, P, cin, cout, s, splits):
+    """Algorithmic FLOPs and gathered+written bytes per pass (valid pairs only)."""
+    nbr_bytes = 4 * 28 * N  # nbr [N,27] + mask [N]
+    w = 27 * cin * cout * s
+    return {
+        "fwd": (2.0 * P * cin * cout, P * cin * s + N * cout * s + nbr_bytes + w),
+        "dgrad": (2.0 * P * cin * cout, P * cout * s + N * cin * s + nbr_bytes + w),
+        "wgrad": (2.0 * P * cin * cout, P * cin * s + P * cout * s + 2 * splits * 27 * cin * cout * 4
+                  + 27 * cin * cout * s + N * cout * s),
+    }
+
+
+def nbrmap_bytes(N):
+    # coords read twice (insert + Morton) + probe: coords + 27 table probes (~12 B) + nbr/mask write
+    return 16 * N * 3 + 27 * 12 * N + 4 * 28 * N
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.devnull if False else os.path.join("/tmp", f"vg_clocks_{os.getpid()}.csv"), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.out.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from voxel_gemm_gb300 import ops, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = synth.WORKLOADS[args.workload]
+    coords_np = synth.make_coords(wl)
+    N = coords_np.shape[0]
+    s = 4 if wl.dtype == "f32" else 2
+    dt = synth.torch_dtype(wl.dtype)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        coords = torch.from_numpy(coords_np).to(dev)
+        f, W, b, dY = synth.make_tensors(wl, N, device=dev)
+        m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag, device=dev)
+        ws = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
+        out = torch.empty(N, wl.cout, dtype=dt, device=dev)
+        dX = torch.empty(N, wl.cin, dtype=dt, device=dev)
+        dW = torch.empty(27, wl.cin, wl.cout, dtype=dt, device=dev)
+        db = torch.empty(wl.cout, dtype=dt, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        m.build(coords, stream)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=stream)
+
+    def timed(fn, k, ev_list):
+        for _ in range(k):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ev_list.append((e0, e1))
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    assert m.status(stream) == ops.VG_OK
+    P = int(torch.stack([(m.mask >> k) & 1 for k in range(27)]).sum().item())
+
+    # ---- timed region: exactly K steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    evs = []
+    t_wall0 = time.perf_counter()
+    timed(step, args.steps, evs)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b_) for a, b_ in evs]
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    assert m.status(stream) == ops.VG_OK and ops.vg_conv_status(ws, stream) == ops.VG_OK
+    ms_per_step = tot_ms / args.steps
+
+    # ---- per-pass timings (same stream, same flush rule), for the roofline
+    phases = {}
+    kph = max(3, min(args.steps, 50))
+    calls = {
+        "nbrmap": lambda: m.build(coords, stream),
+        "fwd": lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream),
+        "dgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws,
+                                                stream=stream),
+        "wgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws,
+                                                stream=stream),
+    }
+    for name, fn in calls.items():
+        ev = []
+        fn()
+        timed(fn, kph, ev)
+        torch.cuda.synchronize(dev)
+        phases[name] = sum(a.elapsed_time(b_) for a, b_ in ev) / kph
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the region
+    h_coords = torch.from_numpy(coords_np).pin_memory()
+    h_f, h_W, h_b, h_dY = (t.to("cpu").pin_memory() for t in (f, W, b, dY))
+    h_out = torch.empty(out.shape, dtype=dt).pin_memory()
+    h_dX = torch.empty(dX.shape, dtype=dt).pin_memory()
+    h_dW = torch.empty(dW.shape, dtype=dt).pin_memory()
+    h_db = torch.empty(db.shape, dtype=dt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            coords.copy_(h_coords, non_blocking=True)
+            f.copy_(h_f, non_blocking=True)
+            W.copy_(h_W, non_blocking=True)
+            b.copy_(h_b, non_blocking=True)
+            dY.copy_(h_dY, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            h_dX.copy_(dX, non_blocking=True)
+            h_dW.copy_(dW, non_blocking=True)
+            h_db.copy_(db, non_blocking=True)
+
+    ke = max(3, min(args.steps, 100))
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    ev = []
+    timed(e2e_step, ke, ev)
+    stream.synchronize()
+    e2e_ms = sum(a.elapsed_time(b_) for a, b_ in ev) / ke
+
+    # ---- roofline of the dominant kernel pass
+    peaks = load_peaks()
+    cplan = ops.vg_conv_describe(N, wl.cin, wl.cout, dt)
+    nplan = ops.vg_nbrmap_describe(N, *wl.grid, wl.key_flag)
+    splits = cplan["splits"]
+    work = pass_work(N, P, wl.cin, wl.cout, s, splits)
+    work["nbrmap"] = (0.0, float(nbrmap_bytes(N)))
+    tc_peak = peaks["bf16_tflops"] * 1e12
+    bw = peaks["hbm_gbs"] * 1e9
+    rows = {}
+    for name, (fl, by) in work.items():
+        t = phases[name] * 1e-3
+        bound = "tensor" if fl / tc_peak > by / bw else "hbm"
+        if wl.dtype == "f32" and name != "nbrmap":
+            bound = "hbm" if fl / tc_peak <= by / bw else "alu"
+        rows[name] = {"ms": phases[name], "flops": fl, "bytes": by, "bound": bound,
+                      "tflops": fl / t / 1e12, "gbs": by / t / 1e9,
+                      "frac": (by / bw) / t if bound == "hbm" else (fl / tc_peak) / t}
+    dom = max(("fwd", "dgrad", "wgrad", "nbrmap"), key=lambda k: phases[k])
+    d = rows[dom]
+    roof = {"kernel": dom, "bound": d["bound"],
+            "achieved": d["gbs"] if d["bound"] == "hbm" else d["tflops"],
+            "peak": peaks["hbm_gbs"] if d["bound"] == "hbm" else peaks["bf16_tflops"],
+            "unit": "GB/s" if d["bound"] == "hbm" else "TFLOP/s",
+            "traffic": None, "peak_source": peaks["source"] + " (burst)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    t_roof = sum(max(fl / tc_peak, by / bw) for fl, by in work.values())
+    total_fl = sum(fl for fl, _ in work.values())
+    res = {
+        "metric": METRIC, "value": world * N / (ms_per_step * 1e-3), "unit": "voxels/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "res": wl.res, "N": N, "P": P, "cin": wl.cin,
+                   "cout": wl.cout, "step": "nbrmap build + fwd + dgrad + wgrad + dbias",
+                   "l2": "flushed between steps (256 MiB write, outside the per-step events)",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": world * total_fl / (ms_per_step * 1e-3) / 1e12,
+        "roofline_step_frac": t_roof / (ms_per_step * 1e-3),
+        "roofline": roof,
+        "passes": rows,
+        "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "voxels/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (nplan["launches"] + cplan["launches_fwd"] + cplan["launches_bwd"]),
+        "path": {"tensor_core": bool(cplan["tensor_core"]), "wgrad_splits": splits,
+                 "hash_keys": 64 if nplan["key64"] else 32, "sort_passes": nplan["sort_passes"]},
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+    }
+    return res
+
+
+# ------------------------------------------------------------------ oracle arm (CPU)
+def oracle_sample(wl, coords_np, budget_rows, seed=0):
+    """Time the oracle on a bounded sample of the workload: the full neighbour map
+    (scaled per voxel) and fwd + dgrad + wgrad over `budget_rows` sampled rows."""
+    import numpy as np
+    import oracle
+    N = coords_np.shape[0]
+    t0 = time.perf_counter()
+    nbr, mask = oracle.nbrmap(coords_np, *wl.grid)
+    t_map = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    R = min(N, budget_rows)
+    rows = np.sort(rng.choice(N, size=R, replace=False))
+    sub = nbr[rows]
+    valid = sub != oracle.NONE
+    used = np.unique(sub[valid]).astype(np.int64)
+    remap = np.full(sub.shape, oracle.NONE, dtype=np.uint32)
+    remap[valid] = np.searchsorted(used, sub[valid].astype(np.int64)).astype(np.uint32)
+    f = rng.standard_normal((used.size, wl.cin))
+    W = rng.standard_normal((27, wl.cin, wl.cout)) * 0.05
+    b = rng.standard_normal(wl.cout)
+    g_used = rng.standard_normal((used.size, wl.cout))
+    g_rows = rng.standard_normal((R, wl.cout))
+    t1 = time.perf_counter()
+    oracle.fwd(remap, f, W, b)
+    oracle.dgrad_rows(remap, g_used, W)
+    oracle.wgrad(remap, f, g_rows)
+    t_conv = time.perf_counter() - t1
+    per_voxel = t_map / N + t_conv / R
+    return 1.0 / per_voxel, {"rows": R, "t_map_s": t_map, "t_conv_s": t_conv}
+
+
+def run_reference(args):
+    from voxel_gemm_gb300 import synth
+    import oracle
+    wl = synth.WORKLOADS[args.workload]
+    coords_np = synth.make_coords(wl)
+    budget = rows_budget(wl)
+    for _ in range(args.warmup):
+        oracle_sample(wl, coords_np, max(64, budget // 8))
+    vals = []
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        v, _ = oracle_sample(wl, coords_np, budget, seed=k)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    cores = oracle.num_threads()
+    sample = (f"full neighbour map of N={coords_np.shape[0]} voxels, then fwd+dgrad+wgrad over "
+              f"{min(budget, coords_np.shape[0])} seeded sampled rows per step; voxels/s = 1 / (map time per "
+              f"voxel + conv time per sampled row)")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "res": wl.res, "N": int(coords_np.shape[0]),
+                       "cin": wl.cin, "cout": wl.cout},
+            "cpu_baseline": {"value": value, "unit": "voxels/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def rows_budget(wl):
+    # about 2-4 s of fp64 work per sample on a many-core host
+    per_row = 3 * 10.6 * wl.cin * wl.cout
+    return int(max(256, min(65536, 4e9 / per_row)))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            from voxel_gemm_gb300 import synth
+            import oracle
+            wl = synth.WORKLOADS[args.workload]
+            coords_np = synth.make_coords(wl)
+            v, info = oracle_sample(wl, coords_np, rows_budget(wl))
+            res["cpu_baseline"] = {"value": v, "unit": "voxels/s", "cores": oracle.num_threads(),
+                                   "kind": "oracle",
+                                   "sample": f"full map of N={coords_np.shape[0]}, fwd+dgrad+wgrad over "
+                                             f"{info['rows']} sampled rows ({info['t_map_s']:.2f}s map, "
+                                             f"{info['t_conv_s']:.2f}s conv)"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * vg.h — C ABI of the GB300 (sm_103a) submanifold sparse 3D convolution library
+ * (libvoxelgemm.so).
+ *
+ * The operator is the submanifold convolution of "Contribution Tasks —
+ * JeffreyXiang/FlexGEMM", §一 (positioning) and §二 (architecture map; "how one
+ * call flows through the modules"; key types and functions table):
+ * sparse_submanifold_conv3d(feats, coords, shape, weight, bias) evaluates a
+ * 3x3x3 convolution only at the active voxels, through a neighbour map that is
+ * built once from a coordinate hash map and reused by the forward and the
+ * backward pass (the page's neighbor_cache).  The kernel interface in "From
+ * CUDA to Triton: Triton JIT and autotuning", §六 6.2 (signature of
+ * sparse_submanifold_conv_fwd_masked_implicit_gemm_kernel) fixes V = 27 taps,
+ * a uint32 neighbour table, a row order (sorted_idx) and a contraction over
+ * V * Ci.
+ *
+ * Conventions used by every call below:
+ *  - tap k <-> offset (dx,dy,dz) in {-1,0,1}^3 with k = 9(dx+1) + 3(dy+1) + (dz+1);
+ *    k = 13 is the centre and o_{26-k} = -o_k.
+ *  - nbr[i][k] = j when voxel j sits at coord_i + o_k in the same batch element,
+ *    else VG_NONE; mask[i] bit k is set iff nbr[i][k] != VG_NONE.  A neighbour
+ *    outside the grid is absent (no wrap, no padding).  Row indices are the
+ *    caller's row order.
+ *  - forward:  out[i][co] = bias[co] + sum_k sum_ci W[k][ci][co] * feats[nbr[i][k]][ci]
+ *    input gradient:  dX[j] = sum over (i,k) with nbr[i][k] = j of W_k dY[i]
+ *    weight gradient: dW[k][ci][co] = sum_i f[nbr[i][k]][ci] * dY[i][co];  db = sum_i dY[i]
+ *  - Every pointer argument is a DEVICE pointer (cudaMalloc'd or equivalent),
+ *    row-major and contiguous, owned by the caller; the library allocates no
+ *    memory and keeps no global state.  `stream` is a cudaStream_t (NULL = the
+ *    legacy default stream).  Calls are stream-ordered and asynchronous unless
+ *    stated otherwise.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned as a status code; nothing is written in that case.
+ *  - Accumulation is fp32 on every path; outputs are rounded to the input
+ *    dtype with round-to-nearest-even.
+ *  - N < 2^31 rows.
+ */
+#ifndef VOXEL_GEMM_VG_H
+#define VOXEL_GEMM_VG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VG_API __attribute__((visibility("default")))
+#else
+#define VG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------- */
+#define VG_OK                       0
+#define VG_ERR_INVALID_ARG          1  /* null pointer, bad size, misaligned pointer     */
+#define VG_ERR_COORD_OUT_OF_RANGE   2  /* a coordinate outside [0,B)x[0,X)x[0,Y)x[0,Z)    */
+#define VG_ERR_DUPLICATE_COORD      3  /* two rows with the same (b,x,y,z)               */
+#define VG_ERR_HASH_FULL            4  /* the voxel hash table overflowed                */
+#define VG_ERR_UNSUPPORTED          5  /* channel counts/dtype/flags this build does not run */
+#define VG_ERR_WORKSPACE_TOO_SMALL  6  /* ws_bytes below the matching *_workspace_bytes() */
+#define VG_ERR_CUDA                 7  /* a CUDA runtime call or launch failed           */
+#define VG_ERR_DEVICE_TIMEOUT       8  /* a bounded device-side wait gave up (kernel returned early) */
+
+/* ---- element types ---------------------------------------------------------------- */
+#define VG_F32   0
+#define VG_F16   1
+#define VG_BF16  2
+
+/* ---- flags -------------------------------------------------------------------------- */
+#define VG_KEY32            0x1u   /* force 32-bit hash keys (needs B*X*Y*Z < 2^32)    */
+#define VG_KEY64            0x2u   /* force 64-bit hash keys                            */
+/* Testing aid: size the hash table below N so that the overflow path
+ * (VG_ERR_HASH_FULL) can be exercised from the host. */
+#define VG_TEST_SMALL_HASH  0x100u
+
+#define VG_NONE 0xFFFFFFFFu        /* missing neighbour in nbr                          */
+#define VG_TILE_ROWS 128           /* rows per tile of the sorted order (tile masks)    */
+
+/* Human-readable name of a status code (static string). */
+VG_API const char* vg_strerror(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+VG_API int vg_version(void);
+
+/* ======================================================================================
+ * Neighbour map (hash build, 27-tap probe, valid-tap mask, Morton row order, tile masks)
+ * Follows the page's hashmap_insert_3d_idx_as_val + subm_neighbor_map +
+ * migemm_neighmap_pp steps ("Contribution Tasks — JeffreyXiang/FlexGEMM", §二,
+ * module table rows kernels.cuda.hash and kernels.cuda.spconv; init_hashmap picks
+ * uint32 or uint64 keys by grid volume).  Reading taken: 64-bit keys iff
+ * B*X*Y*Z >= 2^30, unless VG_KEY32/VG_KEY64 forces the width; the map itself is
+ * identical either way.
+ * ====================================================================================== */
+
+/* Bytes of device workspace vg_nbrmap_build needs for these sizes and flags
+ * (0 if the arguments are invalid).  The workspace is the neighbour cache: it
+ * holds the hash table, the sorted row order and the per-tile masks, and must
+ * stay alive and unmodified while convolutions use the map. */
+VG_API size_t vg_nbrmap_workspace_bytes(int64_t N, int B, int X, int Y, int Z, unsigned flags);
+
+/* Build the neighbour map of N voxels.
+ *   coords  [N][4] int32 (b,x,y,z), 16-byte aligned
+ *   ws      workspace of >= vg_nbrmap_workspace_bytes(...) bytes, 256-byte aligned
+ *   nbr     [N][27] uint32 output (original row order), mask [N] uint32 output
+ * Asynchronous: argument errors are returned at once; data-dependent errors
+ * (out-of-range or duplicate coordinates, hash overflow) are recorded on the
+ * device in ws and returned by vg_nbrmap_status().  The convolution calls read
+ * that record on the device and write nothing when the map is bad. */
+VG_API int vg_nbrmap_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z,
+                    unsigned flags, void* ws, size_t ws_bytes,
+                    uint32_t* nbr, uint32_t* mask, void* stream);
+
+/* Synchronises `stream` and returns the data-dependent status of the last build
+ * into ws (VG_OK, VG_ERR_COORD_OUT_OF_RANGE, VG_ERR_DUPLICATE_COORD or
+ * VG_ERR_HASH_FULL; the first in that order if several apply). */
+VG_API int vg_nbrmap_status(const void* ws, void* stream);
+
+/* Device pointers into a built workspace (no device access, no sync):
+ *   sorted_idx [N] uint32 — row r of the Morton (z-order) sequence is voxel sorted_idx[r]
+ *                (the page's sorted_idx; stable sort of (b, interleaved x,y,z) keys)
+ *   tile_mask  [ceil(N/128)] uint32 — OR of mask over sorted rows [128t, 128t+128) */
+VG_API const uint32_t* vg_nbrmap_sorted_idx(const void* ws);
+VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);
+
+/* Host-only description of the build plan (no device access):
+ *   info[0] = 1 if the hash keys are 64-bit, info[1] = significant bits of the
+ *   Morton key, info[2] = radix-sort passes, info[3] = kernels launched by
+ *   vg_nbrmap_build (memsets not counted).  Returns VG_OK or VG_ERR_INVALID_ARG. */
+VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int info[4]);
+
+/* ======================================================================================
+ * Convolution (forward, input gradient, weight/bias gradient)
+ * The masked implicit GEMM of "From CUDA to Triton: Triton JIT and autotuning",
+ * §六 6.2 (kernel arguments input, weight, bias, neighbor, sorted_idx, output;
+ * contraction V * Ci) and its backward ("Contribution Tasks — JeffreyXiang/FlexGEMM",
+ * §二 call flow: the backward reuses the neighbour cache and returns feats.grad
+ * and weight.grad).
+ *   dtype: VG_F32 (fp32 FFMA path), VG_F16 or VG_BF16 (tensor-core path when
+ *          Cin and Cout are multiples of 64, CUDA-core path otherwise).
+ *   Cin and Cout must be multiples of 8 (VG_ERR_UNSUPPORTED otherwise); flags
+ *   must be 0.
+ *   feats [N][Cin], weight [27][Cin][Cout], bias [Cout] (or NULL), out [N][Cout],
+ *   all of `dtype`, 16-byte aligned.
+ *   nbr_ws/nbr/mask: a map built by vg_nbrmap_build for the same N.
+ *   conv_ws: >= vg_conv_workspace_bytes(...) bytes, 256-byte aligned; holds the
+ *   repacked weights, split-K partial sums and a device error record.
+ * ====================================================================================== */
+
+/* Bytes of conv workspace needed by vg_subm_conv3d_fwd/bwd for these sizes. */
+VG_API size_t vg_conv_workspace_bytes(int64_t N, int Cin, int Cout, int dtype, unsigned flags);
+
+/* Host-only description of the convolution plan (no device access):
+ *   info[0] = 1 on the tensor-core path, info[1] = split-K chunks of the weight
+ *   gradient, info[2] = kernels launched by a forward call, info[3] = kernels
+ *   launched by a backward call producing all three gradients (memsets not
+ *   counted).  Returns VG_OK or the status vg_subm_conv3d_fwd would return
+ *   for these sizes. */
+VG_API int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int info[4]);
+
+VG_API int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask, int64_t N,
+                       int dtype, const void* feats, const void* weight, const void* bias,
+                       void* out, int Cin, int Cout, unsigned flags,
+                       void* conv_ws, size_t conv_ws_bytes, void* stream);
+
+/* Backward.  grad_out [N][Cout]; outputs grad_feats [N][Cin], grad_weight
+ * [27][Cin][Cout], grad_bias [Cout]; each output may be NULL to skip it.
+ * grad_weight is reduced over split-K chunks in a fixed order (bitwise
+ * deterministic run to run). */
+VG_API int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask, int64_t N,
+                       int dtype, const void* grad_out, const void* feats, const void* weight,
+                       void* grad_feats, void* grad_weight, void* grad_bias,
+                       int Cin, int Cout, unsigned flags,
+                       void* conv_ws, size_t conv_ws_bytes, void* stream);
+
+/* Synchronises `stream` and returns VG_ERR_DEVICE_TIMEOUT if a kernel of the
+ * most recent vg_subm_conv3d_fwd/bwd call on conv_ws gave up a bounded
+ * device-side wait (its outputs are then incomplete), else VG_OK.  Every
+ * fwd/bwd call clears this record when it starts. */
+VG_API int vg_conv_status(void* conv_ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VOXEL_GEMM_VG_H */

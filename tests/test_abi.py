@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads and exports every symbol include/vg.h declares (CPU only).
+
+Only host-side calls are made here (sizes, strings, argument validation that
+returns before any device work); nothing computes without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from voxel_gemm_gb300 import build, ops
+    build.build()
+    return ops
+
+
+def declared_symbols():
+    syms = set()
+    for name in os.listdir(os.path.join(ROOT, "include")):
+        if name.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", name)).read()
+            syms |= set(re.findall(r"^VG_API\s+[\w\s\*]+?\b(vg_\w+)\s*\(", text, flags=re.M))
+    return syms
+
+
+def test_every_declared_symbol_is_exported(ops):
+    syms = declared_symbols()
+    assert len(syms) >= 11
+    L = ctypes.CDLL(ops.LIB_PATH)
+    for s in sorted(syms):
+        assert hasattr(L, s), s
+
+
+def test_host_only_queries(ops):
+    assert ops.vg_version() >= 100
+    assert ops.vg_strerror(ops.VG_ERR_DUPLICATE_COORD) == "duplicate coordinate"
+    assert ops.vg_strerror(12345) == "unknown status"
+    n32 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, 0)
+    n64 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, ops.VG_KEY64)
+    assert n64 > n32 > 0
+    assert ops.vg_nbrmap_workspace_bytes(-1, 1, 8, 8, 8, 0) == 0
+    assert ops.vg_nbrmap_workspace_bytes(10, 0, 8, 8, 8, 0) == 0
+    assert ops.vg_nbrmap_workspace_bytes(10, 1, 8, 8, 8, ops.VG_KEY32 | ops.VG_KEY64) == 0
+    # 32-bit keys cannot address a 2^32-cell grid
+    assert ops.vg_nbrmap_workspace_bytes(10, 4, 1024, 1024, 1024, ops.VG_KEY32) == 0
+    assert ops.vg_conv_workspace_bytes(1000, 64, 64, ops.VG_F16) > 0
+    assert ops.vg_conv_workspace_bytes(1000, 60, 64, ops.VG_F16) == 0      # Cin % 8 != 0
+    assert ops.vg_conv_workspace_bytes(1000, 64, 64, 7) == 0               # bad dtype
+    assert ops.vg_conv_workspace_bytes(0, 64, 64, ops.VG_BF16) > 0
+
+
+def test_argument_errors_return_before_any_launch(ops):
+    L = ops.lib()
+    P = ctypes.c_void_p
+    # null workspace / coords: rejected on the host
+    st = L.vg_nbrmap_build(None, 10, 1, 8, 8, 8, 0, None, 0, None, None, None)
+    assert st == ops.VG_ERR_INVALID_ARG
+    # misaligned workspace pointer
+    st = L.vg_nbrmap_build(P(16), 10, 1, 8, 8, 8, 0, P(0x1001), 1 << 20, P(64), P(64), None)
+    assert st == ops.VG_ERR_INVALID_ARG
+    # workspace too small
+    need = ops.vg_nbrmap_workspace_bytes(10, 1, 8, 8, 8, 0)
+    st = L.vg_nbrmap_build(P(256), 10, 1, 8, 8, 8, 0, P(0x10000), need - 1, P(256), P(256), None)
+    assert st == ops.VG_ERR_WORKSPACE_TOO_SMALL
+    # conv: unsupported channels, unknown flags
+    st = L.vg_subm_conv3d_fwd(P(256), P(256), P(256), 10, ops.VG_F16, P(256), P(256), None, P(256),
+                              12, 64, 0, P(256), 1 << 20, None)
+    assert st == ops.VG_ERR_UNSUPPORTED
+    st = L.vg_subm_conv3d_fwd(P(256), P(256), P(256), 10, ops.VG_F16, P(256), P(256), None, P(256),
+                              64, 64, 0x80, P(256), 1 << 20, None)
+    assert st == ops.VG_ERR_UNSUPPORTED
+    st = L.vg_subm_conv3d_bwd(P(256), P(256), P(256), 10, ops.VG_F16, P(256), P(256), P(256),
+                              P(256), None, None, 64, 64, 0, P(256), 16, None)
+    assert st == ops.VG_ERR_WORKSPACE_TOO_SMALL
+    assert L.vg_conv_status(None, None) == ops.VG_ERR_INVALID_ARG
+    assert L.vg_nbrmap_status(None, None) == ops.VG_ERR_INVALID_ARG

@@ -1,0 +1,141 @@
+"""GPU forward / input gradient / weight and bias gradient vs the oracle.
+
+Small workloads are compared element by element in full; the large ones on
+seeded samples the oracle computes one by one (output rows x a column subset
+for fwd and dgrad, full-sum dW entries over ci x co column subsets), in the
+same launch configuration the benchmark times.  Bound: relative Frobenius
+error <= 1e-5 (fp32, FFMA) and <= 1e-2 (fp16/bf16 with fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (TOL, coords_of, f64, oracle_dgrad_rows, oracle_fwd_rows, oracle_map,
+                     oracle_wgrad_cols, rel_fro, u32)
+from voxel_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(coords_np, grid, f, W, b, dY, key_flag=0, want=("out", "dX", "dW", "db")):
+    dev = "cuda"
+    c = torch.from_numpy(coords_np).to(dev)
+    N = coords_np.shape[0]
+    m = ops.NbrMap.alloc(N, grid, key_flag).build(c)
+    fd, Wd, dYd = f.to(dev), W.to(dev), dY.to(dev)
+    bd = None if b is None else b.to(dev)
+    Cin, Cout = W.shape[1], W.shape[2]
+    ws = ops.conv_workspace(N, Cin, Cout, f.dtype)
+    res = {}
+    out = torch.empty(N, Cout, dtype=f.dtype, device=dev)
+    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, fd, Wd, bd, out, ws)
+    dX = torch.empty(N, Cin, dtype=f.dtype, device=dev)
+    dW = torch.empty(27, Cin, Cout, dtype=f.dtype, device=dev)
+    db = torch.empty(Cout, dtype=f.dtype, device=dev)
+    ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dYd, fd, Wd, dX, dW, db, ws)
+    assert m.status() == ops.VG_OK
+    assert ops.vg_conv_status(ws) == ops.VG_OK
+    res.update(out=out.cpu(), dX=dX.cpu(), dW=dW.cpu(), db=db.cpu(), nbr=u32(m.nbr))
+    return res
+
+
+def full_check(coords, grid, f, W, b, dY, tol, key_flag=0):
+    nbr_ref, _ = oracle.nbrmap(coords, *grid)
+    r = run_gpu(coords, grid, f, W, b, dY, key_flag)
+    assert np.array_equal(r["nbr"], nbr_ref)
+    out_ref = oracle.fwd(nbr_ref, f64(f), f64(W), None if b is None else f64(b))
+    dX_ref = oracle.dgrad_scatter(nbr_ref, f64(dY), f64(W))
+    dW_ref, db_ref = oracle.wgrad(nbr_ref, f64(f), f64(dY))
+    errs = {"out": rel_fro(f64(r["out"]), out_ref), "dX": rel_fro(f64(r["dX"]), dX_ref),
+            "dW": rel_fro(f64(r["dW"]), dW_ref), "db": rel_fro(f64(r["db"]), db_ref)}
+    for k, e in errs.items():
+        assert e <= tol, (k, e, errs)
+    return errs
+
+
+@pytest.mark.parametrize("name", ["sphere16_c32_f32", "b4_r64_spheres_c64_f16"])
+def test_workload_full(name):
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    full_check(coords, wl.grid, f, W, b, dY, TOL[wl.dtype], wl.key_flag)
+
+
+SAMPLED = ["b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16", "b1_r512_shapes_c512_bf16",
+           "b1_r512_shapes_c1024_bf16", "b1_r1024_shapes_c64_f16"]
+
+
+@pytest.mark.parametrize("name", SAMPLED)
+def test_workload_sampled(name):
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    N = coords.shape[0]
+    nbr_ref, _ = oracle_map(name)
+    f, W, b, dY = synth.make_tensors(wl, N)
+    r = run_gpu(coords, wl.grid, f, W, b, dY, wl.key_flag)
+    assert np.array_equal(r["nbr"], nbr_ref)
+    rng = np.random.default_rng(1234 + wl.seed)
+    rows = np.sort(rng.choice(N, size=min(N, 4096), replace=False))
+    ncol = min(wl.cout, 64)
+    cols_out = np.sort(rng.choice(wl.cout, size=ncol, replace=False))
+    cols_in = np.sort(rng.choice(wl.cin, size=min(wl.cin, 64), replace=False))
+    out_ref = oracle_fwd_rows(nbr_ref, rows, cols_out, f, W, b)
+    e_out = rel_fro(f64(r["out"][rows][:, cols_out]), out_ref)
+    dX_ref = oracle_dgrad_rows(nbr_ref, rows, cols_in, dY, W)
+    e_dx = rel_fro(f64(r["dX"][rows][:, cols_in]), dX_ref)
+    ci = np.sort(rng.choice(wl.cin, size=8, replace=False))
+    co = np.sort(rng.choice(wl.cout, size=8, replace=False))
+    dW_ref, db_ref = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
+    e_dw = rel_fro(f64(r["dW"][:, ci][:, :, co]), dW_ref)
+    e_db = rel_fro(f64(r["db"][co]), db_ref)
+    tol = TOL[wl.dtype]
+    assert max(e_out, e_dx, e_dw, e_db) <= tol, (e_out, e_dx, e_dw, e_db)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("cin,cout", [(64, 64), (64, 128), (128, 64), (192, 64), (40, 24), (8, 8)])
+def test_ragged_and_shapes(dtype, cin, cout):
+    # N not a multiple of the tile, Cin != Cout, both tensor-core-shaped and CUDA-core-shaped channels
+    coords = synth.random_coords(cin * 7 + cout, 1111, 2, 14, 14, 14)
+    wl = synth.Workload("t", 2, 14, 0, ("sphere",), cin, cout, dtype, 9, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    full_check(coords, (2, 14, 14, 14), f, W, b, dY, TOL[dtype])
+
+
+def test_bias_none_and_closed_form():
+    # all-ones features and weights: out[i] = popcount(mask_i) * Cin exactly (small integers)
+    coords = coords_of("b4_r64_spheres_c64_f16")
+    N = coords.shape[0]
+    _, mask_ref = oracle_map("b4_r64_spheres_c64_f16")
+    f = torch.ones(N, 64, dtype=torch.float16)
+    W = torch.ones(27, 64, 64, dtype=torch.float16)
+    r = run_gpu(coords, (4, 64, 64, 64), f, W, None, torch.zeros(N, 64, dtype=torch.float16))
+    pop = np.array([bin(int(x)).count("1") for x in mask_ref], dtype=np.float64)
+    assert np.array_equal(f64(r["out"]), np.repeat(pop[:, None] * 64, 64, axis=1))
+    assert torch.count_nonzero(r["dW"]) == 0 and torch.count_nonzero(r["db"]) == 0
+
+
+def test_wgrad_is_deterministic():
+    name = "b2_r256_shapes_c128_bf16"
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    outs = [run_gpu(coords, wl.grid, f, W, b, dY) for _ in range(3)]
+    for o in outs[1:]:
+        for k in ("out", "dX", "dW", "db"):
+            assert torch.equal(o[k].view(torch.int16), outs[0][k].view(torch.int16)), k
+
+
+def test_empty_input():
+    m = ops.NbrMap.alloc(0, (1, 8, 8, 8)).build(torch.zeros(0, 4, dtype=torch.int32, device="cuda"))
+    ws = ops.conv_workspace(0, 64, 64, torch.bfloat16)
+    f = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.randn(27, 64, 64, device="cuda").bfloat16()
+    out = torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda")
+    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, None, out, ws)
+    dW = torch.full((27, 64, 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    db = torch.full((64,), 3.0, dtype=torch.bfloat16, device="cuda")
+    ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, f, f, W, f, dW, db, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dW) == 0 and torch.count_nonzero(db) == 0

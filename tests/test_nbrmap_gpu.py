@@ -1,0 +1,127 @@
+"""GPU neighbour map vs the oracle: bit-exact nbr and mask on every workload, plus
+the sorted row order, tile masks, key-width equivalence and the error records."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import coords_of, oracle_map, u32
+from voxel_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+
+MAP_WORKLOADS = ["sphere16_c32_f32", "b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16",
+                 "b1_r512_shapes_c256_bf16", "b1_r1024_shapes_c64_f16"]
+
+
+def gpu_map(coords_np, grid, flags=0):
+    c = torch.from_numpy(coords_np).cuda()
+    m = ops.NbrMap.alloc(coords_np.shape[0], grid, flags)
+    m.build(c)
+    st = m.status()
+    return m, st
+
+
+def morton_keys(coords, grid):
+    B, X, Y, Z = grid
+    L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
+    c = coords.astype(np.uint64)
+    key = c[:, 0] << np.uint64(3 * L)
+    for m in range(L):
+        for col, pos in ((1, 2), (2, 1), (3, 0)):
+            key |= ((c[:, col] >> np.uint64(m)) & np.uint64(1)) << np.uint64(3 * m + pos)
+    return key
+
+
+@pytest.mark.parametrize("name", MAP_WORKLOADS)
+def test_nbrmap_bit_exact(name):
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    nbr_ref, mask_ref = oracle_map(name)
+    m, st = gpu_map(coords, wl.grid, wl.key_flag)
+    assert st == ops.VG_OK
+    assert np.array_equal(u32(m.nbr), nbr_ref)
+    assert np.array_equal(u32(m.mask), mask_ref)
+    # sorted order: a permutation, stable-sorted by the Morton key
+    order = u32(m.sorted_idx()).astype(np.int64)
+    n = coords.shape[0]
+    assert np.array_equal(np.sort(order), np.arange(n))
+    keys = morton_keys(coords, wl.grid)[order]
+    assert np.all(keys[1:] >= keys[:-1])
+    ties = keys[1:] == keys[:-1]
+    assert np.all(order[1:][ties] > order[:-1][ties])
+    # tile masks: OR of the valid-tap masks of each block of 128 sorted rows
+    T = (n + 127) // 128
+    pad = np.zeros(T * 128, dtype=np.uint32)
+    pad[:n] = mask_ref[order]
+    want = np.bitwise_or.reduce(pad.reshape(T, 128), axis=1)
+    assert np.array_equal(u32(m.tile_mask()), want)
+
+
+def test_key_width_does_not_change_the_map():
+    name = "b2_r256_shapes_c128_bf16"
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    m32, s32 = gpu_map(coords, wl.grid, ops.VG_KEY32)
+    m64, s64 = gpu_map(coords, wl.grid, ops.VG_KEY64)
+    assert s32 == s64 == ops.VG_OK
+    assert torch.equal(m32.nbr, m64.nbr) and torch.equal(m32.mask, m64.mask)
+    assert torch.equal(m32.sorted_idx(), m64.sorted_idx())
+
+
+def test_large_grid_forces_64bit_keys_and_matches():
+    # B*X*Y*Z = 2^33 cannot use 32-bit keys; coordinates near the far corner
+    coords = synth.random_coords(3, 3000, 8, 1024, 1024, 1024)
+    coords[:, 1:] = np.minimum(coords[:, 1:] // 64 + 1000, 1023)  # cluster them
+    keys = ((coords[:, 0].astype(np.int64) * 1024 + coords[:, 1]) * 1024 + coords[:, 2]) * 1024 + coords[:, 3]
+    _, first = np.unique(keys, return_index=True)
+    coords = coords[np.sort(first)]
+    nbr_ref, mask_ref = oracle.nbrmap(coords, 8, 1024, 1024, 1024)
+    m, st = gpu_map(coords, (8, 1024, 1024, 1024))
+    assert st == ops.VG_OK
+    assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 4097, 5000])
+def test_ragged_sizes(n):
+    coords = synth.random_coords(n, n, 2, 12, 12, 12)
+    nbr_ref, mask_ref = oracle.nbrmap(coords, 2, 12, 12, 12)
+    m, st = gpu_map(coords, (2, 12, 12, 12))
+    assert st == ops.VG_OK
+    assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
+
+
+def test_empty_map():
+    m = ops.NbrMap.alloc(0, (1, 8, 8, 8))
+    m.build(torch.zeros(0, 4, dtype=torch.int32, device="cuda"))
+    assert m.status() == ops.VG_OK
+
+
+def test_duplicate_and_out_of_range_are_reported():
+    c = np.array([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=np.int32)
+    _, st = gpu_map(c, (1, 8, 8, 8))
+    assert st == ops.VG_ERR_DUPLICATE_COORD
+    for bad in ([1, 0, 0, 0], [0, 8, 0, 0], [0, 0, -1, 0], [0, 0, 0, 9]):
+        c = np.array([[0, 1, 1, 1], bad], dtype=np.int32)
+        _, st = gpu_map(c, (1, 8, 8, 8))
+        assert st == ops.VG_ERR_COORD_OUT_OF_RANGE
+
+
+def test_hash_overflow_is_reported():
+    coords = synth.random_coords(7, 4000, 1, 32, 32, 32)
+    _, st = gpu_map(coords, (1, 32, 32, 32), ops.VG_TEST_SMALL_HASH)
+    assert st == ops.VG_ERR_HASH_FULL
+
+
+def test_bad_map_blocks_the_convolution():
+    # a map with a duplicate must make the convolution write nothing
+    c = np.array([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=np.int32)
+    m, st = gpu_map(c, (1, 8, 8, 8))
+    assert st == ops.VG_ERR_DUPLICATE_COORD
+    f = torch.randn(3, 16, device="cuda")
+    W = torch.randn(27, 16, 16, device="cuda")
+    out = torch.full((3, 16), 7.0, device="cuda")
+    ws = ops.conv_workspace(3, 16, 16, torch.float32)
+    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, None, out, ws)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)

@@ -1,0 +1,58 @@
+// Shared device/host helpers of the GPU library (not used by the CPU oracle).
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "../../include/vg.h"
+
+namespace vg {
+
+constexpr uint32_t kNone = VG_NONE;
+constexpr int kTaps = 27;
+constexpr int kTileRows = VG_TILE_ROWS;
+
+// Device-side error record bits (nbr-map header word 0 and the conv workspace word).
+constexpr uint32_t kErrRange = 1u;
+constexpr uint32_t kErrDup = 2u;
+constexpr uint32_t kErrFull = 4u;
+constexpr uint32_t kErrTimeout = 8u;
+
+// Bound on mbarrier polls before a kernel gives up (~seconds at GB300 clocks).
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// -------- element conversion --------
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// -------- neighbour-map workspace layout (byte offsets; computed identically on host) --------
+struct NbrLayout {
+    int64_t n = 0;
+    int key64 = 0;          // hash keys are 64-bit
+    int sort64 = 0;         // Morton sort keys are 64-bit
+    int sort_bits = 0;      // significant bits of the Morton key
+    int cap_log2 = 0;       // hash capacity = 2^cap_log2
+    int64_t num_tiles = 0;  // ceil(n / 128)
+    int64_t sort_blocks = 0;
+    size_t off_hdr = 0, off_sorted = 0, off_tmask = 0, off_hkeys = 0, off_hvals = 0;
+    size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, total = 0;
+};
+
+constexpr int kSortItems = 16;                        // keys per thread in the radix sort
+constexpr int kSortThreads = 256;
+constexpr int kSortTile = kSortItems * kSortThreads;  // keys per sort block
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+
+}  // namespace vg

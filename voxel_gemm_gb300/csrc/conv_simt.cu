@@ -1,0 +1,306 @@
+// CUDA-core (FFMA) masked implicit GEMM: the fp32 path, and the path for
+// 16-bit channel counts the tensor-core kernel does not tile (not multiples of 64).
+//
+// Forward / input gradient: "From CUDA to Triton: Triton JIT and autotuning",
+// §六 6.2 (masked implicit GEMM over sorted rows, contraction V * Ci, taps
+// that are empty for the whole tile are skipped).  Weight gradient: the
+// split-K backward ("Contribution Tasks — JeffreyXiang/FlexGEMM", §二 key
+// types table: sparse_submanifold_conv_bwd_masked_implicit_gemm_splitk).
+#include "common.cuh"
+#include "internal.h"
+
+namespace vg {
+
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 32;
+
+// Tile of BM sorted rows x BN output columns; 256 threads, 4x4 outputs each.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_gather_gemm_simt(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
+                   const uint32_t* __restrict__ nbr_status, int64_t n,
+                   const T* __restrict__ A, int Kdim, const T* __restrict__ W, int flip,
+                   int64_t sK, int64_t sN, const T* __restrict__ bias, T* __restrict__ out,
+                   int Ndim) {
+    __shared__ uint32_t s_rows[BM];
+    __shared__ uint32_t s_nbr[BM][kTaps];
+    __shared__ float As[BK][BM + 4];
+    __shared__ float Bs[BK][BN + 4];
+    __shared__ uint32_t s_tmask;
+    if (*nbr_status) return;
+    const int tid = threadIdx.x;
+    const int64_t row0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+    if (tid < BM) {
+        const int64_t r = row0 + tid;
+        s_rows[tid] = r < n ? sorted_idx[r] : kNone;
+    }
+    if (tid == 0) s_tmask = 0;
+    __syncthreads();
+    for (int idx = tid; idx < BM * kTaps; idx += 256) {
+        const int rr = idx / kTaps, k = idx - rr * kTaps;
+        const uint32_t v = s_rows[rr];
+        s_nbr[rr][k] = v != kNone ? nbr[(int64_t)v * kTaps + k] : kNone;
+    }
+    __syncthreads();
+    if (tid < BM) {
+        uint32_t m = 0;
+        for (int k = 0; k < kTaps; ++k) m |= (s_nbr[tid][k] != kNone ? 1u : 0u) << k;
+        m = __reduce_or_sync(0xffffffffu, m);
+        if ((tid & 31) == 0) atomicOr(&s_tmask, m);
+    }
+    __syncthreads();
+    const uint32_t tmask = s_tmask;
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    const int64_t tap_stride = (int64_t)Kdim * Ndim;
+    for (int k = 0; k < kTaps; ++k) {
+        if (!((tmask >> k) & 1u)) continue;
+        const T* Wk = W + (int64_t)(flip ? 26 - k : k) * tap_stride;
+        for (int kk0 = 0; kk0 < Kdim; kk0 += BK) {
+            {
+                const int rr = tid >> 2, c0 = (tid & 3) * 8;
+                const uint32_t j = s_nbr[rr][k];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kk = kk0 + c0 + e;
+                    As[c0 + e][rr] = (j != kNone && kk < Kdim) ? to_f32(A[(int64_t)j * Kdim + kk]) : 0.f;
+                }
+            }
+            {
+                const int kr = tid >> 3, c0 = (tid & 7) * 8;
+                const int kk = kk0 + kr;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int nn = n0 + c0 + e;
+                    Bs[kr][c0 + e] = (kk < Kdim && nn < Ndim) ? to_f32(Wk[kk * sK + nn * sN]) : 0.f;
+                }
+            }
+            __syncthreads();
+#pragma unroll 8
+            for (int kk = 0; kk < BK; ++kk) {
+                float a[4], b[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+            }
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = s_rows[ty * 4 + i];
+        if (v == kNone) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int nn = n0 + tx * 4 + j;
+            if (nn < Ndim) {
+                const float b = bias ? to_f32(bias[nn]) : 0.f;
+                out[(int64_t)v * Ndim + nn] = from_f32<T>(acc[i][j] + b);
+            }
+        }
+    }
+}
+
+constexpr int WR = 32;  // rows per step of the weight-gradient kernel
+
+// Partial dW for (tap k, ci block, co block, row chunk s) -> partial[s][k][ci][co].
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_wgrad_simt(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
+             const uint32_t* __restrict__ nbr_status, int64_t n, const T* __restrict__ f,
+             const T* __restrict__ dy, int Cin, int Cout, int64_t rows_per_chunk,
+             float* __restrict__ partial) {
+    __shared__ float Fs[WR][BM + 4];
+    __shared__ float Gs[WR][BN + 4];
+    __shared__ uint32_t s_i[WR], s_j[WR];
+    if (*nbr_status) return;
+    const int tid = threadIdx.x;
+    const int co0 = blockIdx.x * BN, ci0 = blockIdx.y * BM;
+    const int k = blockIdx.z % kTaps;
+    const int s = blockIdx.z / kTaps;
+    const int64_t rb = (int64_t)s * rows_per_chunk;
+    const int64_t re = min(n, rb + rows_per_chunk);
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int64_t r0 = rb; r0 < re; r0 += WR) {
+        if (tid < WR) {
+            const int64_t r = r0 + tid;
+            const uint32_t v = r < re ? sorted_idx[r] : kNone;
+            s_i[tid] = v;
+            s_j[tid] = v != kNone ? nbr[(int64_t)v * kTaps + k] : kNone;
+        }
+        __syncthreads();
+        const int any = __syncthreads_or(tid < WR && s_j[tid] != kNone);
+        if (!any) continue;
+        {
+            const int rr = tid >> 3, c0 = (tid & 7) * 8;
+            const uint32_t j = s_j[rr], i = s_i[rr];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int ci = ci0 + c0 + e, co = co0 + c0 + e;
+                Fs[rr][c0 + e] = (j != kNone && ci < Cin) ? to_f32(f[(int64_t)j * Cin + ci]) : 0.f;
+                Gs[rr][c0 + e] = (j != kNone && co < Cout) ? to_f32(dy[(int64_t)i * Cout + co]) : 0.f;
+            }
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int rr = 0; rr < WR; ++rr) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = Fs[rr][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Gs[rr][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    float* P = partial + ((int64_t)s * kTaps + k) * Cin * Cout;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int ci = ci0 + ty * 4 + i;
+        if (ci >= Cin) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int co = co0 + tx * 4 + j;
+            if (co < Cout) P[(int64_t)ci * Cout + co] = acc[i][j];
+        }
+    }
+}
+
+}  // namespace
+
+// Fixed-order sum of split-K partials (deterministic), then round to T.
+template <typename T>
+__global__ void k_reduce_splits(const float* __restrict__ partial, int splits, int64_t total,
+                                T* __restrict__ out, const uint32_t* __restrict__ nbr_status) {
+    if (*nbr_status) return;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    float s = 0.f;
+    for (int p = 0; p < splits; ++p) s += partial[(int64_t)p * total + i];
+    out[i] = from_f32<T>(s);
+}
+
+// db partial sums over row chunks (original row order), one thread per column.
+template <typename T>
+__global__ void k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows_per_chunk,
+                                float* __restrict__ partial_db, const uint32_t* __restrict__ nbr_status) {
+    if (*nbr_status) return;
+    const int co = blockIdx.x * blockDim.x + threadIdx.x;
+    const int s = blockIdx.y;
+    if (co >= Cout) return;
+    const int64_t rb = (int64_t)s * rows_per_chunk, re = min(n, rb + rows_per_chunk);
+    float acc = 0.f;
+    for (int64_t r = rb; r < re; ++r) acc += to_f32(dy[r * Cout + co]);
+    partial_db[(int64_t)s * Cout + co] = acc;
+}
+
+template <typename T>
+static int launch_gather(const GatherPass& p, cudaStream_t s) {
+    const dim3 grid((unsigned)((p.n + BM - 1) / BM), (unsigned)((p.Ndim + BN - 1) / BN));
+    // W offsets: fwd  W[k][kk][n]  -> sK = Cout, sN = 1
+    //            dgrad W[26-k][n][kk] -> sK = 1,    sN = Cout
+    const int64_t sK = p.dgrad ? 1 : p.Cout;
+    const int64_t sN = p.dgrad ? p.Cout : 1;
+    k_gather_gemm_simt<T><<<grid, 256, 0, s>>>(p.sorted_idx, p.nbr, p.nbr_status, p.n,
+                                               static_cast<const T*>(p.A), p.Kdim,
+                                               static_cast<const T*>(p.W), p.dgrad, sK, sN,
+                                               static_cast<const T*>(p.bias), static_cast<T*>(p.out),
+                                               p.Ndim);
+    return VG_OK;
+}
+
+int simt_gather_pass(const GatherPass& p, cudaStream_t s) {
+    if (p.n == 0) return VG_OK;
+    switch (p.dtype) {
+        case VG_F32: return launch_gather<float>(p, s);
+        case VG_F16: return launch_gather<__half>(p, s);
+        case VG_BF16: return launch_gather<__nv_bfloat16>(p, s);
+    }
+    return VG_ERR_INVALID_ARG;
+}
+
+int simt_wgrad_splits(int64_t n, int Cin, int Cout) {
+    const int64_t tiles = (int64_t)kTaps * ((Cin + BM - 1) / BM) * ((Cout + BN - 1) / BN);
+    int64_t s = (4 * 152 + tiles - 1) / tiles;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, (n + 1023) / 1024));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
+}
+
+template <typename T>
+static int launch_wgrad(const WgradPass& p, cudaStream_t s) {
+    const int S = p.splits;
+    const int64_t rpc = ((p.n + S - 1) / S + WR - 1) / WR * WR;
+    const int64_t total = (int64_t)kTaps * p.Cin * p.Cout;
+    if (p.dW) {
+        const dim3 grid((unsigned)((p.Cout + BN - 1) / BN), (unsigned)((p.Cin + BM - 1) / BM),
+                        (unsigned)(kTaps * S));
+        k_wgrad_simt<T><<<grid, 256, 0, s>>>(p.sorted_idx, p.nbr, p.nbr_status, p.n,
+                                             static_cast<const T*>(p.f), static_cast<const T*>(p.dy),
+                                             p.Cin, p.Cout, rpc, p.partial);
+        launch_reduce_splits(p.partial, S, total, p.dW, p.dtype, p.nbr_status, s);
+    }
+    if (p.db) launch_dbias(p.dy, p.n, p.Cout, S, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    return VG_OK;
+}
+
+int simt_wgrad(const WgradPass& p, cudaStream_t s) {
+    if (p.n == 0) return VG_OK;  // zero-fill of empty outputs is done by the caller
+    switch (p.dtype) {
+        case VG_F32: return launch_wgrad<float>(p, s);
+        case VG_F16: return launch_wgrad<__half>(p, s);
+        case VG_BF16: return launch_wgrad<__nv_bfloat16>(p, s);
+    }
+    return VG_ERR_INVALID_ARG;
+}
+
+template <typename T>
+static void reduce_t(const float* partial, int splits, int64_t total, void* out,
+                     const uint32_t* nbr_status, cudaStream_t s) {
+    k_reduce_splits<T><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+        partial, splits, total, static_cast<T*>(out), nbr_status);
+}
+
+void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
+                          const uint32_t* nbr_status, cudaStream_t s) {
+    if (dtype == VG_F32) reduce_t<float>(partial, splits, total, out, nbr_status, s);
+    else if (dtype == VG_F16) reduce_t<__half>(partial, splits, total, out, nbr_status, s);
+    else reduce_t<__nv_bfloat16>(partial, splits, total, out, nbr_status, s);
+}
+
+template <typename T>
+static void dbias_t(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+                    const uint32_t* nbr_status, cudaStream_t s) {
+    const int64_t rpc = (n + splits - 1) / splits;
+    const dim3 grid((unsigned)((Cout + 127) / 128), (unsigned)splits);
+    k_dbias_partial<T><<<grid, 128, 0, s>>>(static_cast<const T*>(dy), n, Cout, rpc, partial_db,
+                                           nbr_status);
+    reduce_t<T>(partial_db, splits, Cout, db, nbr_status, s);
+}
+
+void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+                  int dtype, const uint32_t* nbr_status, cudaStream_t s) {
+    if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
+    else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
+    else dbias_t<__nv_bfloat16>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
+}
+
+}  // namespace vg

@@ -1,0 +1,86 @@
+// Internal (C++ linkage) entry points shared by the library's translation units.
+#pragma once
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vg {
+
+struct NbrLayout;
+
+int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout* L);
+int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
+              void* ws, size_t ws_bytes, uint32_t* nbr, uint32_t* mask, cudaStream_t s);
+int nbr_status(const void* ws, cudaStream_t s);
+
+// Byte offset of sorted_idx / tile masks inside a neighbour-map workspace.
+constexpr size_t kSortedIdxOffset = 256;
+inline size_t tile_mask_offset(int64_t N) { return 256 + ((4 * (size_t)N + 255) / 256) * 256; }
+
+// ---- convolution passes (all asynchronous on stream s) ----
+// One "gather GEMM" pass over the sorted rows:
+//   out[v][n] = bias[n] + sum_k sum_kk A[nbr[v][k]][kk] * Wk(k, kk, n)
+// fwd:   A = feats (Kdim = Cin),  Ndim = Cout, Wk(k,kk,n) = W[k][kk][n]
+// dgrad: A = dY    (Kdim = Cout), Ndim = Cin,  Wk(k,kk,n) = W[26-k][n][kk]
+struct GatherPass {
+    const uint32_t* sorted_idx;
+    const uint32_t* tile_mask;   // per 128 sorted rows
+    const uint32_t* nbr;
+    const uint32_t* nbr_status;  // device word; non-zero = bad map, write nothing
+    int64_t n;
+    const void* A;
+    int Kdim;
+    const void* W;               // user weight [27][Cin][Cout]
+    int Cin, Cout;
+    int dgrad;                   // 0 = forward, 1 = input gradient
+    const void* bias;            // may be null
+    void* out;
+    int Ndim;
+    int dtype;
+    uint32_t* err;               // conv workspace error word
+};
+
+int simt_gather_pass(const GatherPass& p, cudaStream_t s);
+
+struct WgradPass {
+    const uint32_t* sorted_idx;
+    const uint32_t* nbr;
+    const uint32_t* mask;
+    const uint32_t* nbr_status;
+    int64_t n;
+    const void* f;
+    const void* dy;
+    int Cin, Cout, dtype;
+    void* dW;      // may be null
+    void* db;      // may be null
+    float* partial;     // [S][27][Cin][Cout]
+    float* partial_db;  // [S][Cout]
+    int splits;
+    uint32_t* err;
+};
+
+int simt_wgrad_splits(int64_t n, int Cin, int Cout);
+int simt_wgrad(const WgradPass& p, cudaStream_t s);
+
+// Deterministic fixed-order sum of split-K partials [splits][total] into out (dtype).
+void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
+                          const uint32_t* nbr_status, cudaStream_t s);
+// db = column sums of dy over `splits` row chunks, reduced in a fixed order.
+void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+                  int dtype, const uint32_t* nbr_status, cudaStream_t s);
+
+// ---- tensor-core (tcgen05) path, 16-bit types ----
+int tc_supported(int dtype, int Cin, int Cout);
+int tc_wgrad_splits(int64_t n, int Cin, int Cout);
+size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim);
+// Repack W into the swizzled shared-memory image of the B operand
+// (dgrad = 0: B_k = W_k^T, K = Cin;  dgrad = 1: B_k = W_{26-k}, K = Cout).
+int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void* packed,
+                    const uint32_t* nbr_status, cudaStream_t s);
+int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
+int tc_wgrad(const WgradPass& p, cudaStream_t s);
+int tc_fwd_launches();   // kernels per forward call on the tensor-core path
+int tc_bwd_launches();   // kernels per full backward call on the tensor-core path
+
+}  // namespace vg
