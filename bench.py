@@ -267,6 +267,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "voxels/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * (nplan["launches"] + cplan["launches_fwd"] + cplan["launches_bwd"]),
+        "gpu_launches_per_step": {"nbrmap": nplan["launches"], "fwd": cplan["launches_fwd"],
+                                  "bwd": cplan["launches_bwd"]},
         "path": {"tensor_core": bool(cplan["tensor_core"]), "wgrad_splits": splits,
                  "hash_keys": 64 if nplan["key64"] else 32, "sort_passes": nplan["sort_passes"]},
         "clocks": clocks,
@@ -276,9 +278,10 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ oracle arm (CPU)
-def oracle_sample(wl, coords_np, budget_rows, seed=0):
+def oracle_sample(wl, coords_np, budget_rows, seed=0, min_seconds=5.0):
     """Time the oracle on a bounded sample of the workload: the full neighbour map
-    (scaled per voxel) and fwd + dgrad + wgrad over `budget_rows` sampled rows."""
+    (scaled per voxel) and fwd + dgrad + wgrad over sampled rows, repeated over
+    fresh row samples until at least `min_seconds` of conv work has run."""
     import numpy as np
     import oracle
     N = coords_np.shape[0]
@@ -287,24 +290,27 @@ def oracle_sample(wl, coords_np, budget_rows, seed=0):
     t_map = time.perf_counter() - t0
     rng = np.random.default_rng(seed)
     R = min(N, budget_rows)
-    rows = np.sort(rng.choice(N, size=R, replace=False))
-    sub = nbr[rows]
-    valid = sub != oracle.NONE
-    used = np.unique(sub[valid]).astype(np.int64)
-    remap = np.full(sub.shape, oracle.NONE, dtype=np.uint32)
-    remap[valid] = np.searchsorted(used, sub[valid].astype(np.int64)).astype(np.uint32)
-    f = rng.standard_normal((used.size, wl.cin))
-    W = rng.standard_normal((27, wl.cin, wl.cout)) * 0.05
-    b = rng.standard_normal(wl.cout)
-    g_used = rng.standard_normal((used.size, wl.cout))
-    g_rows = rng.standard_normal((R, wl.cout))
-    t1 = time.perf_counter()
-    oracle.fwd(remap, f, W, b)
-    oracle.dgrad_rows(remap, g_used, W)
-    oracle.wgrad(remap, f, g_rows)
-    t_conv = time.perf_counter() - t1
-    per_voxel = t_map / N + t_conv / R
-    return 1.0 / per_voxel, {"rows": R, "t_map_s": t_map, "t_conv_s": t_conv}
+    rows_done, t_conv = 0, 0.0
+    while t_conv < min_seconds or rows_done == 0:
+        rows = np.sort(rng.choice(N, size=R, replace=False))
+        sub = nbr[rows]
+        valid = sub != oracle.NONE
+        used = np.unique(sub[valid]).astype(np.int64)
+        remap = np.full(sub.shape, oracle.NONE, dtype=np.uint32)
+        remap[valid] = np.searchsorted(used, sub[valid].astype(np.int64)).astype(np.uint32)
+        f = rng.standard_normal((used.size, wl.cin))
+        W = rng.standard_normal((27, wl.cin, wl.cout)) * 0.05
+        b = rng.standard_normal(wl.cout)
+        g_used = rng.standard_normal((used.size, wl.cout))
+        g_rows = rng.standard_normal((R, wl.cout))
+        t1 = time.perf_counter()
+        oracle.fwd(remap, f, W, b)
+        oracle.dgrad_rows(remap, g_used, W)
+        oracle.wgrad(remap, f, g_rows)
+        t_conv += time.perf_counter() - t1
+        rows_done += R
+    per_voxel = t_map / N + t_conv / rows_done
+    return 1.0 / per_voxel, {"rows": rows_done, "t_map_s": t_map, "t_conv_s": t_conv}
 
 
 def run_reference(args):
@@ -314,11 +320,11 @@ def run_reference(args):
     coords_np = synth.make_coords(wl)
     budget = rows_budget(wl)
     for _ in range(args.warmup):
-        oracle_sample(wl, coords_np, max(64, budget // 8))
+        oracle_sample(wl, coords_np, max(64, budget // 8), min_seconds=0.0)
     vals = []
     t0 = time.perf_counter()
     for k in range(args.steps):
-        v, _ = oracle_sample(wl, coords_np, budget, seed=k)
+        v, _ = oracle_sample(wl, coords_np, budget, seed=k, min_seconds=2.0)
         vals.append(v)
     wall = time.perf_counter() - t0
     value = statistics.median(vals)
@@ -346,7 +352,7 @@ def rows_budget(wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -22,15 +22,18 @@ def gpu_map(coords_np, grid, flags=0):
     return m, st
 
 
-def morton_keys(coords, grid):
+def order_keys(coords, mask, grid):
+    """The documented sort key: 128^3 Morton blocks, then the tap mask, then Morton order."""
     B, X, Y, Z = grid
     L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
     c = coords.astype(np.uint64)
-    key = c[:, 0] << np.uint64(3 * L)
-    for m in range(L):
+    m = c[:, 0] << np.uint64(3 * L)
+    for b in range(L):
         for col, pos in ((1, 2), (2, 1), (3, 0)):
-            key |= ((c[:, col] >> np.uint64(m)) & np.uint64(1)) << np.uint64(3 * m + pos)
-    return key
+            m |= ((c[:, col] >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b + pos)
+    F = np.uint64(min(3 * L, 21))
+    fine = m & ((np.uint64(1) << F) - np.uint64(1))
+    return ((m >> F) << (np.uint64(27) + F)) | (mask.astype(np.uint64) << F) | fine
 
 
 @pytest.mark.parametrize("name", MAP_WORKLOADS)
@@ -46,7 +49,7 @@ def test_nbrmap_bit_exact(name):
     order = u32(m.sorted_idx()).astype(np.int64)
     n = coords.shape[0]
     assert np.array_equal(np.sort(order), np.arange(n))
-    keys = morton_keys(coords, wl.grid)[order]
+    keys = order_keys(coords, mask_ref, wl.grid)[order]
     assert np.all(keys[1:] >= keys[:-1])
     ties = keys[1:] == keys[:-1]
     assert np.all(order[1:][ties] > order[:-1][ties])

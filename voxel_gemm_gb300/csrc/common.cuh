@@ -54,5 +54,6 @@ constexpr int kSortThreads = 256;
 constexpr int kSortTile = kSortItems * kSortThreads;  // keys per sort block
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
+constexpr int kFineOrderBits = 21;                    // fine Morton bits below the tap mask (128^3 blocks)
 
 }  // namespace vg

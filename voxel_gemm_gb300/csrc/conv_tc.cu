@@ -1,14 +1,396 @@
-// Tensor-core (tcgen05 / TMEM) masked implicit GEMM — placeholder until the kernel lands.
+// Tensor-core (tcgen05 / TMEM) masked implicit GEMM for 16-bit features:
+// the forward pass and the input-gradient pass over Morton-sorted row tiles.
+//
+// Method: "From CUDA to Triton: Triton JIT and autotuning", §六 6.2 — the
+// masked implicit GEMM kernel takes (input, weight, bias, neighbor,
+// sorted_idx, output), gathers input rows per tap and contracts over V * Ci,
+// skipping taps no row of the tile uses.  The backward reuses the same
+// neighbour cache ("Contribution Tasks — JeffreyXiang/FlexGEMM", §二 call flow).
+//
+// GB300 design (one CTA per SM, persistent over (128-row tile, N block) units):
+//   warps 0-3  gather: per tap and 64-channel K block, 128 rows x 128 B of the
+//              feature matrix via 16-byte cp.async with zero fill for missing
+//              neighbours, written in the 128-byte-swizzled K-major layout;
+//              thread 0 also bulk-copies the prepacked weight tile (TMA engine).
+//   warp 4     TMEM allocation and the single MMA-issuing thread:
+//              tcgen05.mma M=128, N=BN, K=16, fp32 accumulators in TMEM,
+//              two accumulator buffers so the epilogue overlaps the next tile.
+//   warps 5-8  epilogue: tcgen05.ld, + bias, round to fp16/bf16, scatter rows
+//              back to the caller's order through sorted_idx.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace vg {
-int tc_supported(int, int, int) { return 0; }
-int tc_wgrad_splits(int64_t, int, int) { return 1; }
-size_t tc_packed_weight_bytes(int, int, int) { return 0; }
-int tc_pack_weights(const void*, int, int, int, int, void*, const uint32_t*, cudaStream_t) { return VG_ERR_UNSUPPORTED; }
-int tc_gather_pass(const GatherPass&, const void*, cudaStream_t) { return VG_ERR_UNSUPPORTED; }
-int tc_wgrad(const WgradPass&, cudaStream_t) { return VG_ERR_UNSUPPORTED; }
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 288;          // 9 warps
+constexpr int kBM = 128;               // rows per tile (MMA M)
+constexpr int kBK = 64;                // 16-bit elements per K block (128 bytes)
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+
+int choose_bn(int ndim) {
+    if (ndim % 256 == 0) return 256;
+    if (ndim % 128 == 0) return 128;
+    return 64;
+}
+
+template <int BN>
+struct Cfg {
+    static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);  // pipeline stages
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kTmemCols = 2 * BN;                         // two accumulators
+    static constexpr size_t kSmemA = (size_t)S * kABytes;
+    static constexpr size_t kSmemB = (size_t)S * kBBytes;
+    static constexpr size_t kNbrBytes = (size_t)kBM * kTaps * 4;
+    static constexpr size_t kRowsBytes = (size_t)kBM * 4;
+    static constexpr int kNumBars = 2 * S + 5;                       // full, empty, tfull x2, tempty x2, done
+    static constexpr size_t kSmem = 1024 + kSmemA + kSmemB + kNbrBytes + kRowsBytes + 8 * kNumBars + 16;
+};
+
+struct TcArgs {
+    const uint32_t* sorted_idx;
+    const uint32_t* tile_mask;
+    const uint32_t* nbr;
+    const uint32_t* nbr_status;
+    int64_t n;
+    int64_t num_tiles;
+    const uint16_t* A;    // [n][Kdim] 16-bit
+    int Kdim;
+    const uint8_t* Bimg;  // packed weight tiles
+    const uint16_t* bias; // [Ndim] or null
+    uint16_t* out;        // [n][Ndim]
+    int Ndim;
+    uint32_t* err;
+};
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+template <bool BF16>
+__device__ __forceinline__ float bits_to_f32(uint16_t b) {
+    if constexpr (BF16) return __uint_as_float((uint32_t)b << 16);
+    else return __half2float(__ushort_as_half(b));
+}
+
+template <int BN, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
+    using C = Cfg<BN>;
+    constexpr int S = C::S;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::kSmemA;
+    uint32_t* s_nbr = reinterpret_cast<uint32_t*>(sB + C::kSmemB);
+    uint32_t* s_rows = s_nbr + kBM * kTaps;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_rows + kBM);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile uint32_t* s_abort = s_tmem + 1;
+
+    if (*a.nbr_status) return;  // bad neighbour map: write nothing (uniform over the block)
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+    const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full0 + 8 * i, 128 + 1);  // 128 gather threads + the weight-tile expect_tx
+            mbar_init(empty0 + 8 * i, 1);       // one tcgen05.commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull0 + 8 * i, 1);
+            mbar_init(tempty0 + 8 * i, 4);      // one arrive per epilogue warp
+        }
+        mbar_init(done_bar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int NB = a.Ndim / BN;
+    const int KB = a.Kdim / kBK;
+    const int64_t units = a.num_tiles * NB;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ gather producer
+        // Every gather thread runs the same unit loop and the same named barriers;
+        // after a failed wait a thread only skips work, so no barrier is left short.
+        const int p = threadIdx.x;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+            const int64_t t = u / NB;
+            const int nb = (int)(u - t * NB);
+            named_bar_sync(1, 128);  // all gather threads are done reading s_nbr of the previous unit
+            {
+                const int64_t r = t * kBM + p;
+                s_rows[p] = r < a.n ? a.sorted_idx[r] : kNone;
+            }
+            named_bar_sync(1, 128);
+            for (int idx = p; idx < kBM * kTaps; idx += 128) {
+                const int rr = idx / kTaps, k = idx - rr * kTaps;
+                const uint32_t v = s_rows[rr];
+                s_nbr[idx] = v != kNone ? a.nbr[(int64_t)v * kTaps + k] : kNone;
+            }
+            named_bar_sync(1, 128);
+            if (!ok) continue;
+            const uint32_t tm = a.tile_mask[t];
+            for (int k = 0; k < kTaps && ok; ++k) {
+                if (!((tm >> k) & 1u)) continue;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t stage = it % S, ph = (it / S) & 1u;
+                    if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
+                        ok = false;
+                        *s_abort = 1;
+                        break;
+                    }
+                    if (p == 0) {
+                        mbar_arrive_expect_tx(full0 + 8 * stage, C::kBBytes);
+                        const uint8_t* src = a.Bimg + (((int64_t)nb * kTaps + k) * KB + kb) * C::kBBytes;
+                        bulk_g2s(smem_u32(sB + stage * C::kBBytes), src, C::kBBytes, full0 + 8 * stage);
+                    }
+                    const uint32_t a_base = smem_u32(sA + stage * kABytes);
+                    const int ch = p & 7;
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) {
+                        const int row = i2 * 16 + (p >> 3);
+                        const uint32_t j = s_nbr[row * kTaps + k];
+                        const uint16_t* src = a.A + (int64_t)(j != kNone ? j : 0u) * a.Kdim + kb * kBK + ch * 8;
+                        cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src, j != kNone ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    cp_async_wait<S - 1>();
+                    if (it >= (uint32_t)(S - 1)) {
+                        fence_proxy_async_smem();
+                        mbar_arrive(full0 + 8 * ((it - (S - 1)) % S));
+                    }
+                    ++it;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        const uint32_t first = it >= (uint32_t)(S - 1) ? it - (S - 1) : 0u;
+        for (uint32_t q = first; q < it; ++q) mbar_arrive(full0 + 8 * (q % S));
+        if (!ok) atomicOr(a.err, kErrTimeout);
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BF16, BN);
+            uint32_t it = 0, ua = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
+                const int64_t t = u / NB;
+                const uint32_t buf = ua & 1u;
+                if (!mbar_wait(tempty0 + 8 * buf, ((ua >> 1) & 1u) ^ 1u, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * BN;
+                const uint32_t tm = a.tile_mask[t];
+                uint32_t acc = 0;
+                for (int k = 0; k < kTaps && ok; ++k) {
+                    if (!((tm >> k) & 1u)) continue;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t stage = it % S, ph = (it / S) & 1u;
+                        if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_base = smem_u32(sA + stage * kABytes);
+                        const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+                        for (int j = 0; j < kBK / 16; ++j) {
+                            mma_f16(d_tmem, sw128_kmajor_desc(a_base + 32 * j), sw128_kmajor_desc(b_base + 32 * j),
+                                    idesc, acc | (uint32_t)j);
+                        }
+                        acc = 1;
+                        mma_commit(empty0 + 8 * stage);
+                        ++it;
+                    }
+                }
+                if (ok) mma_commit(tfull0 + 8 * buf);
+            }
+            // all issued MMAs must finish before TMEM is released: time-bounded, ignores the abort flag
+            mma_commit(done_bar);
+            const bool drained = mbar_wait_timed(done_bar, 0);
+            if (!ok || !drained) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        uint32_t ua = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
+            const int64_t t = u / NB;
+            const int nb = (int)(u - t * NB);
+            const uint32_t buf = ua & 1u;
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua >> 1) & 1u, s_abort));
+            if (!ok) break;  // warp-uniform
+            tc_fence_after();
+            const int64_t r = t * kBM + q * 32 + lane;
+            const uint32_t v = r < a.n ? a.sorted_idx[r] : kNone;
+            const int col0 = nb * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t acc[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
+                tmem_ld_wait();
+                if (v != kNone) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
+                        if (a.bias) {
+                            lo += bits_to_f32<BF16>(a.bias[col0 + c0 + 2 * i]);
+                            hi += bits_to_f32<BF16>(a.bias[col0 + c0 + 2 * i + 1]);
+                        }
+                        pk[i] = pack2<BF16>(lo, hi);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)v * a.Ndim + col0 + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            atomicOr(a.err, kErrTimeout);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Repack W into the B-operand tiles the MMA reads: for tap k, N block nb and
+// K block kb, a [BN rows][64 K elements] tile, rows of 128 B in the 128-byte
+// swizzled layout (row n at (n/8)*1024 + (n%8)*128, 16-byte chunk c stored at
+// chunk c ^ (n%8)).  fwd: row n = output channel, K = input channel,
+// element W[k][kk][n].  dgrad: row n = input channel, K = output channel,
+// element W[26-k][n][kk] (the flipped, transposed tap).
+__global__ void __launch_bounds__(256)
+k_pack_weights(const uint16_t* __restrict__ W, int Cin, int Cout, int dgrad, int BN, uint8_t* __restrict__ img) {
+    __shared__ uint16_t tile[64][66];
+    const int k = blockIdx.x, kb = blockIdx.y, n0 = blockIdx.z * 64;
+    const int Kdim = dgrad ? Cout : Cin;
+    const int KB = Kdim / 64;
+    const int tid = threadIdx.x;
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        if (!dgrad) {
+            const int kk = idx >> 6, n = idx & 63;
+            tile[kk][n] = W[((int64_t)k * Cin + kb * 64 + kk) * Cout + n0 + n];
+        } else {
+            const int n = idx >> 6, kk = idx & 63;
+            tile[kk][n] = W[((int64_t)(26 - k) * Cin + n0 + n) * Cout + kb * 64 + kk];
+        }
+    }
+    __syncthreads();
+    for (int chk = tid; chk < 64 * 8; chk += 256) {
+        const int n = chk >> 3, c = chk & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = (uint32_t)tile[c * 8 + 2 * e][n] | ((uint32_t)tile[c * 8 + 2 * e + 1][n] << 16);
+        const int gn = n0 + n, nb = gn / BN, nl = gn - nb * BN;
+        const int64_t base = (((int64_t)nb * kTaps + k) * KB + kb) * (int64_t)BN * 128;
+        const int64_t off = base + (nl >> 3) * 1024 + (nl & 7) * 128 + ((c ^ (nl & 7)) << 4);
+        *reinterpret_cast<uint4*>(img + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+template <int BN, bool BF16>
+int launch_tc(const TcArgs& a, cudaStream_t s) {
+    using C = Cfg<BN>;
+    auto kern = k_gather_gemm_tc<BN, BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+        return VG_ERR_CUDA;
+    const int64_t units = a.num_tiles * (a.Ndim / BN);
+    const int grid = (int)std::min<int64_t>(units, sm_count());
+    kern<<<grid, kThreads, C::kSmem, s>>>(a);
+    return VG_OK;
+}
+
+}  // namespace
+
+int tc_supported(int dtype, int Cin, int Cout) {
+    return (dtype == VG_F16 || dtype == VG_BF16) && Cin % 64 == 0 && Cout % 64 == 0 ? 1 : 0;
+}
+
+size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim) {
+    (void)dtype;
+    return (size_t)kTaps * Kdim * Ndim * 2;
+}
+
+int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void* packed,
+                    const uint32_t* nbr_status, cudaStream_t s) {
+    (void)dtype;
+    (void)nbr_status;
+    const int Kdim = dgrad ? Cout : Cin, Ndim = dgrad ? Cin : Cout;
+    const dim3 grid(kTaps, Kdim / 64, Ndim / 64);
+    k_pack_weights<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(W), Cin, Cout, dgrad, choose_bn(Ndim),
+                                        static_cast<uint8_t*>(packed));
+    return VG_OK;
+}
+
+int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
+    if (p.n == 0) return VG_OK;
+    TcArgs a;
+    a.sorted_idx = p.sorted_idx;
+    a.tile_mask = p.tile_mask;
+    a.nbr = p.nbr;
+    a.nbr_status = p.nbr_status;
+    a.n = p.n;
+    a.num_tiles = (p.n + kBM - 1) / kBM;
+    a.A = static_cast<const uint16_t*>(p.A);
+    a.Kdim = p.Kdim;
+    a.Bimg = static_cast<const uint8_t*>(packed);
+    a.bias = static_cast<const uint16_t*>(p.bias);
+    a.out = static_cast<uint16_t*>(p.out);
+    a.Ndim = p.Ndim;
+    a.err = p.err;
+    const bool bf16 = p.dtype == VG_BF16;
+    switch (choose_bn(p.Ndim)) {
+        case 256: return bf16 ? launch_tc<256, true>(a, s) : launch_tc<256, false>(a, s);
+        case 128: return bf16 ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
+        default: return bf16 ? launch_tc<64, true>(a, s) : launch_tc<64, false>(a, s);
+    }
+}
+
+// Weight gradient: CUDA-core split-K kernel for now.
+int tc_wgrad_splits(int64_t n, int Cin, int Cout) { return simt_wgrad_splits(n, Cin, Cout); }
+int tc_wgrad(const WgradPass& p, cudaStream_t s) { return simt_wgrad(p, s); }
 int tc_fwd_launches() { return 2; }
-int tc_bwd_launches() { return 6; }
+int tc_bwd_launches() { return 2 + 2 + 2; }
+
 }  // namespace vg

@@ -102,19 +102,29 @@ k_probe(const int4* __restrict__ coords, int64_t n, int X, int Y, int Z,
     }
 }
 
-// ------------------------------------------------------------------ Morton order
+// ------------------------------------------------------------------ row order
+// Sort key of voxel i (the page's sorted_idx groups rows for the masked GEMM):
+//   m      = (b << 3L) | interleave(x, y, z)            Morton (z-order) code
+//   key    = ((m >> F) << (27 + F)) | (mask_i << F) | (m & (2^F - 1)),  F = min(3L, 21)
+// i.e. coarse Morton block of 128^3 voxels, then the valid-tap mask, then the
+// fine Morton order.  Rows of one tile then share most of their taps (few
+// zero-filled rows in the MMA) while a block's rows stay spatially close
+// (gathered neighbours are reused from L2).
 template <typename SK>
-__global__ void k_morton(const int4* __restrict__ coords, int64_t n, int L, SK* __restrict__ keys) {
+__global__ void k_order_key(const int4* __restrict__ coords, const uint32_t* __restrict__ mask, int64_t n,
+                            int L, SK* __restrict__ keys) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int4 c = coords[i];
-    SK key = (SK)(uint32_t)c.x << (3 * L);
-    for (int m = 0; m < L; ++m) {
-        key |= (SK)(((uint32_t)c.y >> m) & 1u) << (3 * m + 2);
-        key |= (SK)(((uint32_t)c.z >> m) & 1u) << (3 * m + 1);
-        key |= (SK)(((uint32_t)c.w >> m) & 1u) << (3 * m);
+    uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
+    for (int b = 0; b < L; ++b) {
+        m |= (uint64_t)(((uint32_t)c.y >> b) & 1u) << (3 * b + 2);
+        m |= (uint64_t)(((uint32_t)c.z >> b) & 1u) << (3 * b + 1);
+        m |= (uint64_t)(((uint32_t)c.w >> b) & 1u) << (3 * b);
     }
-    keys[i] = key;
+    const int F = min(3 * L, kFineOrderBits);
+    const uint64_t fine = m & ((uint64_t(1) << F) - 1);
+    keys[i] = (SK)(((m >> F) << (kTaps + F)) | ((uint64_t)mask[i] << F) | fine);
 }
 
 // Stable LSD radix sort, 8-bit digits.  Pass = histogram -> scan -> scatter.
@@ -260,7 +270,7 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     } else l.key64 = vol >= 1073741824.0 ? 1 : 0;
     const int lb = ceil_log2(B);
     const int lg = ceil_log2(std::max(X, std::max(Y, Z)));
-    l.sort_bits = lb + 3 * lg;
+    l.sort_bits = lb + 3 * lg + kTaps;  // Morton code + the 27-bit valid-tap mask
     if (l.sort_bits > 64) return VG_ERR_UNSUPPORTED;
     l.sort64 = l.sort_bits > 32 ? 1 : 0;
     if (flags & VG_TEST_SMALL_HASH) {
@@ -306,8 +316,8 @@ static void launch_hash(const int4* coords, const NbrLayout& l, int B, int X, in
 }
 
 template <typename SK>
-static void launch_sort(const int4* coords, const NbrLayout& l, int X, int Y, int Z, char* ws,
-                        cudaStream_t s) {
+static void launch_sort(const int4* coords, const uint32_t* mask, const NbrLayout& l, int X, int Y, int Z,
+                        char* ws, cudaStream_t s) {
     const int64_t n = l.n;
     const int L = ceil_log2(std::max(X, std::max(Y, Z)));
     SK* ka = reinterpret_cast<SK*>(ws + l.off_skeys_a);
@@ -315,7 +325,7 @@ static void launch_sort(const int4* coords, const NbrLayout& l, int X, int Y, in
     uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + l.off_sorted);
     uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + l.off_svals_b);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + l.off_hist);
-    k_morton<SK><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(coords, n, L, ka);
+    k_order_key<SK><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(coords, mask, n, L, ka);
     const int passes = std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits);
     const unsigned g = (unsigned)l.sort_blocks;
     const uint32_t* vin = nullptr;
@@ -350,8 +360,8 @@ int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsi
         const int4* c4 = reinterpret_cast<const int4*>(coords);
         if (l.key64) launch_hash<uint64_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
         else launch_hash<uint32_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
-        if (l.sort64) launch_sort<uint64_t>(c4, l, X, Y, Z, ws, s);
-        else launch_sort<uint32_t>(c4, l, X, Y, Z, ws, s);
+        if (l.sort64) launch_sort<uint64_t>(c4, mask, l, X, Y, Z, ws, s);
+        else launch_sort<uint32_t>(c4, mask, l, X, Y, Z, ws, s);
         k_tile_mask<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
             reinterpret_cast<const uint32_t*>(ws + l.off_sorted), mask, N,
             reinterpret_cast<uint32_t*>(ws + l.off_tmask));
