@@ -57,6 +57,23 @@ def nbrmap_bytes(N):
     return 16 * N * 3 + 27 * 12 * N + 4 * 28 * N
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Slowest rank's value (the timed region ends when every replica is done)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_voxels_per_s(n_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own replica of n_per_rank voxels."""
+    return world * n_per_rank / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -148,6 +165,22 @@ def run_ours(args, rank, world, local_rank):
         step()
     stream.synchronize()
     assert m.status(stream) == ops.VG_OK
+
+    def graphed(fn):
+        """Capture fn (stream-ordered C-ABI calls on `stream`) once; replay per step."""
+        if args.no_graph:
+            return fn
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        stream.synchronize()
+        return g.replay
+
+    eager_step = step
+    step = graphed(eager_step)
+    for _ in range(3):
+        step()
+    stream.synchronize()
     P = int(torch.stack([(m.mask >> k) & 1 for k in range(27)]).sum().item())
 
     # ---- timed region: exactly K steps
@@ -165,11 +198,7 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b_) for a, b_ in evs]
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), world, dev)
     assert m.status(stream) == ops.VG_OK and ops.vg_conv_status(ws, stream) == ops.VG_OK
     ms_per_step = tot_ms / args.steps
 
@@ -186,6 +215,7 @@ def run_ours(args, rank, world, local_rank):
     }
     for name, fn in calls.items():
         ev = []
+        fn = graphed(fn)
         fn()
         timed(fn, kph, ev)
         torch.cuda.synchronize(dev)
@@ -201,18 +231,20 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
 
-    def e2e_step():
+    def e2e_eager():
         with torch.cuda.stream(stream):
             coords.copy_(h_coords, non_blocking=True)
             f.copy_(h_f, non_blocking=True)
             W.copy_(h_W, non_blocking=True)
             b.copy_(h_b, non_blocking=True)
             dY.copy_(h_dY, non_blocking=True)
-            step()
+            eager_step()
             h_out.copy_(out, non_blocking=True)
             h_dX.copy_(dX, non_blocking=True)
             h_dW.copy_(dW, non_blocking=True)
             h_db.copy_(db, non_blocking=True)
+
+    e2e_step = graphed(e2e_eager)
 
     ke = max(3, min(args.steps, 100))
     for _ in range(2):
@@ -252,14 +284,15 @@ def run_ours(args, rank, world, local_rank):
     t_roof = sum(max(fl / tc_peak, by / bw) for fl, by in work.values())
     total_fl = sum(fl for fl, _ in work.values())
     res = {
-        "metric": METRIC, "value": world * N / (ms_per_step * 1e-3), "unit": "voxels/s",
+        "metric": METRIC, "value": aggregate_voxels_per_s(N, world, ms_per_step), "unit": "voxels/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "res": wl.res, "N": N, "P": P, "cin": wl.cin,
                    "cout": wl.cout, "step": "nbrmap build + fwd + dgrad + wgrad + dbias",
                    "l2": "flushed between steps (256 MiB write, outside the per-step events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": "eager" if args.no_graph else "CUDA graph replay of the step's C-ABI calls"},
         "tflops": world * total_fl / (ms_per_step * 1e-3) / 1e12,
         "roofline_step_frac": t_roof / (ms_per_step * 1e-3),
         "roofline": roof,
@@ -357,6 +390,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each call eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

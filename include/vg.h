@@ -126,6 +126,10 @@ VG_API int vg_nbrmap_status(const void* ws, void* stream);
  *   tile_mask  [ceil(N/128)] uint32 — OR of mask over sorted rows [128t, 128t+128) */
 VG_API const uint32_t* vg_nbrmap_sorted_idx(const void* ws);
 VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);
+/*   sorted_nbr [ceil(N/128)*128][27] uint32 — sorted_nbr[r][k] = nbr[sorted_idx[r]][k],
+ *                rows past N are VG_NONE (the map in processing order, so a tile's
+ *                neighbour lists are one contiguous 13.5 KB block). */
+VG_API const uint32_t* vg_nbrmap_sorted_nbr(const void* ws, int64_t N);
 
 /* Host-only description of the build plan (no device access):
  *   info[0] = 1 if the hash keys are 64-bit, info[1] = significant bits of the
@@ -182,6 +186,7 @@ VG_API int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uin
  * device-side wait (its outputs are then incomplete), else VG_OK.  Every
  * fwd/bwd call clears this record when it starts. */
 VG_API int vg_conv_status(void* conv_ws, void* stream);
+
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,10 @@ def test_nbrmap_bit_exact(name):
     pad[:n] = mask_ref[order]
     want = np.bitwise_or.reduce(pad.reshape(T, 128), axis=1)
     assert np.array_equal(u32(m.tile_mask()), want)
+    # neighbour lists in processing order, padded with VG_NONE to whole tiles
+    sn = u32(m.sorted_nbr())
+    assert sn.shape == (T * 128, 27)
+    assert np.array_equal(sn[:n], nbr_ref[order]) and np.all(sn[n:] == 0xFFFFFFFF)
 
 
 def test_key_width_does_not_change_the_map():

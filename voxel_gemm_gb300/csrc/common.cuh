@@ -46,7 +46,7 @@ struct NbrLayout {
     int64_t num_tiles = 0;  // ceil(n / 128)
     int64_t sort_blocks = 0;
     size_t off_hdr = 0, off_sorted = 0, off_tmask = 0, off_hkeys = 0, off_hvals = 0;
-    size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, total = 0;
+    size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, off_nbr_sorted = 0, total = 0;
 };
 
 constexpr int kSortItems = 16;                        // keys per thread in the radix sort

@@ -45,16 +45,15 @@ struct Cfg {
     static constexpr int kTmemCols = 2 * BN;                         // two accumulators
     static constexpr size_t kSmemA = (size_t)S * kABytes;
     static constexpr size_t kSmemB = (size_t)S * kBBytes;
-    static constexpr size_t kNbrBytes = (size_t)kBM * kTaps * 4;
-    static constexpr size_t kRowsBytes = (size_t)kBM * 4;
-    static constexpr int kNumBars = 2 * S + 5;                       // full, empty, tfull x2, tempty x2, done
-    static constexpr size_t kSmem = 1024 + kSmemA + kSmemB + kNbrBytes + kRowsBytes + 8 * kNumBars + 16;
+    static constexpr size_t kNbrTileBytes = (size_t)kBM * kTaps * 4;  // one tile of neighbour lists
+    static constexpr int kNumBars = 2 * S + 7;  // full[S], empty[S], tfull x2, tempty x2, done, nbr x2
+    static constexpr size_t kSmem = 1024 + kSmemA + kSmemB + 2 * kNbrTileBytes + 8 * kNumBars + 16;
 };
 
 struct TcArgs {
     const uint32_t* sorted_idx;
     const uint32_t* tile_mask;
-    const uint32_t* nbr;
+    const uint32_t* sorted_nbr;  // [tiles*128][27]
     const uint32_t* nbr_status;
     int64_t n;
     int64_t num_tiles;
@@ -91,9 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::kSmemA;
-    uint32_t* s_nbr = reinterpret_cast<uint32_t*>(sB + C::kSmemB);
-    uint32_t* s_rows = s_nbr + kBM * kTaps;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_rows + kBM);
+    uint32_t* s_nbr = reinterpret_cast<uint32_t*>(sB + C::kSmemB);  // [2][128*27]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_nbr + 2 * kBM * kTaps);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile uint32_t* s_abort = s_tmem + 1;
 
@@ -103,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
+    const uint32_t nbar0 = smem_u32(bars + 2 * S + 5);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, 128 + 1);  // 128 gather threads + the weight-tile expect_tx
@@ -113,6 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             mbar_init(tempty0 + 8 * i, 4);      // one arrive per epilogue warp
         }
         mbar_init(done_bar, 1);
+        mbar_init(nbar0, 1);
+        mbar_init(nbar0 + 8, 1);
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -133,26 +134,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         // ------------------------------------------------------------ gather producer
         // Every gather thread runs the same unit loop and the same named barriers;
         // after a failed wait a thread only skips work, so no barrier is left short.
+        // The neighbour lists of the next unit's tile arrive by one bulk copy while
+        // the current unit is gathered (two buffers).
         const int p = threadIdx.x;
-        uint32_t it = 0;
+        const uint32_t tile_bytes = (uint32_t)C::kNbrTileBytes;
+        uint32_t it = 0, idx = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        int64_t u = blockIdx.x;
+        if (p == 0 && u < units) {
+            mbar_arrive_expect_tx(nbar0, tile_bytes);
+            bulk_g2s(smem_u32(s_nbr), a.sorted_nbr + (u / NB) * kBM * kTaps, tile_bytes, nbar0);
+        }
+        uint32_t tm_next = u < units ? a.tile_mask[u / NB] : 0u;
+        for (; u < units; u += gridDim.x, ++idx) {
             const int64_t t = u / NB;
             const int nb = (int)(u - t * NB);
-            named_bar_sync(1, 128);  // all gather threads are done reading s_nbr of the previous unit
-            {
-                const int64_t r = t * kBM + p;
-                s_rows[p] = r < a.n ? a.sorted_idx[r] : kNone;
+            const uint32_t buf = idx & 1u;
+            const uint32_t tm = tm_next;
+            const int64_t un = u + gridDim.x;
+            if (un < units) {
+                tm_next = a.tile_mask[un / NB];
+                if (p == 0) {  // buffer buf^1 was released by the named barrier that ended the previous unit
+                    mbar_arrive_expect_tx(nbar0 + 8 * (buf ^ 1u), tile_bytes);
+                    bulk_g2s(smem_u32(s_nbr + (buf ^ 1u) * kBM * kTaps), a.sorted_nbr + (un / NB) * kBM * kTaps,
+                             tile_bytes, nbar0 + 8 * (buf ^ 1u));
+                }
             }
-            named_bar_sync(1, 128);
-            for (int idx = p; idx < kBM * kTaps; idx += 128) {
-                const int rr = idx / kTaps, k = idx - rr * kTaps;
-                const uint32_t v = s_rows[rr];
-                s_nbr[idx] = v != kNone ? a.nbr[(int64_t)v * kTaps + k] : kNone;
+            // always wait for this unit's copy, so none is in flight when the block exits
+            if (!mbar_wait_timed(nbar0 + 8 * buf, (idx >> 1) & 1u)) {
+                ok = false;
+                *s_abort = 1;
             }
-            named_bar_sync(1, 128);
-            if (!ok) continue;
-            const uint32_t tm = a.tile_mask[t];
+            const uint32_t* nb_tile = s_nbr + buf * kBM * kTaps;
             for (int k = 0; k < kTaps && ok; ++k) {
                 if (!((tm >> k) & 1u)) continue;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -172,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
                         const int row = i2 * 16 + (p >> 3);
-                        const uint32_t j = s_nbr[row * kTaps + k];
+                        const uint32_t j = nb_tile[row * kTaps + k];
                         const uint16_t* src = a.A + (int64_t)(j != kNone ? j : 0u) * a.Kdim + kb * kBK + ch * 8;
                         cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src, j != kNone ? 16u : 0u);
                     }
@@ -185,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                     ++it;
                 }
             }
+            named_bar_sync(1, 128);  // every gather thread is done with buffer buf
         }
         cp_async_wait<0>();
         fence_proxy_async_smem();
@@ -197,13 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             constexpr uint32_t idesc = idesc_f16(BF16, BN);
             uint32_t it = 0, ua = 0;
             bool ok = true;
+            uint32_t tm_next = (int64_t)blockIdx.x < units ? a.tile_mask[blockIdx.x / NB] : 0u;
             for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
-                const int64_t t = u / NB;
                 const uint32_t buf = ua & 1u;
+                const uint32_t tm = tm_next;
+                if (u + gridDim.x < units) tm_next = a.tile_mask[(u + gridDim.x) / NB];
                 if (!mbar_wait(tempty0 + 8 * buf, ((ua >> 1) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * BN;
-                const uint32_t tm = a.tile_mask[t];
                 uint32_t acc = 0;
                 for (int k = 0; k < kTaps && ok; ++k) {
                     if (!((tm >> k) & 1u)) continue;
@@ -368,7 +383,7 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     TcArgs a;
     a.sorted_idx = p.sorted_idx;
     a.tile_mask = p.tile_mask;
-    a.nbr = p.nbr;
+    a.sorted_nbr = p.sorted_nbr;
     a.nbr_status = p.nbr_status;
     a.n = p.n;
     a.num_tiles = (p.n + kBM - 1) / kBM;
@@ -387,10 +402,6 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     }
 }
 
-// Weight gradient: CUDA-core split-K kernel for now.
-int tc_wgrad_splits(int64_t n, int Cin, int Cout) { return simt_wgrad_splits(n, Cin, Cout); }
-int tc_wgrad(const WgradPass& p, cudaStream_t s) { return simt_wgrad(p, s); }
-int tc_fwd_launches() { return 2; }
-int tc_bwd_launches() { return 2 + 2 + 2; }
+int tc_fwd_launches() { return 2; }  // weight repack, gather GEMM
 
 }  // namespace vg

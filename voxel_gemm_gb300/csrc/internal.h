@@ -17,6 +17,10 @@ int nbr_status(const void* ws, cudaStream_t s);
 // Byte offset of sorted_idx / tile masks inside a neighbour-map workspace.
 constexpr size_t kSortedIdxOffset = 256;
 inline size_t tile_mask_offset(int64_t N) { return 256 + ((4 * (size_t)N + 255) / 256) * 256; }
+inline size_t sorted_nbr_offset(int64_t N) {
+    const size_t tiles = (size_t)((N + 127) / 128);
+    return tile_mask_offset(N) + ((4 * tiles + 255) / 256) * 256;
+}
 
 // ---- convolution passes (all asynchronous on stream s) ----
 // One "gather GEMM" pass over the sorted rows:
@@ -27,6 +31,7 @@ struct GatherPass {
     const uint32_t* sorted_idx;
     const uint32_t* tile_mask;   // per 128 sorted rows
     const uint32_t* nbr;
+    const uint32_t* sorted_nbr;  // [tiles*128][27] neighbour lists in processing order
     const uint32_t* nbr_status;  // device word; non-zero = bad map, write nothing
     int64_t n;
     const void* A;
@@ -45,6 +50,8 @@ int simt_gather_pass(const GatherPass& p, cudaStream_t s);
 
 struct WgradPass {
     const uint32_t* sorted_idx;
+    const uint32_t* tile_mask;
+    const uint32_t* sorted_nbr;
     const uint32_t* nbr;
     const uint32_t* mask;
     const uint32_t* nbr_status;

@@ -248,6 +248,17 @@ k_tile_mask(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict_
     }
 }
 
+// nbr_sorted[r][k] = nbr[sorted_idx[r]][k] for r < n, VG_NONE for the padding rows
+// up to a whole number of 128-row tiles.  One thread per entry (coalesced writes).
+__global__ void k_sort_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
+                            int64_t n, int64_t total, uint32_t* __restrict__ nbr_sorted) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= total) return;
+    const int64_t r = e / kTaps;
+    const int k = (int)(e - r * kTaps);
+    nbr_sorted[e] = r < n ? nbr[(int64_t)sorted_idx[r] * kTaps + k] : kNone;
+}
+
 // ------------------------------------------------------------------ host side
 static int ceil_log2(int64_t v) {
     int b = 0;
@@ -289,6 +300,7 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     l.off_hdr = o;      o += 256;
     l.off_sorted = o;   o += align_up(4 * (size_t)N, 256);
     l.off_tmask = o;    o += align_up(4 * (size_t)l.num_tiles, 256);
+    l.off_nbr_sorted = o; o += align_up(4 * (size_t)kTaps * kTileRows * l.num_tiles, 256);
     l.off_hkeys = o;    o += align_up(ks * cap, 256);
     l.off_hvals = o;    o += align_up(4 * cap, 256);
     l.off_skeys_a = o;  o += align_up(ss * (size_t)N, 256);
@@ -365,6 +377,10 @@ int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsi
         k_tile_mask<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
             reinterpret_cast<const uint32_t*>(ws + l.off_sorted), mask, N,
             reinterpret_cast<uint32_t*>(ws + l.off_tmask));
+        const int64_t total = (int64_t)kTaps * kTileRows * l.num_tiles;
+        k_sort_rows<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            reinterpret_cast<const uint32_t*>(ws + l.off_sorted), nbr, N, total,
+            reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted));
     }
     return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
 }

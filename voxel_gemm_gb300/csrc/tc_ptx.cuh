@@ -152,6 +152,27 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor, MN-major operand in the 128-byte swizzle
+// layout: each K row holds 64 consecutive M (or N) elements in 128 B, 8 K rows
+// form a 1024-byte atom (stride byte offset between 8-row K groups = 1024),
+// consecutive 64-element M/N blocks lie lbo bytes apart (leading byte offset);
+// start address advances by 2048 B per K=16 step.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16 with both operands MN-major.
+__host__ __device__ constexpr uint32_t idesc_f16_mn(bool bf16, int n) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | (1u << 15) | (1u << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
 // Instruction descriptor for kind::f16: D fp32, A/B fp16 (0) or bf16 (1), both
 // K-major, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int n) {

@@ -88,6 +88,10 @@ const uint32_t* vg_nbrmap_sorted_idx(const void* ws) {
     return ws ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(ws) + kSortedIdxOffset) : nullptr;
 }
 
+const uint32_t* vg_nbrmap_sorted_nbr(const void* ws, int64_t N) {
+    return ws ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(ws) + sorted_nbr_offset(N)) : nullptr;
+}
+
 const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N) {
     return ws ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(ws) + tile_mask_offset(N)) : nullptr;
 }
@@ -100,7 +104,7 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     info[0] = l.key64;
     info[1] = l.sort_bits;
     info[2] = passes;
-    info[3] = N > 0 ? 3 + 3 * passes + 1 : 0;  // insert, probe, morton, passes x (hist, scan, scatter), tile masks
+    info[3] = N > 0 ? 3 + 3 * passes + 2 : 0;  // insert, probe, key, passes x (hist, scan, scatter), tile masks, sorted rows
     return VG_OK;
 }
 
@@ -140,6 +144,7 @@ int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
     g.sorted_idx = vg_nbrmap_sorted_idx(nbr_ws);
     g.tile_mask = vg_nbrmap_tile_mask(nbr_ws, N);
     g.nbr = nbr;
+    g.sorted_nbr = vg_nbrmap_sorted_nbr(nbr_ws, N);
     g.nbr_status = static_cast<const uint32_t*>(nbr_ws);
     g.n = N;
     g.A = feats;
@@ -198,6 +203,7 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         g.sorted_idx = vg_nbrmap_sorted_idx(nbr_ws);
         g.tile_mask = vg_nbrmap_tile_mask(nbr_ws, N);
         g.nbr = nbr;
+        g.sorted_nbr = vg_nbrmap_sorted_nbr(nbr_ws, N);
         g.nbr_status = nbr_status;
         g.n = N;
         g.A = grad_out;
@@ -222,6 +228,8 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
     if (grad_weight || grad_bias) {
         WgradPass w;
         w.sorted_idx = vg_nbrmap_sorted_idx(nbr_ws);
+        w.tile_mask = vg_nbrmap_tile_mask(nbr_ws, N);
+        w.sorted_nbr = vg_nbrmap_sorted_nbr(nbr_ws, N);
         w.nbr = nbr;
         w.mask = mask;
         w.nbr_status = nbr_status;

@@ -1,0 +1,429 @@
+// Tensor-core (tcgen05 / TMEM) weight gradient, split-K over the sorted rows.
+//
+// dW[k][ci][co] = sum_i f[nbr[i][k]][ci] * dY[i][co]: the backward of the
+// masked implicit GEMM with Split-K ("Contribution Tasks — JeffreyXiang/FlexGEMM",
+// §二 key types table: sparse_submanifold_conv_bwd_masked_implicit_gemm_splitk,
+// split-K "reduces the accumulation bottleneck for large K"; here K is the
+// voxel count).
+//
+// One MMA tile: D[128 x BN] in TMEM, D[m][n] += sum over 64-row stages of
+//   A[m][row] = f[nbr[row][tap(m)]][ci(m)]   (gathered feature rows)
+//   B[n][row] = dY[row][co0 + n]
+// Both operands are stored as rows of the sorted order, i.e. MN-major: a row
+// holds 64 consecutive channels (128 B, swizzled).  M = 128 covers two 64-channel
+// blocks, each a (tap, 64 channels) slot; slots are paired in tap-major order.
+// A work unit = (M block, N block, row chunk); a row chunk's 128-row tiles whose
+// tile mask has none of the unit's taps are skipped (their A rows would be zero).
+// Each unit writes an fp32 partial [128 x BN] for its chunk; a second kernel sums
+// the chunks in a fixed order (bitwise deterministic).
+//
+// Warp roles as in the forward kernel: warps 0-3 gather A and B with 16-byte
+// cp.async (zero fill), warp 4 issues tcgen05.mma, warps 5-8 store the partials.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace vg {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 288;
+constexpr int kRowsPerStage = 64;
+constexpr int kABytes = 2 * kRowsPerStage * 128;  // two 64-channel blocks x 64 rows
+
+template <int BN>
+struct WCfg {
+    static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kBBytes = (BN / 64) * kRowsPerStage * 128;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kNumBars = 2 * S + 5;
+    static constexpr size_t kSmem = 1024 + (size_t)S * (kABytes + kBBytes) + 8 * kNumBars + 4 * S + 16;
+};
+
+struct WgArgs {
+    const uint32_t* sorted_idx;
+    const uint32_t* tile_mask;
+    const uint32_t* sorted_nbr;
+    const uint32_t* nbr_status;
+    int64_t n;
+    int64_t num_tiles;
+    int64_t tiles_per_chunk;
+    int splits;
+    const uint16_t* f;
+    const uint16_t* dy;
+    int Cin, Cout;
+    float* partial;  // [splits][27][Cin][Cout]
+    uint32_t* err;
+};
+
+// Taps and channel offsets of M block m.  The 27 * (Cin/64) (tap, 64-channel
+// block) slots, tap-major, are taken two at a time: slots 2m and 2m+1.  With
+// Cin = 64 that pairs two taps; with Cin a multiple of 128 it is 128 channels of
+// one tap; otherwise a pair may straddle two taps.
+struct MUnit {
+    int tap0, tap1;  // tap1 = -1: the second 64-channel block is unused (zero)
+    int c0, c1;
+};
+__host__ __device__ __forceinline__ int num_munits(int Cin) { return (kTaps * (Cin / 64) + 1) / 2; }
+__device__ __forceinline__ MUnit munit(int m, int Cin) {
+    const int CB = Cin / 64;
+    const int s0 = 2 * m, s1 = 2 * m + 1;
+    MUnit r;
+    r.tap0 = s0 / CB;
+    r.c0 = (s0 % CB) * 64;
+    if (s1 < kTaps * CB) {
+        r.tap1 = s1 / CB;
+        r.c1 = (s1 % CB) * 64;
+    } else {
+        r.tap1 = -1;
+        r.c1 = 0;
+    }
+    return r;
+}
+
+// Row metadata a gather thread needs for one stage (its four rows).
+struct Meta {
+    uint32_t i[4], j0[4], j1[4];
+};
+
+__device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit& mu, int64_t row0, int p, Meta& m) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t r = row0 + (p >> 3) + 16 * q;  // r < num_tiles * 128 always
+        m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
+        m.j0[q] = a.sorted_nbr[r * kTaps + mu.tap0];
+        m.j1[q] = mu.tap1 >= 0 ? a.sorted_nbr[r * kTaps + mu.tap1] : kNone;
+    }
+}
+
+// Walks the active 128-row tiles of one chunk, 32 tile masks per coalesced warp load.
+struct TileCursor {
+    int64_t base, end;
+    uint32_t bits;  // active tiles in [base, base + 32) not yet returned
+};
+__device__ __forceinline__ uint32_t window_bits(const WgArgs& a, int64_t base, int64_t end, int64_t first,
+                                                uint32_t umask, int lane) {
+    const int64_t t = base + lane;
+    bool act = false;
+    if (t < end) act = (a.tile_mask[t] & umask) != 0u || t == first;
+    return __ballot_sync(0xffffffffu, act);
+}
+// Next active tile (or -1); all lanes of the warp call it together.
+__device__ __forceinline__ int64_t next_tile(const WgArgs& a, TileCursor& c, int64_t first, uint32_t umask,
+                                             int lane) {
+    while (c.bits == 0u) {
+        c.base += 32;
+        if (c.base >= c.end) return -1;
+        c.bits = window_bits(a, c.base, c.end, first, umask, lane);
+    }
+    const int b = __ffs(c.bits) - 1;
+    c.bits &= c.bits - 1u;
+    return c.base + b;
+}
+
+template <int BN, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
+    using C = WCfg<BN>;
+    constexpr int S = C::S;
+    constexpr int NBB = BN / 64;  // 64-column blocks of B
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + (size_t)S * kABytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * C::kBBytes);
+    uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
+    uint32_t* s_tmem = s_info + S;
+    volatile uint32_t* s_abort = s_tmem + 1;
+
+    if (*a.nbr_status) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
+    const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full0 + 8 * i, 128);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull0 + 8 * i, 1);
+            mbar_init(tempty0 + 8 * i, 4);
+        }
+        mbar_init(done_bar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int M = num_munits(a.Cin);
+    const int NB = a.Cout / BN;
+    const int64_t units = (int64_t)M * NB * a.splits;
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ gather producer
+        const int p = threadIdx.x;
+        const int ch = p & 7;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int m = (int)(u % M);
+            const int64_t rest = u / M;
+            const int nb = (int)(rest % NB);
+            const int64_t s = rest / NB;
+            const MUnit mu = munit(m, a.Cin);
+            const uint32_t umask = (1u << mu.tap0) | (mu.tap1 >= 0 ? 1u << mu.tap1 : 0u);
+            const int64_t t_first = s * a.tiles_per_chunk;
+            TileCursor cur;
+            cur.base = t_first;
+            cur.end = min(a.num_tiles, t_first + a.tiles_per_chunk);
+            cur.bits = window_bits(a, cur.base, cur.end, t_first, umask, lane);
+            int64_t t = next_tile(a, cur, t_first, umask, lane);  // the first tile is always active
+            int h = 0;
+            Meta mc, mn;
+            bool null_stage = false;
+            if (t >= 0) {
+                load_meta(a, mu, t * 128, p, mc);
+            } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
+                null_stage = true;
+                for (int q = 0; q < 4; ++q) mc.i[q] = mc.j0[q] = mc.j1[q] = kNone;
+            }
+            bool first = true;
+            while (t >= 0 || null_stage) {
+                // next stage of this unit: second half of the tile, or the next active tile
+                int64_t tn = t;
+                int hn = h + 1;
+                if (null_stage) {
+                    tn = -1;
+                    null_stage = false;
+                } else if (hn == 2) {
+                    tn = next_tile(a, cur, t_first, umask, lane);
+                    hn = 0;
+                }
+                if (tn >= 0) load_meta(a, mu, tn * 128 + hn * 64, p, mn);
+                const uint32_t stage = it % S, ph = (it / S) & 1u;
+                // warp-uniform decision: the tile cursor below uses warp-wide ballots
+                if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort))) {
+                    ok = false;
+                    *s_abort = 1;
+                    break;
+                }
+                if (p == 0) s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
+                const uint32_t a_base = smem_u32(sA + stage * kABytes);
+                const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {  // A: block e/4, row (p>>3) + 16*(e%4)
+                    const int q = e & 3, blk = e >> 2;
+                    const int row = (p >> 3) + 16 * q;
+                    const uint32_t j = blk ? mc.j1[q] : mc.j0[q];
+                    const int c = blk ? mu.c1 : mu.c0;
+                    const uint16_t* src = a.f + (int64_t)(j != kNone ? j : 0u) * a.Cin + c + ch * 8;
+                    cp_async16(a_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
+                                   ((ch ^ (row & 7)) << 4),
+                               src, j != kNone ? 16u : 0u);
+                }
+#pragma unroll
+                for (int e = 0; e < 4 * NBB; ++e) {  // B: block e/4, same four rows
+                    const int q = e & 3, blk = e >> 2;
+                    const int row = (p >> 3) + 16 * q;
+                    const uint32_t i = mc.i[q];
+                    // rows with neither tap contribute nothing: skip their dY bytes
+                    const bool use = i != kNone && (mc.j0[q] != kNone || mc.j1[q] != kNone);
+                    const uint16_t* src = a.dy + (int64_t)(use ? i : 0u) * a.Cout + nb * BN + blk * 64 + ch * 8;
+                    cp_async16(b_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
+                                   ((ch ^ (row & 7)) << 4),
+                               src, use ? 16u : 0u);
+                }
+                cp_async_commit();
+                cp_async_wait<S - 1>();
+                if (it >= (uint32_t)(S - 1)) {
+                    fence_proxy_async_smem();
+                    mbar_arrive(full0 + 8 * ((it - (S - 1)) % S));
+                }
+                ++it;
+                first = false;
+                t = tn;
+                h = hn;
+                mc = mn;
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        const uint32_t first_q = it >= (uint32_t)(S - 1) ? it - (S - 1) : 0u;
+        for (uint32_t q = first_q; q < it; ++q) mbar_arrive(full0 + 8 * (q % S));
+        if (!ok) atomicOr(a.err, kErrTimeout);
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_mn(BF16, BN);
+            constexpr uint32_t lbo = kRowsPerStage * 128;  // 64-channel blocks are 8 KB apart
+            uint32_t it = 0, ua = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
+                const uint32_t buf = ua & 1u;
+                if (!mbar_wait(tempty0 + 8 * buf, ((ua >> 1) & 1u) ^ 1u, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * BN;
+                while (true) {
+                    const uint32_t stage = it % S, ph = (it / S) & 1u;
+                    if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t info = s_info[stage];
+                    const uint32_t a_base = smem_u32(sA + stage * kABytes);
+                    const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+                    for (int j = 0; j < kRowsPerStage / 16; ++j) {
+                        mma_f16(d_tmem, sw128_mnmajor_desc(a_base + 2048 * j, lbo),
+                                sw128_mnmajor_desc(b_base + 2048 * j, lbo), idesc,
+                                ((info & 1u) && j == 0) ? 0u : 1u);
+                    }
+                    mma_commit(empty0 + 8 * stage);
+                    ++it;
+                    if (info & 2u) break;
+                }
+                if (ok) mma_commit(tfull0 + 8 * buf);
+            }
+            mma_commit(done_bar);
+            const bool drained = mbar_wait_timed(done_bar, 0);
+            if (!ok || !drained) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue: fp32 partials
+        const int q = warp & 3;
+        uint32_t ua = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
+            const int m = (int)(u % M);
+            const int64_t rest = u / M;
+            const int nb = (int)(rest % NB);
+            const int64_t s = rest / NB;
+            const uint32_t buf = ua & 1u;
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua >> 1) & 1u, s_abort));
+            if (!ok) break;
+            tc_fence_after();
+            const MUnit mu = munit(m, a.Cin);
+            const int mrow = q * 32 + lane;  // M index: block mrow / 64, channel mrow % 64
+            const int blk = mrow >> 6;
+            const int tap = blk ? mu.tap1 : mu.tap0;
+            const int ci = (blk ? mu.c1 : mu.c0) + (mrow & 63);
+            float* dst = tap >= 0 ? a.partial + ((s * kTaps + tap) * a.Cin + ci) * (int64_t)a.Cout + nb * BN
+                                  : nullptr;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t acc[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
+                tmem_ld_wait();
+                if (dst) {
+                    float4* d4 = reinterpret_cast<float4*>(dst + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                                            __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * buf);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            atomicOr(a.err, kErrTimeout);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+int wg_bn(int cout) {
+    if (cout % 256 == 0) return 256;
+    if (cout % 128 == 0) return 128;
+    return 64;
+}
+
+int sm_count_w() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+template <int BN, bool BF16>
+int launch_wgrad(const WgArgs& a, cudaStream_t s) {
+    using C = WCfg<BN>;
+    auto kern = k_wgrad_tc<BN, BF16>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+        return VG_ERR_CUDA;
+    const int M = num_munits(a.Cin);
+    const int64_t units = (int64_t)M * (a.Cout / BN) * a.splits;
+    const int grid = (int)std::min<int64_t>(units, sm_count_w());
+    kern<<<grid, kThreads, C::kSmem, s>>>(a);
+    return VG_OK;
+}
+
+}  // namespace
+
+// Split-K chunk count: about four work units per SM, every chunk non-empty,
+// partial sums capped at 1 GiB.
+int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
+    const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
+    const int64_t M = num_munits(Cin);
+    const int64_t per_split = M * (Cout / wg_bn(Cout));
+    int64_t S = std::max<int64_t>(1, (4 * 152 + per_split - 1) / per_split);
+    const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
+    S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
+    S = std::min<int64_t>(S, T);
+    const int64_t tpc = (T + S - 1) / S;
+    return (int)((T + tpc - 1) / tpc);
+}
+
+int tc_wgrad(const WgradPass& p, cudaStream_t s) {
+    if (p.n == 0) return VG_OK;
+    if (p.dW) {
+        WgArgs a;
+        a.sorted_idx = p.sorted_idx;
+        a.tile_mask = p.tile_mask;
+        a.sorted_nbr = p.sorted_nbr;
+        a.nbr_status = p.nbr_status;
+        a.n = p.n;
+        a.num_tiles = (p.n + kTileRows - 1) / kTileRows;
+        a.splits = p.splits;
+        a.tiles_per_chunk = (a.num_tiles + p.splits - 1) / p.splits;
+        a.f = static_cast<const uint16_t*>(p.f);
+        a.dy = static_cast<const uint16_t*>(p.dy);
+        a.Cin = p.Cin;
+        a.Cout = p.Cout;
+        a.partial = p.partial;
+        a.err = p.err;
+        const bool bf16 = p.dtype == VG_BF16;
+        int st;
+        switch (wg_bn(p.Cout)) {
+            case 256: st = bf16 ? launch_wgrad<256, true>(a, s) : launch_wgrad<256, false>(a, s); break;
+            case 128: st = bf16 ? launch_wgrad<128, true>(a, s) : launch_wgrad<128, false>(a, s); break;
+            default: st = bf16 ? launch_wgrad<64, true>(a, s) : launch_wgrad<64, false>(a, s); break;
+        }
+        if (st != VG_OK) return st;
+        launch_reduce_splits(p.partial, p.splits, (int64_t)kTaps * p.Cin * p.Cout, p.dW, p.dtype, p.nbr_status, s);
+    }
+    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.splits, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    return VG_OK;
+}
+
+int tc_bwd_launches() { return 2 + 2 + 2; }  // dgrad (pack, gemm), wgrad (gemm, reduce), dbias (partial, reduce)
+
+}  // namespace vg

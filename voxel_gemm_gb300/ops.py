@@ -57,6 +57,7 @@ def lib():
             "vg_nbrmap_status": ([P, P], I),
             "vg_nbrmap_sorted_idx": ([P], P),
             "vg_nbrmap_tile_mask": ([P, I64], P),
+            "vg_nbrmap_sorted_nbr": ([P, I64], P),
             "vg_conv_workspace_bytes": ([I64, I, I, I, U], SZ),
             "vg_subm_conv3d_fwd": ([P, P, P, I64, I, P, P, P, P, I, I, U, P, SZ, P], I),
             "vg_subm_conv3d_bwd": ([P, P, P, I64, I, P, P, P, P, P, P, I, I, U, P, SZ, P], I),
@@ -126,6 +127,13 @@ def vg_nbrmap_tile_mask(ws, N: int) -> torch.Tensor:
     off = lib().vg_nbrmap_tile_mask(_p(ws), N) - ws.data_ptr()
     T = (N + VG_TILE_ROWS - 1) // VG_TILE_ROWS
     return ws.view(torch.uint8)[off: off + 4 * T].view(torch.int32)
+
+
+def vg_nbrmap_sorted_nbr(ws, N: int) -> torch.Tensor:
+    """View of the workspace's neighbour lists in processing order [ceil(N/128)*128, 27]."""
+    off = lib().vg_nbrmap_sorted_nbr(_p(ws), N) - ws.data_ptr()
+    R = (N + VG_TILE_ROWS - 1) // VG_TILE_ROWS * VG_TILE_ROWS
+    return ws.view(torch.uint8)[off: off + 4 * 27 * R].view(torch.int32).view(R, 27)
 
 
 def vg_conv_workspace_bytes(N: int, Cin: int, Cout: int, dtype, flags: int = 0) -> int:
@@ -204,6 +212,9 @@ class NbrMap:
 
     def tile_mask(self) -> torch.Tensor:
         return vg_nbrmap_tile_mask(self.ws, self.N)
+
+    def sorted_nbr(self) -> torch.Tensor:
+        return vg_nbrmap_sorted_nbr(self.ws, self.N)
 
 
 def conv_workspace(N, Cin, Cout, dtype, device="cuda", flags=0) -> torch.Tensor:
