@@ -188,6 +188,31 @@ VG_API int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uin
 VG_API int vg_conv_status(void* conv_ws, void* stream);
 
 
+/* ======================================================================================
+ * Forward pass without a caller-provided workspace.
+ * The paper has no counterpart to this call.  It is for callers that cannot
+ * allocate device memory: code running inside a stream capture (a cudaMalloc there
+ * is not part of the graph and can break the capture), plug-ins hosted by a runtime
+ * that owns all device memory and forbids allocation after start-up, and hot paths
+ * that cannot afford the device-wide synchronisation of cudaMalloc/cudaFree.
+ * Arguments and result are those of vg_subm_conv3d_fwd without conv_ws: the scratch
+ * (repacked weight tiles and the error word) is a fixed __device__ array of
+ * 8 MiB + 256 B inside the library, which every GPU that loads the library holds
+ * until the process exits.
+ *  - Returns VG_ERR_WORKSPACE_TOO_SMALL when the repacked weights (27*Cin*Cout*2
+ *    bytes on the tensor-core path: 16-bit dtype, Cin and Cout multiples of 64)
+ *    exceed 8 MiB, e.g. Cin = Cout = 512.
+ *  - Allocates nothing.  The first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call uses the same array, which keeps the previous call's contents: calls
+ *    that can overlap on the GPU (other streams, other host threads) race on it and
+ *    must be serialised by the caller.
+ * ====================================================================================== */
+VG_API int vg_subm_conv3d_fwd_noalloc(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask,
+                                      int64_t N, int dtype, const void* feats, const void* weight,
+                                      const void* bias, void* out, int Cin, int Cout, unsigned flags,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

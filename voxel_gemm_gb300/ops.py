@@ -64,6 +64,7 @@ def lib():
             "vg_conv_status": ([P, P], I),
             "vg_nbrmap_describe": ([I64, I, I, I, I, U, ctypes.POINTER(ctypes.c_int)], I),
             "vg_conv_describe": ([I64, I, I, I, U, ctypes.POINTER(ctypes.c_int)], I),
+            "vg_subm_conv3d_fwd_noalloc": ([P, P, P, I64, I, P, P, P, P, I, I, U, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -148,6 +149,15 @@ def vg_subm_conv3d_fwd(nbr_ws, nbr, mask, feats, weight, bias, out, conv_ws, fla
                                     _p(weight), _p(bias), _p(out), Cin, Cout, flags, _p(conv_ws),
                                     conv_ws.numel() * conv_ws.element_size(), _s(stream)),
            "vg_subm_conv3d_fwd")
+
+
+def vg_subm_conv3d_fwd_noalloc(nbr_ws, nbr, mask, feats, weight, bias, out, flags=0, stream=None) -> None:
+    """Forward without a workspace argument (scratch is a fixed array inside the library)."""
+    N, Cin = feats.shape
+    Cout = weight.shape[2]
+    _check(lib().vg_subm_conv3d_fwd_noalloc(_p(nbr_ws), _p(nbr), _p(mask), N, _dtype_code(feats), _p(feats),
+                                            _p(weight), _p(bias), _p(out), Cin, Cout, flags, _s(stream)),
+           "vg_subm_conv3d_fwd_noalloc")
 
 
 def vg_subm_conv3d_bwd(nbr_ws, nbr, mask, grad_out, feats, weight, grad_feats, grad_weight, grad_bias,
