@@ -174,7 +174,11 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.graph(g, stream=stream):
             fn()
         stream.synchronize()
-        return g.replay
+
+        def replay():  # replay() launches on the current stream: make it the timed one
+            with torch.cuda.stream(stream):
+                g.replay()
+        return replay
 
     eager_step = step
     step = graphed(eager_step)

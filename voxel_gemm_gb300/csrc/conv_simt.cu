@@ -199,18 +199,58 @@ __global__ void k_reduce_splits(const float* __restrict__ partial, int splits, i
     out[i] = from_f32<T>(s);
 }
 
-// db partial sums over row chunks (original row order), one thread per column.
+// db partial sums: block b sums rows [b*kDbRows, (b+1)*kDbRows) of dy into
+// partial_db[b][:].  Thread = (row lane, 8-column group); each thread sums its
+// rows in order, then row lanes are combined in order: a fixed summation order.
+constexpr int kDbRows = 4096;
+
+// Eight consecutive elements (16- or 32-byte aligned) as floats.
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 template <typename T>
-__global__ void k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows_per_chunk,
-                                float* __restrict__ partial_db, const uint32_t* __restrict__ nbr_status) {
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = to_f32(e[q]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, float* __restrict__ partial_db,
+                const uint32_t* __restrict__ nbr_status) {
+    __shared__ float red[256 * 8];
     if (*nbr_status) return;
-    const int co = blockIdx.x * blockDim.x + threadIdx.x;
-    const int s = blockIdx.y;
-    if (co >= Cout) return;
-    const int64_t rb = (int64_t)s * rows_per_chunk, re = min(n, rb + rows_per_chunk);
-    float acc = 0.f;
-    for (int64_t r = rb; r < re; ++r) acc += to_f32(dy[r * Cout + co]);
-    partial_db[(int64_t)s * Cout + co] = acc;
+    const int cg8 = Cout / 8;                      // 8-column groups
+    const int lanes = cg8 >= 256 ? 1 : 256 / cg8;  // row lanes per block
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * kDbRows, r1 = min(n, r0 + kDbRows);
+    for (int g0 = 0; g0 < cg8; g0 += 256 / lanes) {
+        const int rl = tid / (256 / lanes), g = g0 + tid % (256 / lanes);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (g < cg8) {
+            for (int64_t r = r0 + rl; r < r1; r += lanes) {
+                float v[8];
+                load8(dy + r * Cout + g * 8, v);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += v[q];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) red[tid * 8 + q] = acc[q];
+        __syncthreads();
+        const int width = 256 / lanes;  // column groups handled in this round
+        for (int c = tid; c < width * 8; c += 256) {
+            const int gg = g0 + c / 8;
+            if (gg >= cg8) continue;
+            float sum = 0.f;
+            for (int l = 0; l < lanes; ++l) sum += red[(l * width + c / 8) * 8 + (c & 7)];
+            partial_db[(int64_t)blockIdx.x * Cout + gg * 8 + (c & 7)] = sum;
+        }
+        __syncthreads();
+    }
 }
 
 template <typename T>
@@ -286,21 +326,22 @@ void launch_reduce_splits(const float* partial, int splits, int64_t total, void*
     else reduce_t<__nv_bfloat16>(partial, splits, total, out, nbr_status, s);
 }
 
+int dbias_blocks(int64_t n) { return (int)std::max<int64_t>(1, (n + kDbRows - 1) / kDbRows); }
+
 template <typename T>
-static void dbias_t(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+static void dbias_t(const void* dy, int64_t n, int Cout, void* db, float* partial_db,
                     const uint32_t* nbr_status, cudaStream_t s) {
-    const int64_t rpc = (n + splits - 1) / splits;
-    const dim3 grid((unsigned)((Cout + 127) / 128), (unsigned)splits);
-    k_dbias_partial<T><<<grid, 128, 0, s>>>(static_cast<const T*>(dy), n, Cout, rpc, partial_db,
-                                           nbr_status);
-    reduce_t<T>(partial_db, splits, Cout, db, nbr_status, s);
+    const int R = dbias_blocks(n);
+    k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, partial_db, nbr_status);
+    reduce_t<T>(partial_db, R, Cout, db, nbr_status, s);
 }
 
 void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s) {
-    if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
-    else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
-    else dbias_t<__nv_bfloat16>(dy, n, Cout, splits, db, partial_db, nbr_status, s);
+    (void)splits;
+    if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, db, partial_db, nbr_status, s);
+    else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, db, partial_db, nbr_status, s);
+    else dbias_t<__nv_bfloat16>(dy, n, Cout, db, partial_db, nbr_status, s);
 }
 
 }  // namespace vg

@@ -73,7 +73,9 @@ int simt_wgrad(const WgradPass& p, cudaStream_t s);
 // Deterministic fixed-order sum of split-K partials [splits][total] into out (dtype).
 void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
                           const uint32_t* nbr_status, cudaStream_t s);
-// db = column sums of dy over `splits` row chunks, reduced in a fixed order.
+// db = column sums of dy over dbias_blocks(n) row blocks, reduced in a fixed order
+// (partial_db holds dbias_blocks(n) x Cout floats; `splits` is unused).
+int dbias_blocks(int64_t n);
 void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s);
 
@@ -87,7 +89,8 @@ int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void
                     const uint32_t* nbr_status, cudaStream_t s);
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
 int tc_wgrad(const WgradPass& p, cudaStream_t s);
-int tc_fwd_launches();   // kernels per forward call on the tensor-core path
+int tc_fwd_launches();
+   // kernels per forward call on the tensor-core path
 int tc_bwd_launches();   // kernels per full backward call on the tensor-core path
 
 }  // namespace vg

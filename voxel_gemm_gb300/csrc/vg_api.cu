@@ -28,7 +28,7 @@ static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, Co
     p.off_wfwd = o;        o += p.tensor_core ? align_up(tc_packed_weight_bytes(dtype, Cin, Cout), 256) : 0;
     p.off_wbwd = o;        o += p.tensor_core ? align_up(tc_packed_weight_bytes(dtype, Cout, Cin), 256) : 0;
     p.off_partial = o;     o += align_up((size_t)p.splits * kTaps * Cin * Cout * 4, 256);
-    p.off_partial_db = o;  o += align_up((size_t)p.splits * Cout * 4, 256);
+    p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N) * Cout * 4, 256);
     (void)wbytes;
     p.total = o;
     *P = p;

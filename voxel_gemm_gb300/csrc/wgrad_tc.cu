@@ -18,7 +18,8 @@
 // the chunks in a fixed order (bitwise deterministic).
 //
 // Warp roles as in the forward kernel: warps 0-3 gather A and B with 16-byte
-// cp.async (zero fill), warp 4 issues tcgen05.mma, warps 5-8 store the partials.
+// cp.async (zero fill; each thread's copies arrive on the stage barrier by
+// themselves), warp 4 issues tcgen05.mma, warps 5-8 store the partials.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
     const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(full0 + 8 * i, 128);
+            mbar_init(full0 + 8 * i, 128 + 1);  // 128 copy arrivals + thread 0's info arrival
             mbar_init(empty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -217,7 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     *s_abort = 1;
                     break;
                 }
-                if (p == 0) s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
+                if (p == 0) {  // published by thread 0's own release arrival below
+                    s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
+                    mbar_arrive(full0 + 8 * stage);
+                }
                 const uint32_t a_base = smem_u32(sA + stage * kABytes);
                 const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
@@ -243,12 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                                    ((ch ^ (row & 7)) << 4),
                                src, use ? 16u : 0u);
                 }
-                cp_async_commit();
-                cp_async_wait<S - 1>();
-                if (it >= (uint32_t)(S - 1)) {
-                    fence_proxy_async_smem();
-                    mbar_arrive(full0 + 8 * ((it - (S - 1)) % S));
-                }
+                cp_async_arrive_noinc(full0 + 8 * stage);  // fires when this thread's copies land
                 ++it;
                 first = false;
                 t = tn;
@@ -256,10 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                 mc = mn;
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        const uint32_t first_q = it >= (uint32_t)(S - 1) ? it - (S - 1) : 0u;
-        for (uint32_t q = first_q; q < it; ++q) mbar_arrive(full0 + 8 * (q % S));
+        cp_async_wait_all();
         if (!ok) atomicOr(a.err, kErrTimeout);
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
@@ -276,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                 while (true) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
+                    fence_proxy_async_smem();  // cp.async (generic proxy) data read by the MMA (async proxy)
                     tc_fence_after();
                     const uint32_t info = s_info[stage];
                     const uint32_t a_base = smem_u32(sA + stage * kABytes);
