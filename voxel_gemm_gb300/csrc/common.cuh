@@ -6,7 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
-#include "../../include/vg.h"
+#include "vg.h"
 
 namespace vg {
 
@@ -45,13 +45,13 @@ struct NbrLayout {
     int cap_log2 = 0;       // hash capacity = 2^cap_log2
     int64_t num_tiles = 0;  // ceil(n / 128)
     int64_t sort_blocks = 0;
-    size_t off_hdr = 0, off_sorted = 0, off_tmask = 0, off_hkeys = 0, off_hvals = 0;
+    int sort_items = 16;    // keys per thread in the radix sort
+    size_t off_hdr = 0, off_sorted = 0, off_tmask = 0, off_table = 0;
     size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, off_nbr_sorted = 0, total = 0;
 };
 
-constexpr int kSortItems = 16;                        // keys per thread in the radix sort
 constexpr int kSortThreads = 256;
-constexpr int kSortTile = kSortItems * kSortThreads;  // keys per sort block
+constexpr int kMaxScanSegs = 1024;                    // segments of the digit-count scan
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kFineOrderBits = 21;                    // fine Morton bits below the tap mask (128^3 blocks)

@@ -199,10 +199,14 @@ __global__ void k_reduce_splits(const float* __restrict__ partial, int splits, i
     out[i] = from_f32<T>(s);
 }
 
-// db partial sums: block b sums rows [b*kDbRows, (b+1)*kDbRows) of dy into
+// db partial sums: block b sums rows [b*rows, (b+1)*rows) of dy into
 // partial_db[b][:].  Thread = (row lane, 8-column group); each thread sums its
 // rows in order, then row lanes are combined in order: a fixed summation order.
-constexpr int kDbRows = 4096;
+// rows = n / (2 * 152) rounded up to a multiple of 256, within [256, 4096].
+__host__ __device__ inline int64_t dbias_rows(int64_t n) {
+    int64_t r = (n / (2 * 152) + 255) / 256 * 256;
+    return r < 256 ? 256 : (r > 4096 ? 4096 : r);
+}
 
 // Eight consecutive elements (16- or 32-byte aligned) as floats.
 __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
@@ -219,14 +223,14 @@ __device__ __forceinline__ void load8(const T* p, float (&v)[8]) {
 
 template <typename T>
 __global__ void __launch_bounds__(256)
-k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, float* __restrict__ partial_db,
+k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows, float* __restrict__ partial_db,
                 const uint32_t* __restrict__ nbr_status) {
     __shared__ float red[256 * 8];
     if (*nbr_status) return;
     const int cg8 = Cout / 8;                      // 8-column groups
     const int lanes = cg8 >= 256 ? 1 : 256 / cg8;  // row lanes per block
     const int tid = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.x * kDbRows, r1 = min(n, r0 + kDbRows);
+    const int64_t r0 = (int64_t)blockIdx.x * rows, r1 = min(n, r0 + rows);
     for (int g0 = 0; g0 < cg8; g0 += 256 / lanes) {
         const int rl = tid / (256 / lanes), g = g0 + tid % (256 / lanes);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -326,13 +330,14 @@ void launch_reduce_splits(const float* partial, int splits, int64_t total, void*
     else reduce_t<__nv_bfloat16>(partial, splits, total, out, nbr_status, s);
 }
 
-int dbias_blocks(int64_t n) { return (int)std::max<int64_t>(1, (n + kDbRows - 1) / kDbRows); }
+int dbias_blocks(int64_t n) { return (int)std::max<int64_t>(1, (n + dbias_rows(n) - 1) / dbias_rows(n)); }
 
 template <typename T>
 static void dbias_t(const void* dy, int64_t n, int Cout, void* db, float* partial_db,
                     const uint32_t* nbr_status, cudaStream_t s) {
     const int R = dbias_blocks(n);
-    k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, partial_db, nbr_status);
+    k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, dbias_rows(n), partial_db,
+                                         nbr_status);
     reduce_t<T>(partial_db, R, Cout, db, nbr_status, s);
 }
 

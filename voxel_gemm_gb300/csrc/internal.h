@@ -10,6 +10,7 @@ namespace vg {
 struct NbrLayout;
 
 int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout* L);
+int nbr_sort_passes(const NbrLayout& l);
 int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
               void* ws, size_t ws_bytes, uint32_t* nbr, uint32_t* mask, cudaStream_t s);
 int nbr_status(const void* ws, cudaStream_t s);

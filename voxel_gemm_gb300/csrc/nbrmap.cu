@@ -14,25 +14,38 @@
 namespace vg {
 
 // ------------------------------------------------------------------ hashing
-// Fibonacci (multiplicative) hashing onto a power-of-two table, linear probing.
-__device__ __forceinline__ uint32_t hash_slot(uint32_t key, int cap_log2) {
-    return (key * 0x9E3779B1u) >> (32 - cap_log2);
+// Open addressing with linear probing over a power-of-two table of slots, each
+// slot holding {key, row} together (one 8- or 16-byte access per probe).  The
+// start slot keeps runs of 8 consecutive linear keys (8 voxels along z) in 8
+// adjacent slots: group = key >> 3 is Fibonacci-hashed to a group of slots and
+// key & 7 picks the slot inside it, so the 27 probes of one voxel touch about a
+// dozen slot groups instead of 27 unrelated slots.
+template <typename K> struct Slot;
+template <> struct Slot<uint32_t> { using T = uint2; };       // {key, row}
+template <> struct Slot<uint64_t> { using T = ulonglong2; };  // {key, row}
+
+__device__ __forceinline__ uint32_t group_hash(uint32_t g, int bits) {
+    return bits > 0 ? (g * 0x9E3779B1u) >> (32 - bits) : 0u;
 }
-__device__ __forceinline__ uint32_t hash_slot(uint64_t key, int cap_log2) {
-    return (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> (64 - cap_log2));
+__device__ __forceinline__ uint32_t group_hash(uint64_t g, int bits) {
+    return bits > 0 ? (uint32_t)((g * 0x9E3779B97F4A7C15ull) >> (64 - bits)) : 0u;
 }
-__device__ __forceinline__ uint32_t cas(uint32_t* p, uint32_t cmp, uint32_t v) {
-    return atomicCAS(reinterpret_cast<unsigned int*>(p), cmp, v);
+template <typename K>
+__device__ __forceinline__ uint32_t start_slot(K key, int cap_log2) {
+    const int gb = cap_log2 - 3;
+    return ((group_hash((K)(key >> 3), gb) << 3) | (uint32_t)(key & 7)) & ((1u << cap_log2) - 1u);
 }
-__device__ __forceinline__ uint64_t cas(uint64_t* p, uint64_t cmp, uint64_t v) {
-    return (uint64_t)atomicCAS(reinterpret_cast<unsigned long long*>(p),
-                               (unsigned long long)cmp, (unsigned long long)v);
+__device__ __forceinline__ uint32_t cas_key(uint2* s, uint32_t cmp, uint32_t v) {
+    return atomicCAS(reinterpret_cast<unsigned int*>(&s->x), cmp, v);
+}
+__device__ __forceinline__ uint64_t cas_key(ulonglong2* s, uint64_t cmp, uint64_t v) {
+    return (uint64_t)atomicCAS(reinterpret_cast<unsigned long long*>(&s->x), (unsigned long long)cmp,
+                               (unsigned long long)v);
 }
 
 template <typename K>
 __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int X, int Y, int Z,
-                         K* __restrict__ hkeys, uint32_t* __restrict__ hvals, int cap_log2,
-                         uint32_t* __restrict__ status) {
+                         typename Slot<K>::T* __restrict__ table, int cap_log2, uint32_t* __restrict__ status) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int4 c = coords[i];
@@ -43,11 +56,11 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
     const K key = (K)((((int64_t)c.x * X + c.y) * Y + c.z) * Z + c.w);
     const uint32_t cmask = (1u << cap_log2) - 1u;
     const K empty = ~K(0);
-    uint32_t slot = hash_slot(key, cap_log2);
+    uint32_t slot = start_slot(key, cap_log2);
     for (uint32_t p = 0; p <= cmask; ++p) {
-        const K prev = cas(&hkeys[slot], empty, key);
+        const K prev = cas_key(&table[slot], empty, key);
         if (prev == empty) {
-            hvals[slot] = (uint32_t)i;
+            table[slot].y = i;
             return;
         }
         if (prev == key) {
@@ -59,63 +72,8 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
     atomicOr(status, kErrFull);
 }
 
-// One thread per (voxel, tap); a block covers 32 voxels x 27 taps so the
-// nbr rows it writes are one contiguous, coalesced range.
-constexpr int kProbeVoxels = 32;
-constexpr int kProbeThreads = kProbeVoxels * kTaps;  // 864
-
-template <typename K>
-__global__ void __launch_bounds__(kProbeThreads)
-k_probe(const int4* __restrict__ coords, int64_t n, int X, int Y, int Z,
-        const K* __restrict__ hkeys, const uint32_t* __restrict__ hvals, int cap_log2,
-        uint32_t* __restrict__ nbr, uint32_t* __restrict__ mask) {
-    __shared__ uint32_t smask[kProbeVoxels];
-    const int t = threadIdx.x;
-    const int local = t / kTaps;
-    const int k = t - local * kTaps;
-    const int64_t i = (int64_t)blockIdx.x * kProbeVoxels + local;
-    if (t < kProbeVoxels) smask[t] = 0;
-    __syncthreads();
-    if (i < n) {
-        const int4 c = coords[i];
-        const int x = c.y + (k / 9 - 1), y = c.z + ((k / 3) % 3 - 1), z = c.w + (k % 3 - 1);
-        uint32_t j = kNone;
-        if (x >= 0 && x < X && y >= 0 && y < Y && z >= 0 && z < Z) {
-            const K key = (K)((((int64_t)c.x * X + x) * Y + y) * Z + z);
-            const uint32_t cmask = (1u << cap_log2) - 1u;
-            const K empty = ~K(0);
-            uint32_t slot = hash_slot(key, cap_log2);
-            for (uint32_t p = 0; p <= cmask; ++p) {
-                const K kk = hkeys[slot];
-                if (kk == key) { j = hvals[slot]; break; }
-                if (kk == empty) break;
-                slot = (slot + 1u) & cmask;
-            }
-        }
-        nbr[i * kTaps + k] = j;
-        if (j != kNone) atomicOr(&smask[local], 1u << k);
-    }
-    __syncthreads();
-    if (t < kProbeVoxels) {
-        const int64_t ii = (int64_t)blockIdx.x * kProbeVoxels + t;
-        if (ii < n) mask[ii] = smask[t];
-    }
-}
-
-// ------------------------------------------------------------------ row order
-// Sort key of voxel i (the page's sorted_idx groups rows for the masked GEMM):
-//   m      = (b << 3L) | interleave(x, y, z)            Morton (z-order) code
-//   key    = ((m >> F) << (27 + F)) | (mask_i << F) | (m & (2^F - 1)),  F = min(3L, 21)
-// i.e. coarse Morton block of 128^3 voxels, then the valid-tap mask, then the
-// fine Morton order.  Rows of one tile then share most of their taps (few
-// zero-filled rows in the MMA) while a block's rows stay spatially close
-// (gathered neighbours are reused from L2).
-template <typename SK>
-__global__ void k_order_key(const int4* __restrict__ coords, const uint32_t* __restrict__ mask, int64_t n,
-                            int L, SK* __restrict__ keys) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int4 c = coords[i];
+// Row-order key of one voxel (see k_key_hist): coarse Morton block, tap mask, fine Morton.
+__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
     uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
     for (int b = 0; b < L; ++b) {
         m |= (uint64_t)(((uint32_t)c.y >> b) & 1u) << (3 * b + 2);
@@ -124,21 +82,103 @@ __global__ void k_order_key(const int4* __restrict__ coords, const uint32_t* __r
     }
     const int F = min(3 * L, kFineOrderBits);
     const uint64_t fine = m & ((uint64_t(1) << F) - 1);
-    keys[i] = (SK)(((m >> F) << (kTaps + F)) | ((uint64_t)mask[i] << F) | fine);
+    return ((m >> F) << (kTaps + F)) | ((uint64_t)mask << F) | fine;
+}
+
+// Probe of the 13 taps k < 13 (offsets with dx < 0, or dx = 0 and dy < 0, or
+// dx = dy = 0 and dz < 0) plus the centre.  Since o_{26-k} = -o_k, finding j at
+// tap k of voxel i also fixes nbr[j][26-k] = i, which this thread writes too;
+// every entry is written by exactly one thread, the rest keep the VG_NONE fill.
+// One block = 32 voxels x 14 threads.
+constexpr int kProbeVoxels = 32;
+constexpr int kHalfTaps = 14;  // taps 0..12 and the centre 13
+constexpr int kProbeThreads = kProbeVoxels * kHalfTaps;  // 448
+
+template <typename K>
+__global__ void __launch_bounds__(kProbeThreads)
+k_probe_half(const int4* __restrict__ coords, int64_t n, int X, int Y, int Z,
+             const typename Slot<K>::T* __restrict__ table, int cap_log2, uint32_t* __restrict__ nbr) {
+    const int t = threadIdx.x;
+    const int local = t / kHalfTaps;
+    const int k = t - local * kHalfTaps;
+    const int64_t i = (int64_t)blockIdx.x * kProbeVoxels + local;
+    if (i >= n) return;
+    if (k == 13) {
+        nbr[i * kTaps + 13] = (uint32_t)i;
+        return;
+    }
+    const int4 c = coords[i];
+    const int x = c.y + (k / 9 - 1), y = c.z + ((k / 3) % 3 - 1), z = c.w + (k % 3 - 1);
+    if (x < 0 || x >= X || y < 0 || y >= Y || z < 0 || z >= Z) return;
+    const K key = (K)((((int64_t)c.x * X + x) * Y + y) * Z + z);
+    const uint32_t cmask = (1u << cap_log2) - 1u;
+    const K empty = ~K(0);
+    uint32_t slot = start_slot(key, cap_log2);
+    for (uint32_t p = 0; p <= cmask; ++p) {
+        const typename Slot<K>::T e = table[slot];
+        if ((K)e.x == key) {
+            const uint32_t j = (uint32_t)e.y;
+            nbr[i * kTaps + k] = j;
+            nbr[(int64_t)j * kTaps + (26 - k)] = (uint32_t)i;
+            return;
+        }
+        if ((K)e.x == empty) return;
+        slot = (slot + 1u) & cmask;
+    }
+}
+
+// Valid-tap mask from a voxel's neighbour row.
+__device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < kTaps; ++k) m |= (row[k] != kNone ? 1u : 0u) << k;
+    return m;
+}
+
+// Row-order sort key of every voxel, its valid-tap mask, and the digit histogram
+// of the first radix pass (same block layout as k_radix_hist):
+//   m   = (b << 3L) | interleave(x, y, z)            Morton (z-order) code
+//   key = ((m >> F) << (27 + F)) | (mask << F) | (m & (2^F - 1)),  F = min(3L, 21)
+// i.e. coarse Morton block of 128^3 voxels, then the valid-tap mask, then the
+// fine Morton order (the page's sorted_idx groups rows for the masked GEMM).
+// Rows of one tile then share most of their taps (few zero-filled rows in the
+// MMA) while a block's rows stay spatially close (neighbours reused from L2).
+template <typename SK>
+__global__ void __launch_bounds__(kSortThreads)
+k_key_hist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L,
+           uint32_t* __restrict__ mask, SK* __restrict__ keys, uint32_t* __restrict__ hist, int64_t nblocks,
+           int items) {
+    __shared__ uint32_t h[kRadix];
+    const int t = threadIdx.x;
+    h[t] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
+    for (int it = 0; it < items; ++it) {
+        const int64_t i = base + (int64_t)it * kSortThreads + t;
+        if (i < n) {
+            const uint32_t m = row_mask(nbr + i * kTaps);
+            mask[i] = m;
+            const SK key = (SK)order_key(coords[i], m, L);
+            keys[i] = key;
+            atomicAdd(&h[(uint32_t)key & (kRadix - 1)], 1u);
+        }
+    }
+    __syncthreads();
+    hist[(int64_t)t * nblocks + blockIdx.x] = h[t];
 }
 
 // Stable LSD radix sort, 8-bit digits.  Pass = histogram -> scan -> scatter.
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
 k_radix_hist(const SK* __restrict__ keys, int64_t n, int shift, uint32_t* __restrict__ hist,
-             int64_t nblocks) {
+             int64_t nblocks, int items) {
     __shared__ uint32_t h[kRadix];
     const int t = threadIdx.x;
     h[t] = 0;
     __syncthreads();
-    const int64_t base = (int64_t)blockIdx.x * kSortTile;
+    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
 #pragma unroll 4
-    for (int it = 0; it < kSortItems; ++it) {
+    for (int it = 0; it < items; ++it) {
         const int64_t idx = base + (int64_t)it * kSortThreads + t;
         if (idx < n) atomicAdd(&h[(uint32_t)(keys[idx] >> shift) & (kRadix - 1)], 1u);
     }
@@ -146,24 +186,27 @@ k_radix_hist(const SK* __restrict__ keys, int64_t n, int shift, uint32_t* __rest
     hist[(int64_t)t * nblocks + blockIdx.x] = h[t];
 }
 
-// Exclusive scan of `total` counters, one block of 1024 threads, each owning a
-// contiguous segment (digit-major, block-minor order gives stable offsets).
-__global__ void __launch_bounds__(1024) k_scan_exclusive(uint32_t* __restrict__ v, int64_t total) {
+// Exclusive scan of the (digit-major, block-minor) digit counts in segments of
+// kScanSeg entries: each block scans one segment in place and writes the
+// segment's total; the scatter kernel adds the prefix of the segment totals.
+constexpr int kScanSeg = 4096;  // 1024 threads x 4 entries
+
+__global__ void __launch_bounds__(1024)
+k_scan_segments(uint32_t* __restrict__ v, int64_t total, uint32_t* __restrict__ seg_total) {
     __shared__ uint32_t wsum[32];
-    const int t = threadIdx.x;
-    const int64_t per = (total + 1023) / 1024;
-    const int64_t b = t * per, e = min(total, b + per);
-    uint32_t s = 0;
-    for (int64_t i = b; i < e; ++i) s += v[i];
-    // inclusive scan of s across the block
-    uint32_t x = s;
-    const int lane = t & 31, w = t >> 5;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int64_t base = (int64_t)blockIdx.x * kScanSeg + 4 * t;
+    uint32_t x[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) x[q] = base + q < total ? v[base + q] : 0u;
+    const uint32_t s = x[0] + x[1] + x[2] + x[3];
+    uint32_t inc = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
     }
-    if (lane == 31) wsum[w] = x;
+    if (lane == 31) wsum[w] = inc;
     __syncthreads();
     if (w == 0) {
         uint32_t y = wsum[lane];
@@ -175,27 +218,58 @@ __global__ void __launch_bounds__(1024) k_scan_exclusive(uint32_t* __restrict__ 
         wsum[lane] = y;
     }
     __syncthreads();
-    uint32_t run = x - s + (w > 0 ? wsum[w - 1] : 0u);
-    for (int64_t i = b; i < e; ++i) {
-        const uint32_t c = v[i];
-        v[i] = run;
-        run += c;
+    uint32_t run = inc - s + (w > 0 ? wsum[w - 1] : 0u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (base + q < total) v[base + q] = run;
+        run += x[q];
     }
+    if (t == 1023) seg_total[blockIdx.x] = wsum[31];
 }
 
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
 k_radix_scatter(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK* __restrict__ kout,
                 uint32_t* __restrict__ vout, int64_t n, int shift,
-                const uint32_t* __restrict__ hist, int64_t nblocks) {
+                const uint32_t* __restrict__ hist, int64_t nblocks, int items,
+                const uint32_t* __restrict__ seg_total, int nseg) {
     constexpr int kWarps = kSortThreads / 32;
     __shared__ uint32_t offs[kRadix];
     __shared__ uint32_t wcount[kWarps][kRadix];
+    __shared__ uint32_t seg_prefix[kMaxScanSegs];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    offs[t] = hist[(int64_t)t * nblocks + blockIdx.x];
-    const int64_t base = (int64_t)blockIdx.x * kSortTile;
+    {  // exclusive prefix of the segment totals (<= 1024: four per thread)
+        __shared__ uint32_t wtot[kWarps];
+        uint32_t x[4], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x[q] = 4 * t + q < nseg ? seg_total[4 * t + q] : 0u;
+            sum += x[q];
+        }
+        uint32_t inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wtot[warp] = inc;
+        __syncthreads();
+        uint32_t run = inc - sum;
+        for (int w = 0; w < warp; ++w) run += wtot[w];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (4 * t + q < nseg) seg_prefix[4 * t + q] = run;
+            run += x[q];
+        }
+    }
+    __syncthreads();
+    {
+        const int64_t e = (int64_t)t * nblocks + blockIdx.x;
+        offs[t] = hist[e] + seg_prefix[e / kScanSeg];
+    }
+    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int it = 0; it < kSortItems; ++it) {
+    for (int it = 0; it < items; ++it) {
         const int64_t idx = base + (int64_t)it * kSortThreads + t;
         const bool valid = idx < n;
         SK key = 0;
@@ -232,12 +306,19 @@ k_radix_scatter(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK
     }
 }
 
+// Per 128-row tile of the processing order: the OR of the rows' tap masks, and
+// the tile's neighbour lists copied into processing order,
+// sorted_nbr[r][k] = nbr[sorted_idx[r]][k] (VG_NONE for padding rows past n).
 __global__ void __launch_bounds__(kTileRows)
-k_tile_mask(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ mask, int64_t n,
-            uint32_t* __restrict__ tmask) {
+k_tile_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
+            const uint32_t* __restrict__ mask, int64_t n, uint32_t* __restrict__ tmask,
+            uint32_t* __restrict__ sorted_nbr) {
+    __shared__ uint32_t rows[kTileRows];
     __shared__ uint32_t w[kTileRows / 32];
     const int64_t r = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
-    uint32_t m = r < n ? mask[sorted_idx[r]] : 0u;
+    const uint32_t v = r < n ? sorted_idx[r] : kNone;
+    rows[threadIdx.x] = v;
+    uint32_t m = v != kNone ? mask[v] : 0u;
     m = __reduce_or_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0) w[threadIdx.x >> 5] = m;
     __syncthreads();
@@ -246,17 +327,12 @@ k_tile_mask(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict_
         for (int i = 0; i < kTileRows / 32; ++i) o |= w[i];
         tmask[blockIdx.x] = o;
     }
-}
-
-// nbr_sorted[r][k] = nbr[sorted_idx[r]][k] for r < n, VG_NONE for the padding rows
-// up to a whole number of 128-row tiles.  One thread per entry (coalesced writes).
-__global__ void k_sort_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
-                            int64_t n, int64_t total, uint32_t* __restrict__ nbr_sorted) {
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= total) return;
-    const int64_t r = e / kTaps;
-    const int k = (int)(e - r * kTaps);
-    nbr_sorted[e] = r < n ? nbr[(int64_t)sorted_idx[r] * kTaps + k] : kNone;
+    uint32_t* dst = sorted_nbr + (int64_t)blockIdx.x * kTileRows * kTaps;
+    for (int e = threadIdx.x; e < kTileRows * kTaps; e += kTileRows) {
+        const int rr = e / kTaps, k = e - rr * kTaps;
+        const uint32_t vv = rows[rr];
+        dst[e] = vv != kNone ? nbr[(int64_t)vv * kTaps + k] : kNone;
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -289,56 +365,62 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
         while ((int64_t(1) << (c + 1)) <= N / 2) ++c;
         l.cap_log2 = c;
     } else {
-        l.cap_log2 = std::max(6, ceil_log2(2 * std::max<int64_t>(N, 1)));
+        l.cap_log2 = std::max(6, ceil_log2(2 * std::max<int64_t>(N, 1)));  // load <= 1/2
     }
     if (l.cap_log2 > 31) return VG_ERR_UNSUPPORTED;
     const size_t cap = size_t(1) << l.cap_log2;
     l.num_tiles = (N + kTileRows - 1) / kTileRows;
-    l.sort_blocks = (N + kSortTile - 1) / kSortTile;
-    const size_t ks = l.key64 ? 8 : 4, ss = l.sort64 ? 8 : 4;
+    // keys per thread in the radix sort: enough blocks to fill the GPU (about
+    // 2 per SM), at most 16 keys per thread
+    const int64_t per_block_target = std::max<int64_t>(1, N / (2 * 152));
+    l.sort_items = (int)std::min<int64_t>(16, std::max<int64_t>(1, (per_block_target + kSortThreads - 1) / kSortThreads));
+    int64_t tile = (int64_t)kSortThreads * l.sort_items;
+    l.sort_blocks = std::max<int64_t>(1, (N + tile - 1) / tile);
+    while ((int64_t)kRadix * l.sort_blocks > (int64_t)kMaxScanSegs * kScanSeg) {  // keep the segments few
+        ++l.sort_items;
+        tile = (int64_t)kSortThreads * l.sort_items;
+        l.sort_blocks = (N + tile - 1) / tile;
+    }
+    const size_t slot = l.key64 ? 16 : 8, ss = l.sort64 ? 8 : 4;
     size_t o = 0;
     l.off_hdr = o;      o += 256;
     l.off_sorted = o;   o += align_up(4 * (size_t)N, 256);
     l.off_tmask = o;    o += align_up(4 * (size_t)l.num_tiles, 256);
     l.off_nbr_sorted = o; o += align_up(4 * (size_t)kTaps * kTileRows * l.num_tiles, 256);
-    l.off_hkeys = o;    o += align_up(ks * cap, 256);
-    l.off_hvals = o;    o += align_up(4 * cap, 256);
+    l.off_table = o;    o += align_up(slot * cap, 256);
     l.off_skeys_a = o;  o += align_up(ss * (size_t)N, 256);
     l.off_skeys_b = o;  o += align_up(ss * (size_t)N, 256);
     l.off_svals_b = o;  o += align_up(4 * (size_t)N, 256);
-    l.off_hist = o;     o += align_up(4 * (size_t)kRadix * l.sort_blocks, 256);
+    l.off_hist = o;     o += align_up(4 * ((size_t)kRadix * l.sort_blocks + kMaxScanSegs), 256);
     l.total = o;
     *L = l;
     return VG_OK;
 }
 
-template <typename K>
-static void launch_hash(const int4* coords, const NbrLayout& l, int B, int X, int Y, int Z,
-                        char* ws, uint32_t* nbr, uint32_t* mask, cudaStream_t s) {
+int nbr_sort_passes(const NbrLayout& l) { return std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits); }
+
+template <typename K, typename SK>
+static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, int Y, int Z, char* ws,
+                         uint32_t* nbr, uint32_t* mask, cudaStream_t s) {
     const int64_t n = l.n;
-    K* hk = reinterpret_cast<K*>(ws + l.off_hkeys);
-    uint32_t* hv = reinterpret_cast<uint32_t*>(ws + l.off_hvals);
+    using T = typename Slot<K>::T;
+    T* table = reinterpret_cast<T*>(ws + l.off_table);
     uint32_t* status = reinterpret_cast<uint32_t*>(ws + l.off_hdr);
     const size_t cap = size_t(1) << l.cap_log2;
-    cudaMemsetAsync(hk, 0xFF, cap * sizeof(K), s);
-    k_insert<K><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(coords, n, B, X, Y, Z, hk, hv,
-                                                          l.cap_log2, status);
-    k_probe<K><<<(unsigned)((n + kProbeVoxels - 1) / kProbeVoxels), kProbeThreads, 0, s>>>(
-        coords, n, X, Y, Z, hk, hv, l.cap_log2, nbr, mask);
-}
-
-template <typename SK>
-static void launch_sort(const int4* coords, const uint32_t* mask, const NbrLayout& l, int X, int Y, int Z,
-                        char* ws, cudaStream_t s) {
-    const int64_t n = l.n;
     const int L = ceil_log2(std::max(X, std::max(Y, Z)));
     SK* ka = reinterpret_cast<SK*>(ws + l.off_skeys_a);
     SK* kb = reinterpret_cast<SK*>(ws + l.off_skeys_b);
     uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + l.off_sorted);
     uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + l.off_svals_b);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + l.off_hist);
-    k_order_key<SK><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(coords, mask, n, L, ka);
-    const int passes = std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits);
+    uint32_t* seg_total = hist + kRadix * l.sort_blocks;
+
+    cudaMemsetAsync(table, 0xFF, cap * sizeof(T), s);  // empty keys (row fields are don't-care)
+    cudaMemsetAsync(nbr, 0xFF, (size_t)n * kTaps * sizeof(uint32_t), s);  // VG_NONE everywhere
+    k_insert<K><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(coords, n, B, X, Y, Z, table, l.cap_log2, status);
+    k_probe_half<K><<<(unsigned)((n + kProbeVoxels - 1) / kProbeVoxels), kProbeThreads, 0, s>>>(
+        coords, n, X, Y, Z, table, l.cap_log2, nbr);
+    const int passes = nbr_sort_passes(l);
     const unsigned g = (unsigned)l.sort_blocks;
     const uint32_t* vin = nullptr;
     for (int p = 0; p < passes; ++p) {
@@ -346,12 +428,21 @@ static void launch_sort(const int4* coords, const uint32_t* mask, const NbrLayou
         SK* kout = (p % 2 == 0) ? kb : ka;
         uint32_t* vout = ((passes - 1 - p) % 2 == 0) ? v0 : v1;
         const int shift = p * kRadixBits;
-        k_radix_hist<SK><<<g, kSortThreads, 0, s>>>(kin, n, shift, hist, l.sort_blocks);
-        k_scan_exclusive<<<1, 1024, 0, s>>>(hist, (int64_t)kRadix * l.sort_blocks);
-        k_radix_scatter<SK><<<g, kSortThreads, 0, s>>>(kin, vin, kout, vout, n, shift, hist,
-                                                      l.sort_blocks);
+        if (p == 0)
+            k_key_hist<SK><<<g, kSortThreads, 0, s>>>(coords, nbr, n, L, mask, ka, hist, l.sort_blocks,
+                                                     l.sort_items);
+        else
+            k_radix_hist<SK><<<g, kSortThreads, 0, s>>>(kin, n, shift, hist, l.sort_blocks, l.sort_items);
+        const int64_t total = (int64_t)kRadix * l.sort_blocks;
+        const int nseg = (int)((total + kScanSeg - 1) / kScanSeg);
+        k_scan_segments<<<nseg, 1024, 0, s>>>(hist, total, seg_total);
+        k_radix_scatter<SK><<<g, kSortThreads, 0, s>>>(kin, vin, kout, vout, n, shift, hist, l.sort_blocks,
+                                                      l.sort_items, seg_total, nseg);
         vin = vout;
     }
+    k_tile_rows<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
+        v0, nbr, mask, n, reinterpret_cast<uint32_t*>(ws + l.off_tmask),
+        reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted));
 }
 
 int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
@@ -370,17 +461,13 @@ int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsi
     cudaMemsetAsync(ws + l.off_hdr, 0, 256, s);
     if (N > 0) {
         const int4* c4 = reinterpret_cast<const int4*>(coords);
-        if (l.key64) launch_hash<uint64_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
-        else launch_hash<uint32_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
-        if (l.sort64) launch_sort<uint64_t>(c4, mask, l, X, Y, Z, ws, s);
-        else launch_sort<uint32_t>(c4, mask, l, X, Y, Z, ws, s);
-        k_tile_mask<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
-            reinterpret_cast<const uint32_t*>(ws + l.off_sorted), mask, N,
-            reinterpret_cast<uint32_t*>(ws + l.off_tmask));
-        const int64_t total = (int64_t)kTaps * kTileRows * l.num_tiles;
-        k_sort_rows<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-            reinterpret_cast<const uint32_t*>(ws + l.off_sorted), nbr, N, total,
-            reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted));
+        if (l.key64) {
+            if (l.sort64) launch_build<uint64_t, uint64_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
+            else launch_build<uint64_t, uint32_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
+        } else {
+            if (l.sort64) launch_build<uint32_t, uint64_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
+            else launch_build<uint32_t, uint32_t>(c4, l, B, X, Y, Z, ws, nbr, mask, s);
+        }
     }
     return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
 }

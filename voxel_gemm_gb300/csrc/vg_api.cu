@@ -100,11 +100,11 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     NbrLayout l;
     const int st = nbr_layout(N, B, X, Y, Z, flags, &l);
     if (st != VG_OK || !info) return st != VG_OK ? st : VG_ERR_INVALID_ARG;
-    const int passes = std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits);
+    const int passes = nbr_sort_passes(l);
     info[0] = l.key64;
     info[1] = l.sort_bits;
     info[2] = passes;
-    info[3] = N > 0 ? 3 + 3 * passes + 2 : 0;  // insert, probe, key, passes x (hist, scan, scatter), tile masks, sorted rows
+    info[3] = N > 0 ? 2 + 3 * passes + 1 : 0;  // insert, probe+key, passes x (hist, scan, scatter), tile rows
     return VG_OK;
 }
 

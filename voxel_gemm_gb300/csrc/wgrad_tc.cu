@@ -6,7 +6,8 @@
 // split-K "reduces the accumulation bottleneck for large K"; here K is the
 // voxel count).
 //
-// One MMA tile: D[128 x BN] in TMEM, D[m][n] += sum over 64-row stages of
+// One MMA tile: D[128 x BN] in TMEM (two per work unit, sharing each dY stage),
+// D[m][n] += sum over 64-row stages of
 //   A[m][row] = f[nbr[row][tap(m)]][ci(m)]   (gathered feature rows)
 //   B[n][row] = dY[row][co0 + n]
 // Both operands are stored as rows of the sorted order, i.e. MN-major: a row
@@ -34,13 +35,19 @@ constexpr int kThreads = 288;
 constexpr int kRowsPerStage = 64;
 constexpr int kABytes = 2 * kRowsPerStage * 128;  // two 64-channel blocks x 64 rows
 
+// MU M blocks share every dY stage (their accumulators sit side by side in
+// TMEM); two accumulator sets alternate when they fit in 512 columns.
 template <int BN>
 struct WCfg {
-    static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int MU = 2;
+    static constexpr int kAccCols = MU * BN;
+    static constexpr int NBUF = 2 * kAccCols <= 512 ? 2 : 1;
+    static constexpr int kTmemCols = NBUF * kAccCols;
     static constexpr int kBBytes = (BN / 64) * kRowsPerStage * 128;
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kStageBytes = MU * kABytes + kBBytes;
+    static constexpr int S = 196608 / kStageBytes;  // 192 KB of stages
     static constexpr int kNumBars = 2 * S + 5;
-    static constexpr size_t kSmem = 1024 + (size_t)S * (kABytes + kBBytes) + 8 * kNumBars + 4 * S + 16;
+    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 4 * S + 16;
 };
 
 struct WgArgs {
@@ -72,6 +79,11 @@ __device__ __forceinline__ MUnit munit(int m, int Cin) {
     const int CB = Cin / 64;
     const int s0 = 2 * m, s1 = 2 * m + 1;
     MUnit r;
+    if (s0 >= kTaps * CB) {  // past the last slot (a partial group of M blocks): all zero
+        r.tap0 = r.tap1 = -1;
+        r.c0 = r.c1 = 0;
+        return r;
+    }
     r.tap0 = s0 / CB;
     r.c0 = (s0 % CB) * 64;
     if (s1 < kTaps * CB) {
@@ -84,18 +96,25 @@ __device__ __forceinline__ MUnit munit(int m, int Cin) {
     return r;
 }
 
-// Row metadata a gather thread needs for one stage (its four rows).
+// Row metadata a gather thread needs for one stage (its four rows): the dY row
+// and, for each of the unit's MU M blocks, the neighbour rows of its two taps.
+template <int MU>
 struct Meta {
-    uint32_t i[4], j0[4], j1[4];
+    uint32_t i[4], j0[MU][4], j1[MU][4];
 };
 
-__device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit& mu, int64_t row0, int p, Meta& m) {
+template <int MU>
+__device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit (&mu)[MU], int64_t row0, int p,
+                                          Meta<MU>& m) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int64_t r = row0 + (p >> 3) + 16 * q;  // r < num_tiles * 128 always
         m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
-        m.j0[q] = a.sorted_nbr[r * kTaps + mu.tap0];
-        m.j1[q] = mu.tap1 >= 0 ? a.sorted_nbr[r * kTaps + mu.tap1] : kNone;
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+            m.j0[u][q] = mu[u].tap0 >= 0 ? a.sorted_nbr[r * kTaps + mu[u].tap0] : kNone;
+            m.j1[u][q] = mu[u].tap1 >= 0 ? a.sorted_nbr[r * kTaps + mu[u].tap1] : kNone;
+        }
     }
 }
 
@@ -128,12 +147,13 @@ template <int BN, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
     using C = WCfg<BN>;
     constexpr int S = C::S;
+    constexpr int MU = C::MU;
+    constexpr int NBUF = C::NBUF;
     constexpr int NBB = BN / 64;  // 64-column blocks of B
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + (size_t)S * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * C::kBBytes);
+    uint8_t* stages = smem;  // stage g: MU A tiles (16 KB each), then the B tile
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)S * C::kStageBytes);
     uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
     uint32_t* s_tmem = s_info + S;
     volatile uint32_t* s_abort = s_tmem + 1;
@@ -167,8 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
     const uint32_t tmem = *s_tmem;
 
     const int M = num_munits(a.Cin);
+    const int MG = (M + MU - 1) / MU;  // groups of MU M blocks
     const int NB = a.Cout / BN;
-    const int64_t units = (int64_t)M * NB * a.splits;
+    const int64_t units = (int64_t)MG * NB * a.splits;
 
     if (warp < 4) {
         // ------------------------------------------------------------ gather producer
@@ -177,12 +198,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
         uint32_t it = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int m = (int)(u % M);
-            const int64_t rest = u / M;
+            const int mg = (int)(u % MG);
+            const int64_t rest = u / MG;
             const int nb = (int)(rest % NB);
             const int64_t s = rest / NB;
-            const MUnit mu = munit(m, a.Cin);
-            const uint32_t umask = (1u << mu.tap0) | (mu.tap1 >= 0 ? 1u << mu.tap1 : 0u);
+            MUnit mu[MU];
+            uint32_t umask = 0;
+#pragma unroll
+            for (int v = 0; v < MU; ++v) {
+                mu[v] = munit(mg * MU + v, a.Cin);
+                if (mu[v].tap0 >= 0) umask |= 1u << mu[v].tap0;
+                if (mu[v].tap1 >= 0) umask |= 1u << mu[v].tap1;
+            }
             const int64_t t_first = s * a.tiles_per_chunk;
             TileCursor cur;
             cur.base = t_first;
@@ -190,13 +217,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
             cur.bits = window_bits(a, cur.base, cur.end, t_first, umask, lane);
             int64_t t = next_tile(a, cur, t_first, umask, lane);  // the first tile is always active
             int h = 0;
-            Meta mc, mn;
+            Meta<MU> mc, mn;
             bool null_stage = false;
             if (t >= 0) {
-                load_meta(a, mu, t * 128, p, mc);
+                load_meta<MU>(a, mu, t * 128, p, mc);
             } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
                 null_stage = true;
-                for (int q = 0; q < 4; ++q) mc.i[q] = mc.j0[q] = mc.j1[q] = kNone;
+                for (int q = 0; q < 4; ++q) {
+                    mc.i[q] = kNone;
+                    for (int v = 0; v < MU; ++v) mc.j0[v][q] = mc.j1[v][q] = kNone;
+                }
             }
             bool first = true;
             while (t >= 0 || null_stage) {
@@ -210,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     tn = next_tile(a, cur, t_first, umask, lane);
                     hn = 0;
                 }
-                if (tn >= 0) load_meta(a, mu, tn * 128 + hn * 64, p, mn);
+                if (tn >= 0) load_meta<MU>(a, mu, tn * 128 + hn * 64, p, mn);
                 const uint32_t stage = it % S, ph = (it / S) & 1u;
-                // warp-uniform decision: the tile cursor below uses warp-wide ballots
+                // warp-uniform decision: the tile cursor uses warp-wide ballots
                 if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort))) {
                     ok = false;
                     *s_abort = 1;
@@ -222,26 +252,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
                     mbar_arrive(full0 + 8 * stage);
                 }
-                const uint32_t a_base = smem_u32(sA + stage * kABytes);
-                const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+                uint8_t* st = stages + (size_t)stage * C::kStageBytes;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {  // A: block e/4, row (p>>3) + 16*(e%4)
-                    const int q = e & 3, blk = e >> 2;
-                    const int row = (p >> 3) + 16 * q;
-                    const uint32_t j = blk ? mc.j1[q] : mc.j0[q];
-                    const int c = blk ? mu.c1 : mu.c0;
-                    const uint16_t* src = a.f + (int64_t)(j != kNone ? j : 0u) * a.Cin + c + ch * 8;
-                    cp_async16(a_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
-                                   ((ch ^ (row & 7)) << 4),
-                               src, j != kNone ? 16u : 0u);
+                for (int v = 0; v < MU; ++v) {
+                    const uint32_t a_base = smem_u32(st + v * kABytes);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {  // A: block e/4, row (p>>3) + 16*(e%4)
+                        const int q = e & 3, blk = e >> 2;
+                        const int row = (p >> 3) + 16 * q;
+                        const uint32_t j = blk ? mc.j1[v][q] : mc.j0[v][q];
+                        const int c = blk ? mu[v].c1 : mu[v].c0;
+                        const uint16_t* src = a.f + (int64_t)(j != kNone ? j : 0u) * a.Cin + c + ch * 8;
+                        cp_async16(a_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
+                                       ((ch ^ (row & 7)) << 4),
+                                   src, j != kNone ? 16u : 0u);
+                    }
                 }
+                const uint32_t b_base = smem_u32(st + MU * kABytes);
 #pragma unroll
                 for (int e = 0; e < 4 * NBB; ++e) {  // B: block e/4, same four rows
                     const int q = e & 3, blk = e >> 2;
                     const int row = (p >> 3) + 16 * q;
                     const uint32_t i = mc.i[q];
-                    // rows with neither tap contribute nothing: skip their dY bytes
-                    const bool use = i != kNone && (mc.j0[q] != kNone || mc.j1[q] != kNone);
+                    // rows with none of the unit's taps contribute nothing: skip their dY bytes
+                    bool use = false;
+#pragma unroll
+                    for (int v = 0; v < MU; ++v) use |= mc.j0[v][q] != kNone || mc.j1[v][q] != kNone;
+                    use = use && i != kNone;
                     const uint16_t* src = a.dy + (int64_t)(use ? i : 0u) * a.Cout + nb * BN + blk * 64 + ch * 8;
                     cp_async16(b_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
                                    ((ch ^ (row & 7)) << 4),
@@ -265,23 +302,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
             uint32_t it = 0, ua = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
-                const uint32_t buf = ua & 1u;
-                if (!mbar_wait(tempty0 + 8 * buf, ((ua >> 1) & 1u) ^ 1u, s_abort)) { ok = false; break; }
+                const uint32_t buf = ua % NBUF;
+                if (!mbar_wait(tempty0 + 8 * buf, ((ua / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + buf * BN;
                 while (true) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
                     fence_proxy_async_smem();  // cp.async (generic proxy) data read by the MMA (async proxy)
                     tc_fence_after();
                     const uint32_t info = s_info[stage];
-                    const uint32_t a_base = smem_u32(sA + stage * kABytes);
-                    const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+                    const uint8_t* st = stages + (size_t)stage * C::kStageBytes;
+                    const uint32_t b_base = smem_u32(st + MU * kABytes);
 #pragma unroll
-                    for (int j = 0; j < kRowsPerStage / 16; ++j) {
-                        mma_f16(d_tmem, sw128_mnmajor_desc(a_base + 2048 * j, lbo),
-                                sw128_mnmajor_desc(b_base + 2048 * j, lbo), idesc,
-                                ((info & 1u) && j == 0) ? 0u : 1u);
+                    for (int v = 0; v < MU; ++v) {
+                        const uint32_t a_base = smem_u32(st + v * kABytes);
+                        const uint32_t d_tmem = tmem + buf * C::kAccCols + v * BN;
+#pragma unroll
+                        for (int j = 0; j < kRowsPerStage / 16; ++j) {
+                            mma_f16(d_tmem, sw128_mnmajor_desc(a_base + 2048 * j, lbo),
+                                    sw128_mnmajor_desc(b_base + 2048 * j, lbo), idesc,
+                                    ((info & 1u) && j == 0) ? 0u : 1u);
+                        }
                     }
                     mma_commit(empty0 + 8 * stage);
                     ++it;
@@ -303,32 +344,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
         uint32_t ua = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
-            const int m = (int)(u % M);
-            const int64_t rest = u / M;
+            const int mg = (int)(u % MG);
+            const int64_t rest = u / MG;
             const int nb = (int)(rest % NB);
             const int64_t s = rest / NB;
-            const uint32_t buf = ua & 1u;
-            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua >> 1) & 1u, s_abort));
+            const uint32_t buf = ua % NBUF;
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua / NBUF) & 1u, s_abort));
             if (!ok) break;
             tc_fence_after();
-            const MUnit mu = munit(m, a.Cin);
             const int mrow = q * 32 + lane;  // M index: block mrow / 64, channel mrow % 64
             const int blk = mrow >> 6;
-            const int tap = blk ? mu.tap1 : mu.tap0;
-            const int ci = (blk ? mu.c1 : mu.c0) + (mrow & 63);
-            float* dst = tap >= 0 ? a.partial + ((s * kTaps + tap) * a.Cin + ci) * (int64_t)a.Cout + nb * BN
-                                  : nullptr;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t acc[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
-                tmem_ld_wait();
-                if (dst) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + c0);
+            for (int v = 0; v < MU; ++v) {
+                const MUnit muv = munit(mg * MU + v, a.Cin);
+                const int tap = blk ? muv.tap1 : muv.tap0;
+                const int ci = (blk ? muv.c1 : muv.c0) + (mrow & 63);
+                float* dst = tap >= 0 ? a.partial + ((s * kTaps + tap) * a.Cin + ci) * (int64_t)a.Cout + nb * BN
+                                      : nullptr;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t acc[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * C::kAccCols + v * BN + c0, acc);
+                    tmem_ld_wait();
+                    if (dst) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + c0);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
-                                            __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
+                        for (int i = 0; i < 8; ++i)
+                            d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                                                __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
+                    }
                 }
             }
             tc_fence_before();
@@ -366,8 +410,8 @@ int launch_wgrad(const WgArgs& a, cudaStream_t s) {
     auto kern = k_wgrad_tc<BN, BF16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
-    const int M = num_munits(a.Cin);
-    const int64_t units = (int64_t)M * (a.Cout / BN) * a.splits;
+    const int MG = (num_munits(a.Cin) + C::MU - 1) / C::MU;
+    const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, sm_count_w());
     kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
@@ -379,8 +423,8 @@ int launch_wgrad(const WgArgs& a, cudaStream_t s) {
 // partial sums capped at 1 GiB.
 int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
-    const int64_t M = num_munits(Cin);
-    const int64_t per_split = M * (Cout / wg_bn(Cout));
+    const int64_t MG = (num_munits(Cin) + 1) / 2;  // M blocks are taken two per unit
+    const int64_t per_split = MG * (Cout / wg_bn(Cout));
     int64_t S = std::max<int64_t>(1, (4 * 152 + per_split - 1) / per_split);
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
