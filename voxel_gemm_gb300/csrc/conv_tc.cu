@@ -14,8 +14,9 @@
 //              thread's copies arrive on the stage barrier by themselves
 //              (cp.async.mbarrier.arrive.noinc), so up to S stages are in flight;
 //              thread 0 also bulk-copies the prepacked weight tile (TMA engine)
-//              and, one unit ahead, the tile's 13.5 KB neighbour block; rows of
-//              taps a few stages ahead are pulled into L2 by prefetch.
+//              and, one unit ahead, the tile's 13.5 KB neighbour block.  (L2
+//              prefetching of later taps' rows was measured to slow the gathers:
+//              the prefetches occupy the same per-SM request slots.)
 //   warp 4     TMEM allocation and the single MMA-issuing thread:
 //              tcgen05.mma M=128, N=BN, K=16, fp32 accumulators in TMEM,
 //              two accumulator buffers so the epilogue overlaps the next tile.
@@ -35,7 +36,6 @@ constexpr int kThreads = 288;          // 9 warps
 constexpr int kBM = 128;               // rows per tile (MMA M)
 constexpr int kBK = 64;                // 16-bit elements per K block (128 bytes)
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kPrefetchStages = 6;      // L2 prefetch distance of gathered rows, in pipeline stages
 
 int choose_bn(int ndim) {
     if (ndim % 256 == 0) return 256;
@@ -173,36 +173,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             const uint32_t* nb_tile = s_nbr + buf * kBM * kTaps;
             for (int k = 0; k < kTaps && ok; ++k) {
                 if (!((tm >> k) & 1u)) continue;
-                {
-                    // L2 prefetch of the rows of the tap PT active taps ahead (about kPrefetchStages
-                    // stages), so the gathers that reach it find their rows in L2; past the end of
-                    // this tile the look-ahead continues into the next unit's neighbour block.
-                    const int PT = (kPrefetchStages + KB - 1) / KB;
-                    const uint32_t after = tm & ~((2u << k) - 1u);
-                    const int rem = __popc(after);
-                    const uint32_t* src_tile = nullptr;
-                    int k2 = -1;
-                    if (rem >= PT) {
-                        uint32_t m = after;
-                        for (int i = 1; i < PT; ++i) m &= m - 1u;
-                        k2 = __ffs(m) - 1;
-                        src_tile = nb_tile;
-                    } else if (un < units && mbar_wait_timed(nbar0 + 8 * (buf ^ 1u), ((idx + 1) >> 1) & 1u)) {
-                        uint32_t m = tm_next;
-                        for (int i = 0; i < PT - 1 - rem && m; ++i) m &= m - 1u;
-                        if (m) {
-                            k2 = __ffs(m) - 1;
-                            src_tile = s_nbr + (buf ^ 1u) * kBM * kTaps;
-                        }
-                    }
-                    if (k2 >= 0) {
-                        const uint32_t j = src_tile[p * kTaps + k2];
-                        if (j != kNone) {
-                            const uint8_t* row = reinterpret_cast<const uint8_t*>(a.A + (int64_t)j * a.Kdim);
-                            for (int l = 0; l < KB; ++l) prefetch_l2(row + l * 128);
-                        }
-                    }
-                }
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
