@@ -112,8 +112,9 @@ VG_API int vg_nbrmap_build(const int32_t* coords, int64_t N, int B, int X, int Y
                     uint32_t* nbr, uint32_t* mask, void* stream);
 
 /* Synchronises `stream` and returns the data-dependent status of the last build
- * into ws (VG_OK, VG_ERR_COORD_OUT_OF_RANGE, VG_ERR_DUPLICATE_COORD or
- * VG_ERR_HASH_FULL; the first in that order if several apply). */
+ * into ws (VG_OK, VG_ERR_COORD_OUT_OF_RANGE, VG_ERR_DUPLICATE_COORD,
+ * VG_ERR_HASH_FULL or VG_ERR_DEVICE_TIMEOUT when a bounded wait of the sort
+ * gave up; the first in that order if several apply). */
 VG_API int vg_nbrmap_status(const void* ws, void* stream);
 
 /* Device pointers into a built workspace (no device access, no sync):

@@ -48,10 +48,11 @@ struct NbrLayout {
     int sort_items = 16;    // keys per thread in the radix sort
     size_t off_hdr = 0, off_sorted = 0, off_tmask = 0, off_table = 0;
     size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, off_nbr_sorted = 0, total = 0;
+    size_t off_status = 0, off_tickets = 0;
 };
 
 constexpr int kSortThreads = 256;
-constexpr int kMaxScanSegs = 1024;                    // segments of the digit-count scan
+constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digits
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kFineOrderBits = 21;                    // fine Morton bits below the tap mask (128^3 blocks)

@@ -36,6 +36,7 @@ constexpr int kThreads = 288;          // 9 warps
 constexpr int kBM = 128;               // rows per tile (MMA M)
 constexpr int kBK = 64;                // 16-bit elements per K block (128 bytes)
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kMaxBiasCols = 2048;     // bias staged in shared memory (16-bit) up to this many columns
 
 int choose_bn(int ndim) {
     if (ndim % 256 == 0) return 256;
@@ -47,12 +48,14 @@ template <int BN>
 struct Cfg {
     static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);  // pipeline stages
     static constexpr int kBBytes = BN * kBK * 2;
-    static constexpr int kTmemCols = 2 * BN;                         // two accumulators
+    static constexpr int NBUF = BN <= 128 ? 4 : 2;                  // TMEM accumulator buffers
+    static constexpr int kTmemCols = NBUF * BN;                      // 256 or 512 columns
     static constexpr size_t kSmemA = (size_t)S * kABytes;
     static constexpr size_t kSmemB = (size_t)S * kBBytes;
     static constexpr size_t kNbrTileBytes = (size_t)kBM * kTaps * 4;  // one tile of neighbour lists
-    static constexpr int kNumBars = 2 * S + 7;  // full[S], empty[S], tfull x2, tempty x2, done, nbr x2
-    static constexpr size_t kSmem = 1024 + kSmemA + kSmemB + 2 * kNbrTileBytes + 8 * kNumBars + 16;
+    static constexpr int kNumBars = 2 * S + 2 * NBUF + 3;  // full, empty, tfull, tempty, done, nbr x2
+    static constexpr size_t kSmem = 1024 + kSmemA + kSmemB + 2 * kNbrTileBytes + 8 * kNumBars + 16 +
+                                    2 * kMaxBiasCols;
 };
 
 struct TcArgs {
@@ -99,20 +102,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_nbr + 2 * kBM * kTaps);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile uint32_t* s_abort = s_tmem + 1;
+    uint16_t* s_bias = reinterpret_cast<uint16_t*>(s_tmem + 4);  // [Ndim] when bias is given
 
     if (*a.nbr_status) return;  // bad neighbour map: write nothing (uniform over the block)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
-    const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
-    const uint32_t nbar0 = smem_u32(bars + 2 * S + 5);
+    constexpr int NBUF = C::NBUF;
+    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + NBUF);
+    const uint32_t done_bar = smem_u32(bars + 2 * S + 2 * NBUF);
+    const uint32_t nbar0 = smem_u32(bars + 2 * S + 2 * NBUF + 1);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, 128 + 1);  // 128 gather threads + the weight-tile expect_tx
             mbar_init(empty0 + 8 * i, 1);       // one tcgen05.commit
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NBUF; ++i) {
             mbar_init(tfull0 + 8 * i, 1);
             mbar_init(tempty0 + 8 * i, 4);      // one arrive per epilogue warp
         }
@@ -126,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
         tmem_relinquish();
     }
+    if (a.bias)
+        for (int c = threadIdx.x; c < a.Ndim; c += kThreads) s_bias[c] = a.bias[c];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -211,10 +218,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             bool ok = true;
             uint32_t tm_next = (int64_t)blockIdx.x < units ? a.tile_mask[blockIdx.x / NB] : 0u;
             for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
-                const uint32_t buf = ua & 1u;
+                const uint32_t buf = ua % NBUF;
                 const uint32_t tm = tm_next;
                 if (u + gridDim.x < units) tm_next = a.tile_mask[(u + gridDim.x) / NB];
-                if (!mbar_wait(tempty0 + 8 * buf, ((ua >> 1) & 1u) ^ 1u, s_abort)) { ok = false; break; }
+                if (!mbar_wait(tempty0 + 8 * buf, ((ua / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * BN;
                 uint32_t acc = 0;
@@ -255,15 +262,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         uint32_t ua = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
+        int64_t u = blockIdx.x;
+        // output row of this thread for the next unit, loaded one unit ahead
+        uint32_t v_next = kNone;
+        if (u < units) {
+            const int64_t r = (u / NB) * kBM + q * 32 + lane;
+            v_next = r < a.n ? a.sorted_idx[r] : kNone;
+        }
+        for (; u < units; u += gridDim.x, ++ua) {
             const int64_t t = u / NB;
             const int nb = (int)(u - t * NB);
-            const uint32_t buf = ua & 1u;
-            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua >> 1) & 1u, s_abort));
+            const uint32_t buf = ua % NBUF;
+            const uint32_t v = v_next;
+            if (u + gridDim.x < units) {
+                const int64_t r = ((u + gridDim.x) / NB) * kBM + q * 32 + lane;
+                v_next = r < a.n ? a.sorted_idx[r] : kNone;
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua / NBUF) & 1u, s_abort));
             if (!ok) break;  // warp-uniform
             tc_fence_after();
-            const int64_t r = t * kBM + q * 32 + lane;
-            const uint32_t v = r < a.n ? a.sorted_idx[r] : kNone;
             const int col0 = nb * BN;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -276,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                     for (int i = 0; i < 16; ++i) {
                         float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
                         if (a.bias) {
-                            lo += bits_to_f32<BF16>(a.bias[col0 + c0 + 2 * i]);
-                            hi += bits_to_f32<BF16>(a.bias[col0 + c0 + 2 * i + 1]);
+                            lo += bits_to_f32<BF16>(s_bias[col0 + c0 + 2 * i]);
+                            hi += bits_to_f32<BF16>(s_bias[col0 + c0 + 2 * i + 1]);
                         }
                         pk[i] = pack2<BF16>(lo, hi);
                     }
@@ -381,6 +398,7 @@ int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void
 
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     if (p.n == 0) return VG_OK;
+    if (p.bias && p.Ndim > kMaxBiasCols) return VG_ERR_UNSUPPORTED;
     TcArgs a;
     a.sorted_idx = p.sorted_idx;
     a.tile_mask = p.tile_mask;

@@ -135,8 +135,8 @@ __device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
     return m;
 }
 
-// Row-order sort key of every voxel, its valid-tap mask, and the digit histogram
-// of the first radix pass (same block layout as k_radix_hist):
+// Row-order sort key of every voxel, its valid-tap mask, and the digit
+// histograms of every radix pass (all passes in one read of the keys):
 //   m   = (b << 3L) | interleave(x, y, z)            Morton (z-order) code
 //   key = ((m >> F) << (27 + F)) | (mask << F) | (m & (2^F - 1)),  F = min(3L, 21)
 // i.e. coarse Morton block of 128^3 voxels, then the valid-tap mask, then the
@@ -145,140 +145,143 @@ __device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
 // MMA) while a block's rows stay spatially close (neighbours reused from L2).
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
-k_key_hist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L,
-           uint32_t* __restrict__ mask, SK* __restrict__ keys, uint32_t* __restrict__ hist, int64_t nblocks,
-           int items) {
-    __shared__ uint32_t h[kRadix];
+k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L,
+                 int passes, uint32_t* __restrict__ mask, SK* __restrict__ keys, uint32_t* __restrict__ ghist) {
+    __shared__ uint32_t h[kMaxSortPasses][kRadix];
     const int t = threadIdx.x;
-    h[t] = 0;
+    for (int p = 0; p < passes; ++p) h[p][t] = 0;
     __syncthreads();
-    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
-    for (int it = 0; it < items; ++it) {
-        const int64_t i = base + (int64_t)it * kSortThreads + t;
-        if (i < n) {
-            const uint32_t m = row_mask(nbr + i * kTaps);
-            mask[i] = m;
-            const SK key = (SK)order_key(coords[i], m, L);
-            keys[i] = key;
-            atomicAdd(&h[(uint32_t)key & (kRadix - 1)], 1u);
-        }
+    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + t; i < n; i += (int64_t)gridDim.x * kSortThreads) {
+        const uint32_t m = row_mask(nbr + i * kTaps);
+        mask[i] = m;
+        const SK key = (SK)order_key(coords[i], m, L);
+        keys[i] = key;
+        for (int p = 0; p < passes; ++p) atomicAdd(&h[p][(uint32_t)(key >> (p * kRadixBits)) & (kRadix - 1)], 1u);
     }
     __syncthreads();
-    hist[(int64_t)t * nblocks + blockIdx.x] = h[t];
+    for (int p = 0; p < passes; ++p)
+        if (h[p][t]) atomicAdd(&ghist[p * kRadix + t], h[p][t]);
 }
 
-// Stable LSD radix sort, 8-bit digits.  Pass = histogram -> scan -> scatter.
-template <typename SK>
-__global__ void __launch_bounds__(kSortThreads)
-k_radix_hist(const SK* __restrict__ keys, int64_t n, int shift, uint32_t* __restrict__ hist,
-             int64_t nblocks, int items) {
-    __shared__ uint32_t h[kRadix];
-    const int t = threadIdx.x;
-    h[t] = 0;
-    __syncthreads();
-    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
-#pragma unroll 4
-    for (int it = 0; it < items; ++it) {
-        const int64_t idx = base + (int64_t)it * kSortThreads + t;
-        if (idx < n) atomicAdd(&h[(uint32_t)(keys[idx] >> shift) & (kRadix - 1)], 1u);
-    }
-    __syncthreads();
-    hist[(int64_t)t * nblocks + blockIdx.x] = h[t];
+// One stable counting pass of the LSD radix sort in a single kernel ("one
+// sweep"): each block takes the next virtual tile (ticket order, so every block
+// it waits on has already started), counts its digits, publishes the counts,
+// looks back over earlier tiles' published counts for its global offsets, and
+// scatters.  status[tile][digit] = flag (bits 62-63: 1 aggregate, 2 inclusive
+// prefix) | count.  The look-back wait is bounded; giving up marks the map bad.
+constexpr uint64_t kFlagAgg = 1ull << 62, kFlagInc = 2ull << 62, kCountMask = (1ull << 62) - 1;
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-
-// Exclusive scan of the (digit-major, block-minor) digit counts in segments of
-// kScanSeg entries: each block scans one segment in place and writes the
-// segment's total; the scatter kernel adds the prefix of the segment totals.
-constexpr int kScanSeg = 4096;  // 1024 threads x 4 entries
-
-__global__ void __launch_bounds__(1024)
-k_scan_segments(uint32_t* __restrict__ v, int64_t total, uint32_t* __restrict__ seg_total) {
-    __shared__ uint32_t wsum[32];
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const int64_t base = (int64_t)blockIdx.x * kScanSeg + 4 * t;
-    uint32_t x[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) x[q] = base + q < total ? v[base + q] : 0u;
-    const uint32_t s = x[0] + x[1] + x[2] + x[3];
-    uint32_t inc = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) wsum[w] = inc;
-    __syncthreads();
-    if (w == 0) {
-        uint32_t y = wsum[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
-            if (lane >= o) y += z;
-        }
-        wsum[lane] = y;
-    }
-    __syncthreads();
-    uint32_t run = inc - s + (w > 0 ? wsum[w - 1] : 0u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (base + q < total) v[base + q] = run;
-        run += x[q];
-    }
-    if (t == 1023) seg_total[blockIdx.x] = wsum[31];
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
-k_radix_scatter(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK* __restrict__ kout,
-                uint32_t* __restrict__ vout, int64_t n, int shift,
-                const uint32_t* __restrict__ hist, int64_t nblocks, int items,
-                const uint32_t* __restrict__ seg_total, int nseg) {
+k_onesweep(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK* __restrict__ kout,
+           uint32_t* __restrict__ vout, int64_t n, int shift, const uint32_t* __restrict__ ghist_pass,
+           uint64_t* __restrict__ status, uint32_t* __restrict__ ticket, int items, uint32_t* __restrict__ err) {
     constexpr int kWarps = kSortThreads / 32;
+    extern __shared__ uint8_t dsm[];
+    SK* s_keys = reinterpret_cast<SK*>(dsm);                                     // [items * 256]
+    uint32_t* s_vals = reinterpret_cast<uint32_t*>(s_keys + items * kSortThreads);  // [items * 256]
     __shared__ uint32_t offs[kRadix];
     __shared__ uint32_t wcount[kWarps][kRadix];
-    __shared__ uint32_t seg_prefix[kMaxScanSegs];
+    __shared__ uint32_t s_vid;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    {  // exclusive prefix of the segment totals (<= 1024: four per thread)
-        __shared__ uint32_t wtot[kWarps];
-        uint32_t x[4], sum = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            x[q] = 4 * t + q < nseg ? seg_total[4 * t + q] : 0u;
-            sum += x[q];
-        }
-        uint32_t inc = sum;
+    if (t == 0) s_vid = atomicAdd(ticket, 1u);
+    // bin bases: exclusive scan of this pass's global digit counts
+    {
+        const uint32_t c = ghist_pass[t];
+        uint32_t inc = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
             if (lane >= o) inc += y;
         }
-        if (lane == 31) wtot[warp] = inc;
+        if (lane == 31) wcount[0][warp] = inc;
         __syncthreads();
-        uint32_t run = inc - sum;
-        for (int w = 0; w < warp; ++w) run += wtot[w];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (4 * t + q < nseg) seg_prefix[4 * t + q] = run;
-            run += x[q];
-        }
+        uint32_t base = inc - c;
+        for (int w = 0; w < warp; ++w) base += wcount[0][w];
+        offs[t] = base;
+        __syncthreads();
     }
+    const int64_t vid = s_vid;
+    const int64_t tile0 = vid * kSortThreads * items;
+    // load the tile and count its digits
+    uint32_t cnt = 0;
+    for (int w = 0; w < kWarps; ++w) wcount[w][t] = 0;
     __syncthreads();
-    {
-        const int64_t e = (int64_t)t * nblocks + blockIdx.x;
-        offs[t] = hist[e] + seg_prefix[e / kScanSeg];
-    }
-    const int64_t base = (int64_t)blockIdx.x * kSortThreads * items;
-    const uint32_t lt_mask = (1u << lane) - 1u;
     for (int it = 0; it < items; ++it) {
-        const int64_t idx = base + (int64_t)it * kSortThreads + t;
-        const bool valid = idx < n;
+        const int64_t idx = tile0 + (int64_t)it * kSortThreads + t;
         SK key = 0;
-        uint32_t val = 0, d = kRadix;  // invalid lanes use a digit no bucket has
-        if (valid) {
+        uint32_t val = 0;
+        if (idx < n) {
             key = kin[idx];
             val = vin ? vin[idx] : (uint32_t)idx;
-            d = (uint32_t)(key >> shift) & (kRadix - 1);
+            atomicAdd(&wcount[0][(uint32_t)(key >> shift) & (kRadix - 1)], 1u);
         }
+        s_keys[it * kSortThreads + t] = key;
+        s_vals[it * kSortThreads + t] = val;
+    }
+    __syncthreads();
+    cnt = wcount[0][t];  // this tile's count of digit t
+    uint64_t* my = status + vid * kRadix;
+    st_release(&my[t], (vid == 0 ? kFlagInc : kFlagAgg) | cnt);
+    // look back for the count of digit t in all earlier tiles
+    uint64_t prefix = 0;
+    bool timed_out = false;
+    if (vid > 0) {
+        // walk back 8 tiles per round (independent loads), consuming them in order
+        constexpr int kW = 8;
+        int64_t q = vid - 1;
+        const uint64_t t0 = now_ns();
+        bool done = false;
+        while (!done && q >= 0) {
+            uint64_t st[kW];
+#pragma unroll
+            for (int u = 0; u < kW; ++u) st[u] = q - u >= 0 ? ld_acquire(&status[(q - u) * kRadix + t]) : 0ull;
+            int used = 0;
+#pragma unroll
+            for (int u = 0; u < kW; ++u) {
+                if (done || used < u || q - u < 0) continue;  // stop at the first unpublished tile
+                const uint64_t flag = st[u] & ~kCountMask;
+                if (flag == kFlagInc) {
+                    prefix += st[u] & kCountMask;
+                    done = true;
+                } else if (flag == kFlagAgg) {
+                    prefix += st[u] & kCountMask;
+                    used = u + 1;
+                }
+            }
+            q -= used;
+            if (!done && used < kW && q >= 0 && now_ns() - t0 > 1000000000ull) {  // 1 s: a tile never published
+                timed_out = true;
+                break;
+            }
+        }
+        st_release(&my[t], kFlagInc | (prefix + cnt));
+    }
+    if (timed_out) atomicOr(err, kErrTimeout);
+    offs[t] += (uint32_t)prefix;
+    __syncthreads();
+    // stable scatter, one sub-step of 256 consecutive keys at a time
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int it = 0; it < items; ++it) {
+        const int64_t idx = tile0 + (int64_t)it * kSortThreads + t;
+        const bool valid = idx < n;
+        const SK key = s_keys[it * kSortThreads + t];
+        const uint32_t val = s_vals[it * kSortThreads + t];
+        const uint32_t d = valid ? (uint32_t)(key >> shift) & (kRadix - 1) : (uint32_t)kRadix;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) wcount[w][t] = 0;
         __syncthreads();
@@ -297,7 +300,7 @@ k_radix_scatter(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK
             offs[t] = run;
         }
         __syncthreads();
-        if (valid) {
+        if (valid && !timed_out) {
             const uint32_t pos = wcount[warp][d] + rank;
             kout[pos] = key;
             vout[pos] = val;
@@ -376,11 +379,7 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     l.sort_items = (int)std::min<int64_t>(16, std::max<int64_t>(1, (per_block_target + kSortThreads - 1) / kSortThreads));
     int64_t tile = (int64_t)kSortThreads * l.sort_items;
     l.sort_blocks = std::max<int64_t>(1, (N + tile - 1) / tile);
-    while ((int64_t)kRadix * l.sort_blocks > (int64_t)kMaxScanSegs * kScanSeg) {  // keep the segments few
-        ++l.sort_items;
-        tile = (int64_t)kSortThreads * l.sort_items;
-        l.sort_blocks = (N + tile - 1) / tile;
-    }
+    (void)tile;
     const size_t slot = l.key64 ? 16 : 8, ss = l.sort64 ? 8 : 4;
     size_t o = 0;
     l.off_hdr = o;      o += 256;
@@ -391,7 +390,12 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     l.off_skeys_a = o;  o += align_up(ss * (size_t)N, 256);
     l.off_skeys_b = o;  o += align_up(ss * (size_t)N, 256);
     l.off_svals_b = o;  o += align_up(4 * (size_t)N, 256);
-    l.off_hist = o;     o += align_up(4 * ((size_t)kRadix * l.sort_blocks + kMaxScanSegs), 256);
+    // one-sweep radix sort: global digit counts of every pass, then per pass the
+    // tiles' published counts and a ticket counter (all zeroed by one memset)
+    const int passes = std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits);
+    l.off_hist = o;     o += align_up(4 * (size_t)kRadix * passes, 256);
+    l.off_status = o;   o += align_up(8 * (size_t)kRadix * l.sort_blocks * passes, 256);
+    l.off_tickets = o;  o += align_up(4 * (size_t)passes, 256);
     l.total = o;
     *L = l;
     return VG_OK;
@@ -413,7 +417,6 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
     uint32_t* v0 = reinterpret_cast<uint32_t*>(ws + l.off_sorted);
     uint32_t* v1 = reinterpret_cast<uint32_t*>(ws + l.off_svals_b);
     uint32_t* hist = reinterpret_cast<uint32_t*>(ws + l.off_hist);
-    uint32_t* seg_total = hist + kRadix * l.sort_blocks;
 
     cudaMemsetAsync(table, 0xFF, cap * sizeof(T), s);  // empty keys (row fields are don't-care)
     cudaMemsetAsync(nbr, 0xFF, (size_t)n * kTaps * sizeof(uint32_t), s);  // VG_NONE everywhere
@@ -422,22 +425,20 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
         coords, n, X, Y, Z, table, l.cap_log2, nbr);
     const int passes = nbr_sort_passes(l);
     const unsigned g = (unsigned)l.sort_blocks;
+    cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)passes - l.off_hist, s);  // counts, status, tickets
+    const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * 152);
+    k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, passes, mask, ka, hist);
     const uint32_t* vin = nullptr;
+    const size_t smem = (size_t)kSortThreads * l.sort_items * (sizeof(SK) + 4);
+    cudaFuncSetAttribute(k_onesweep<SK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     for (int p = 0; p < passes; ++p) {
         const SK* kin = (p % 2 == 0) ? ka : kb;
         SK* kout = (p % 2 == 0) ? kb : ka;
         uint32_t* vout = ((passes - 1 - p) % 2 == 0) ? v0 : v1;
-        const int shift = p * kRadixBits;
-        if (p == 0)
-            k_key_hist<SK><<<g, kSortThreads, 0, s>>>(coords, nbr, n, L, mask, ka, hist, l.sort_blocks,
-                                                     l.sort_items);
-        else
-            k_radix_hist<SK><<<g, kSortThreads, 0, s>>>(kin, n, shift, hist, l.sort_blocks, l.sort_items);
-        const int64_t total = (int64_t)kRadix * l.sort_blocks;
-        const int nseg = (int)((total + kScanSeg - 1) / kScanSeg);
-        k_scan_segments<<<nseg, 1024, 0, s>>>(hist, total, seg_total);
-        k_radix_scatter<SK><<<g, kSortThreads, 0, s>>>(kin, vin, kout, vout, n, shift, hist, l.sort_blocks,
-                                                      l.sort_items, seg_total, nseg);
+        k_onesweep<SK><<<g, kSortThreads, smem, s>>>(
+            kin, vin, kout, vout, n, p * kRadixBits, hist + p * kRadix,
+            reinterpret_cast<uint64_t*>(ws + l.off_status) + (size_t)p * kRadix * l.sort_blocks,
+            reinterpret_cast<uint32_t*>(ws + l.off_tickets) + p, l.sort_items, status);
         vin = vout;
     }
     k_tile_rows<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
@@ -480,6 +481,7 @@ int nbr_status(const void* ws, cudaStream_t s) {
     if (h & kErrRange) return VG_ERR_COORD_OUT_OF_RANGE;
     if (h & kErrDup) return VG_ERR_DUPLICATE_COORD;
     if (h & kErrFull) return VG_ERR_HASH_FULL;
+    if (h & kErrTimeout) return VG_ERR_DEVICE_TIMEOUT;
     return VG_OK;
 }
 

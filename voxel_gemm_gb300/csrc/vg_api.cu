@@ -104,7 +104,7 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     info[0] = l.key64;
     info[1] = l.sort_bits;
     info[2] = passes;
-    info[3] = N > 0 ? 2 + 3 * passes + 1 : 0;  // insert, probe+key, passes x (hist, scan, scatter), tile rows
+    info[3] = N > 0 ? 3 + passes + 1 : 0;  // insert, probe, keys + digit counts, passes, tile rows
     return VG_OK;
 }
 
