@@ -32,20 +32,25 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 288;
-constexpr int kRowsPerStage = 64;
-constexpr int kABytes = 2 * kRowsPerStage * 128;  // two 64-channel blocks x 64 rows
 
-// MU M blocks share every dY stage (their accumulators sit side by side in
-// TMEM); two accumulator sets alternate when they fit in 512 columns.
+// One CTA work unit holds MU M blocks (MU accumulators of 128 x BN side by side
+// in TMEM, all sharing every dY stage) and streams stages of R sorted rows:
+//   Cout = 64: MU = 7 (448 columns), R = 32;  Cout >= 128: MU = 2, R = 64.
+// The larger MU, the fewer times dY is re-read (measured: 7 blocks at Cout = 64
+// cut DRAM reads from 7.0 to about 2 GB at 4.9 M voxels; 4 blocks at Cout = 128
+// were slower than 2).
 template <int BN>
 struct WCfg {
-    static constexpr int MU = 2;
+    static constexpr int MU = BN == 64 ? 7 : 2;
+    static constexpr int R = BN == 64 ? 32 : 64;           // rows per stage (K of the MMA)
+    static constexpr int RQ = R / 16;                       // rows per gather thread
     static constexpr int kAccCols = MU * BN;
     static constexpr int NBUF = 2 * kAccCols <= 512 ? 2 : 1;
-    static constexpr int kTmemCols = NBUF * kAccCols;
-    static constexpr int kBBytes = (BN / 64) * kRowsPerStage * 128;
+    static constexpr int kTmemCols = NBUF * kAccCols <= 256 ? 256 : 512;
+    static constexpr int kABytes = 2 * R * 128;             // two 64-channel blocks x R rows
+    static constexpr int kBBytes = (BN / 64) * R * 128;
     static constexpr int kStageBytes = MU * kABytes + kBBytes;
-    static constexpr int S = 196608 / kStageBytes;  // 192 KB of stages
+    static constexpr int S = 196608 / kStageBytes;          // 192 KB of stages
     static constexpr int kNumBars = 2 * S + 5;
     static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 4 * S + 16;
 };
@@ -96,18 +101,18 @@ __device__ __forceinline__ MUnit munit(int m, int Cin) {
     return r;
 }
 
-// Row metadata a gather thread needs for one stage (its four rows): the dY row
+// Row metadata a gather thread needs for one stage (its RQ rows): the dY row
 // and, for each of the unit's MU M blocks, the neighbour rows of its two taps.
-template <int MU>
+template <int MU, int RQ>
 struct Meta {
-    uint32_t i[4], j0[MU][4], j1[MU][4];
+    uint32_t i[RQ], j0[MU][RQ], j1[MU][RQ];
 };
 
-template <int MU>
+template <int MU, int RQ>
 __device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit (&mu)[MU], int64_t row0, int p,
-                                          Meta<MU>& m) {
+                                          Meta<MU, RQ>& m) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < RQ; ++q) {
         const int64_t r = row0 + (p >> 3) + 16 * q;  // r < num_tiles * 128 always
         m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
 #pragma unroll
@@ -149,10 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
     constexpr int S = C::S;
     constexpr int MU = C::MU;
     constexpr int NBUF = C::NBUF;
+    constexpr int R = C::R, RQ = C::RQ;
     constexpr int NBB = BN / 64;  // 64-column blocks of B
+    constexpr int kABytes = C::kABytes;
+    constexpr uint32_t kBlk = R * 128;  // bytes of one 64-channel block of R rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stages = smem;  // stage g: MU A tiles (16 KB each), then the B tile
+    uint8_t* stages = smem;  // stage g: MU A tiles, then the B tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)S * C::kStageBytes);
     uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
     uint32_t* s_tmem = s_info + S;
@@ -217,30 +225,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
             cur.bits = window_bits(a, cur.base, cur.end, t_first, umask, lane);
             int64_t t = next_tile(a, cur, t_first, umask, lane);  // the first tile is always active
             int h = 0;
-            Meta<MU> mc, mn;
+            Meta<MU, RQ> mc, mn;
             bool null_stage = false;
             if (t >= 0) {
-                load_meta<MU>(a, mu, t * 128, p, mc);
+                load_meta<MU, RQ>(a, mu, t * 128, p, mc);
             } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
                 null_stage = true;
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < RQ; ++q) {
                     mc.i[q] = kNone;
                     for (int v = 0; v < MU; ++v) mc.j0[v][q] = mc.j1[v][q] = kNone;
                 }
             }
             bool first = true;
             while (t >= 0 || null_stage) {
-                // next stage of this unit: second half of the tile, or the next active tile
+                // next stage of this unit: the next R rows of the tile, or the next active tile
                 int64_t tn = t;
                 int hn = h + 1;
                 if (null_stage) {
                     tn = -1;
                     null_stage = false;
-                } else if (hn == 2) {
+                } else if (hn == 128 / R) {
                     tn = next_tile(a, cur, t_first, umask, lane);
                     hn = 0;
                 }
-                if (tn >= 0) load_meta<MU>(a, mu, tn * 128 + hn * 64, p, mn);
+                if (tn >= 0) load_meta<MU, RQ>(a, mu, tn * 128 + hn * R, p, mn);
                 const uint32_t stage = it % S, ph = (it / S) & 1u;
                 // warp-uniform decision: the tile cursor uses warp-wide ballots
                 if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort))) {
@@ -257,21 +265,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                 for (int v = 0; v < MU; ++v) {
                     const uint32_t a_base = smem_u32(st + v * kABytes);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {  // A: block e/4, row (p>>3) + 16*(e%4)
-                        const int q = e & 3, blk = e >> 2;
+                    for (int e = 0; e < 2 * RQ; ++e) {  // A: block e / RQ, row (p>>3) + 16*(e % RQ)
+                        const int q = e % RQ, blk = e / RQ;
                         const int row = (p >> 3) + 16 * q;
                         const uint32_t j = blk ? mc.j1[v][q] : mc.j0[v][q];
                         const int c = blk ? mu[v].c1 : mu[v].c0;
                         const uint16_t* src = a.f + (int64_t)(j != kNone ? j : 0u) * a.Cin + c + ch * 8;
-                        cp_async16(a_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
-                                       ((ch ^ (row & 7)) << 4),
+                        cp_async16(a_base + blk * kBlk + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4),
                                    src, j != kNone ? 16u : 0u);
                     }
                 }
                 const uint32_t b_base = smem_u32(st + MU * kABytes);
 #pragma unroll
-                for (int e = 0; e < 4 * NBB; ++e) {  // B: block e/4, same four rows
-                    const int q = e & 3, blk = e >> 2;
+                for (int e = 0; e < NBB * RQ; ++e) {  // B: block e / RQ, the same rows
+                    const int q = e % RQ, blk = e / RQ;
                     const int row = (p >> 3) + 16 * q;
                     const uint32_t i = mc.i[q];
                     // rows with none of the unit's taps contribute nothing: skip their dY bytes
@@ -280,8 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     for (int v = 0; v < MU; ++v) use |= mc.j0[v][q] != kNone || mc.j1[v][q] != kNone;
                     use = use && i != kNone;
                     const uint16_t* src = a.dy + (int64_t)(use ? i : 0u) * a.Cout + nb * BN + blk * 64 + ch * 8;
-                    cp_async16(b_base + blk * (kRowsPerStage * 128) + (row >> 3) * 1024 + (row & 7) * 128 +
-                                   ((ch ^ (row & 7)) << 4),
+                    cp_async16(b_base + blk * kBlk + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4),
                                src, use ? 16u : 0u);
                 }
                 cp_async_arrive_noinc(full0 + 8 * stage);  // fires when this thread's copies land
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_mn(BF16, BN);
-            constexpr uint32_t lbo = kRowsPerStage * 128;  // 64-channel blocks are 8 KB apart
+            constexpr uint32_t lbo = kBlk;  // distance between 64-channel blocks
             uint32_t it = 0, ua = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                         const uint32_t a_base = smem_u32(st + v * kABytes);
                         const uint32_t d_tmem = tmem + buf * C::kAccCols + v * BN;
 #pragma unroll
-                        for (int j = 0; j < kRowsPerStage / 16; ++j) {
+                        for (int j = 0; j < R / 16; ++j) {
                             mma_f16(d_tmem, sw128_mnmajor_desc(a_base + 2048 * j, lbo),
                                     sw128_mnmajor_desc(b_base + 2048 * j, lbo), idesc,
                                     ((info & 1u) && j == 0) ? 0u : 1u);
@@ -419,16 +425,18 @@ int launch_wgrad(const WgArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// Split-K chunk count: about four work units per SM, every chunk non-empty,
-// partial sums capped at 1 GiB.
+// Split-K chunk count: about four work units per SM, at least 4 tiles per chunk
+// (every chunk non-empty), partial sums capped at 1 GiB.
 int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
+    const int bn = wg_bn(Cout);
+    const int mu = bn == 64 ? WCfg<64>::MU : (bn == 128 ? WCfg<128>::MU : WCfg<256>::MU);
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
-    const int64_t MG = (num_munits(Cin) + 1) / 2;  // M blocks are taken two per unit
-    const int64_t per_split = MG * (Cout / wg_bn(Cout));
+    const int64_t MG = (num_munits(Cin) + mu - 1) / mu;
+    const int64_t per_split = MG * (Cout / bn);
     int64_t S = std::max<int64_t>(1, (4 * 152 + per_split - 1) / per_split);
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
-    S = std::min<int64_t>(S, T);
+    S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
     const int64_t tpc = (T + S - 1) / S;
     return (int)((T + tpc - 1) / tpc);
 }
