@@ -120,10 +120,11 @@ VG_API int vg_nbrmap_status(const void* ws, void* stream);
 /* Device pointers into a built workspace (no device access, no sync):
  *   sorted_idx [N] uint32 — row r of the processing order is voxel sorted_idx[r]
  *                (the page's sorted_idx).  Stable sort by the key
- *                ((m >> F) << (27 + F)) | (mask << F) | (m & (2^F - 1)), where
- *                m = (b << 3L) | bit-interleave(x, y, z) is the Morton code,
- *                L = ceil(log2(max(X,Y,Z))) and F = min(3L, 21): 128^3-voxel
- *                Morton blocks, then the valid-tap mask, then Morton order.
+ *                ((m >> F) << (27 + G)) | (mask << G) | ((m & (2^F - 1)) >> (F - G)),
+ *                where m = (b << 3L) | bit-interleave(x, y, z) is the Morton code,
+ *                L = ceil(log2(max(X,Y,Z))), F = min(3L, 21) and G = min(F, 6):
+ *                128^3-voxel Morton blocks, then the valid-tap mask, then the
+ *                8^3 sub-block in Morton order, then the input order (stable).
  *   tile_mask  [ceil(N/128)] uint32 — OR of mask over sorted rows [128t, 128t+128) */
 VG_API const uint32_t* vg_nbrmap_sorted_idx(const void* ws);
 VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);

@@ -23,7 +23,7 @@ def gpu_map(coords_np, grid, flags=0):
 
 
 def order_keys(coords, mask, grid):
-    """The documented sort key: 128^3 Morton blocks, then the tap mask, then Morton order."""
+    """The documented sort key: 128^3 Morton blocks, the tap mask, then the 8^3 sub-block."""
     B, X, Y, Z = grid
     L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
     c = coords.astype(np.uint64)
@@ -32,8 +32,9 @@ def order_keys(coords, mask, grid):
         for col, pos in ((1, 2), (2, 1), (3, 0)):
             m |= ((c[:, col] >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b + pos)
     F = np.uint64(min(3 * L, 21))
-    fine = m & ((np.uint64(1) << F) - np.uint64(1))
-    return ((m >> F) << (np.uint64(27) + F)) | (mask.astype(np.uint64) << F) | fine
+    G = np.uint64(min(3 * L, 21, 6))
+    fine = (m & ((np.uint64(1) << F) - np.uint64(1))) >> (F - G)
+    return ((m >> F) << (np.uint64(27) + G)) | (mask.astype(np.uint64) << G) | fine
 
 
 @pytest.mark.parametrize("name", MAP_WORKLOADS)

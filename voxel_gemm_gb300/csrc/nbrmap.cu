@@ -72,7 +72,10 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
     atomicOr(status, kErrFull);
 }
 
-// Row-order key of one voxel (see k_key_hist): coarse Morton block, tap mask, fine Morton.
+// Row-order key of one voxel (see k_key_hist): coarse Morton block, tap mask, then
+// the top G fine Morton bits (the 8^3 sub-block).  Below that the stable sort keeps
+// the input order; dropping the low Morton bits saves radix passes, and rows with
+// equal masks in one sub-block are gathered alike whatever their order.
 __device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
     uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
     for (int b = 0; b < L; ++b) {
@@ -81,8 +84,9 @@ __device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
         m |= (uint64_t)(((uint32_t)c.w >> b) & 1u) << (3 * b);
     }
     const int F = min(3 * L, kFineOrderBits);
-    const uint64_t fine = m & ((uint64_t(1) << F) - 1);
-    return ((m >> F) << (kTaps + F)) | ((uint64_t)mask << F) | fine;
+    const int G = min(F, kKeptFineBits);
+    const uint64_t fine = (m & ((uint64_t(1) << F) - 1)) >> (F - G);
+    return ((m >> F) << (kTaps + G)) | ((uint64_t)mask << G) | fine;
 }
 
 // Probe of the 13 taps k < 13 (offsets with dx < 0, or dx = 0 and dy < 0, or
@@ -360,7 +364,9 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     } else l.key64 = vol >= 1073741824.0 ? 1 : 0;
     const int lb = ceil_log2(B);
     const int lg = ceil_log2(std::max(X, std::max(Y, Z)));
-    l.sort_bits = lb + 3 * lg + kTaps;  // Morton code + the 27-bit valid-tap mask
+    // Morton code without its low F - G fine bits, plus the 27-bit valid-tap mask
+    const int fine = std::min(3 * lg, kFineOrderBits);
+    l.sort_bits = lb + 3 * lg - (fine - std::min(fine, kKeptFineBits)) + kTaps;
     if (l.sort_bits > 64) return VG_ERR_UNSUPPORTED;
     l.sort64 = l.sort_bits > 32 ? 1 : 0;
     if (flags & VG_TEST_SMALL_HASH) {
