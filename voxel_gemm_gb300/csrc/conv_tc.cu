@@ -178,8 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                 *s_abort = 1;
             }
             const uint32_t* nb_tile = s_nbr + buf * kBM * kTaps;
+            const int ch = p & 7;
             for (int k = 0; k < kTaps && ok; ++k) {
                 if (!((tm >> k) & 1u)) continue;
+                // this thread's 8 source rows for tap k, read from shared memory once per tap
+                // (all eight loads issue back to back) and reused by every K block
+                const uint16_t* src[8];
+                uint32_t src_bytes[8];
+#pragma unroll
+                for (int i2 = 0; i2 < 8; ++i2) {
+                    const uint32_t j = nb_tile[(i2 * 16 + (p >> 3)) * kTaps + k];
+                    src[i2] = a.A + (int64_t)(j != kNone ? j : 0u) * a.Kdim + ch * 8;
+                    src_bytes[i2] = j != kNone ? 16u : 0u;
+                }
                 for (int kb = 0; kb < KB; ++kb) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
                     if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
@@ -193,13 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                         bulk_g2s(smem_u32(sB + stage * C::kBBytes), src, C::kBBytes, full0 + 8 * stage);
                     }
                     const uint32_t a_base = smem_u32(sA + stage * kABytes);
-                    const int ch = p & 7;
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
                         const int row = i2 * 16 + (p >> 3);
-                        const uint32_t j = nb_tile[row * kTaps + k];
-                        const uint16_t* src = a.A + (int64_t)(j != kNone ? j : 0u) * a.Kdim + kb * kBK + ch * 8;
-                        cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src, j != kNone ? 16u : 0u);
+                        cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src[i2] + kb * kBK, src_bytes[i2]);
                     }
                     // arrives on the stage barrier when this thread's copies have landed
                     cp_async_arrive_noinc(full0 + 8 * stage);
