@@ -13,15 +13,17 @@
 //              neighbours, written in the 128-byte-swizzled K-major layout; each
 //              thread's copies arrive on the stage barrier by themselves
 //              (cp.async.mbarrier.arrive.noinc), so up to S stages are in flight;
-//              thread 0 also bulk-copies the prepacked weight tile (TMA engine)
-//              and, one unit ahead, the tile's 13.5 KB neighbour block.  (L2
-//              prefetching of later taps' rows was measured to slow the gathers:
-//              the prefetches occupy the same per-SM request slots.)
+//              each thread reads its eight source rows once per tap and reuses
+//              them for every K block; thread 0 also bulk-copies, one unit ahead,
+//              the tile's 13.5 KB neighbour block.  (L2 prefetching of later taps'
+//              rows was measured to slow the gathers.)
 //   warp 4     TMEM allocation and the single MMA-issuing thread:
 //              tcgen05.mma M=128, N=BN, K=16, fp32 accumulators in TMEM,
 //              two accumulator buffers so the epilogue overlaps the next tile.
 //   warps 5-8  epilogue: tcgen05.ld, + bias, round to fp16/bf16, scatter rows
 //              back to the caller's order through sorted_idx.
+//   warp 9     weight-tile loader: one bulk copy (TMA engine) of the prepacked
+//              weight tile per stage, kept off the gather warps' issue path.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -32,7 +34,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;          // 9 warps
+constexpr int kThreads = 320;          // 10 warps
 constexpr int kBM = 128;               // rows per tile (MMA M)
 constexpr int kBK = 64;                // 16-bit elements per K block (128 bytes)
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
@@ -159,8 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         }
         uint32_t tm_next = u < units ? a.tile_mask[u / NB] : 0u;
         for (; u < units; u += gridDim.x, ++idx) {
-            const int64_t t = u / NB;
-            const int nb = (int)(u - t * NB);
             const uint32_t buf = idx & 1u;
             const uint32_t tm = tm_next;
             const int64_t un = u + gridDim.x;
@@ -198,11 +198,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                         *s_abort = 1;
                         break;
                     }
-                    if (p == 0) {
-                        mbar_arrive_expect_tx(full0 + 8 * stage, C::kBBytes);
-                        const uint8_t* src = a.Bimg + (((int64_t)nb * kTaps + k) * KB + kb) * C::kBBytes;
-                        bulk_g2s(smem_u32(sB + stage * C::kBBytes), src, C::kBBytes, full0 + 8 * stage);
-                    }
                     const uint32_t a_base = smem_u32(sA + stage * kABytes);
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
@@ -218,6 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         }
         cp_async_wait_all();  // no copy of this thread is still writing shared memory
         if (!ok) atomicOr(a.err, kErrTimeout);
+        // Before the block may exit, every stage's last fill must have landed, its
+        // copy-completion arrivals included (already true unless a wait gave up).
+        if (p == 0)
+            for (uint32_t i = 0; i < S && i < it; ++i) {
+                const uint32_t last = it - 1 - i;
+                if (!mbar_wait_timed(full0 + 8 * (last % S), (last / S) & 1u)) atomicOr(a.err, kErrTimeout);
+            }
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp <= 8) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         uint32_t ua = 0;
@@ -319,6 +321,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             *s_abort = 1;
             atomicOr(a.err, kErrTimeout);
         }
+    } else {
+        // ------------------------------------------------------------ weight-tile loader
+        if (lane == 0) {
+            // One bulk copy per stage, in the gather threads' (unit, tap, K block) order;
+            // its expect_tx arrival is the stage barrier's 129th.
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int64_t t = u / NB;
+                const int nb = (int)(u - t * NB);
+                const uint32_t tm = a.tile_mask[t];
+                for (int k = 0; k < kTaps && ok; ++k) {
+                    if (!((tm >> k) & 1u)) continue;
+                    const uint8_t* bsrc = a.Bimg + ((int64_t)nb * kTaps + k) * KB * C::kBBytes;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t stage = it % S, ph = (it / S) & 1u;
+                        if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full0 + 8 * stage, C::kBBytes);
+                        bulk_g2s(smem_u32(sB + stage * C::kBBytes), bsrc + kb * C::kBBytes, C::kBBytes, full0 + 8 * stage);
+                        ++it;
+                    }
+                }
+            }
+            if (!ok) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
