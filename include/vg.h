@@ -124,7 +124,8 @@ VG_API int vg_nbrmap_status(const void* ws, void* stream);
  *                where m = (b << 3L) | bit-interleave(x, y, z) is the Morton code,
  *                L = ceil(log2(max(X,Y,Z))), F = min(3L, 21) and G = min(F, 6):
  *                128^3-voxel Morton blocks, then the valid-tap mask, then the
- *                8^3 sub-block in Morton order, then the input order (stable).
+ *                top G fine Morton bits (a 4x4x4 split of the block), then the
+ *                input order (stable).
  *   tile_mask  [ceil(N/128)] uint32 — OR of mask over sorted rows [128t, 128t+128) */
 VG_API const uint32_t* vg_nbrmap_sorted_idx(const void* ws);
 VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);
@@ -135,7 +136,7 @@ VG_API const uint32_t* vg_nbrmap_sorted_nbr(const void* ws, int64_t N);
 
 /* Host-only description of the build plan (no device access):
  *   info[0] = 1 if the hash keys are 64-bit, info[1] = significant bits of the
- *   Morton key, info[2] = radix-sort passes, info[3] = kernels launched by
+ *   sort key above, info[2] = radix-sort passes, info[3] = kernels launched by
  *   vg_nbrmap_build (memsets not counted).  Returns VG_OK or VG_ERR_INVALID_ARG. */
 VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int info[4]);
 

@@ -56,6 +56,6 @@ constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digi
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kFineOrderBits = 21;                    // fine Morton bits below the tap mask (128^3 blocks)
-constexpr int kKeptFineBits = 6;                      // of those, the top ones kept in the key (8^3 sub-blocks)
+constexpr int kKeptFineBits = 6;                      // of those, the top ones kept in the key (4x4x4 split of a block)
 
 }  // namespace vg

@@ -73,7 +73,7 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
 }
 
 // Row-order key of one voxel (see k_key_hist): coarse Morton block, tap mask, then
-// the top G fine Morton bits (the 8^3 sub-block).  Below that the stable sort keeps
+// the top G fine Morton bits (a 4x4x4 split of the block).  Below that the stable sort keeps
 // the input order; dropping the low Morton bits saves radix passes, and rows with
 // equal masks in one sub-block are gathered alike whatever their order.
 __device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
