@@ -64,6 +64,7 @@ struct WgradPass {
     void* db;      // may be null
     float* partial;     // [S][27][Cin][Cout]
     float* partial_db;  // [S][Cout]
+    void* dy_sorted;    // tensor-core path: tc_wgrad_sorted_dy_bytes bytes of scratch (or null if 0)
     int splits;
     uint32_t* err;
 };
@@ -90,8 +91,10 @@ int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void
                     const uint32_t* nbr_status, cudaStream_t s);
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
 int tc_wgrad(const WgradPass& p, cudaStream_t s);
-int tc_fwd_launches();
-   // kernels per forward call on the tensor-core path
-int tc_bwd_launches();   // kernels per full backward call on the tensor-core path
+// Scratch of the weight gradient: dY rows copied into processing order (zero rows
+// pad the last tile) when Cout takes the wide-N kernel, else 0 bytes.
+size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout);
+int tc_fwd_launches();            // kernels per forward call on the tensor-core path
+int tc_bwd_launches(int Cout);    // kernels per full backward call on the tensor-core path
 
 }  // namespace vg

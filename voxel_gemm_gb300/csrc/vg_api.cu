@@ -9,7 +9,7 @@ namespace vg {
 struct ConvPlan {
     int tensor_core = 0;   // 16-bit tcgen05 path
     int splits = 1;        // split-K chunks of the weight gradient
-    size_t off_err = 0, off_wfwd = 0, off_wbwd = 0, off_partial = 0, off_partial_db = 0, total = 0;
+    size_t off_err = 0, off_wfwd = 0, off_wbwd = 0, off_partial = 0, off_partial_db = 0, off_dys = 0, total = 0;
 };
 
 static size_t dtype_size(int dt) { return dt == VG_F32 ? 4 : 2; }
@@ -29,6 +29,7 @@ static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, Co
     p.off_wbwd = o;        o += p.tensor_core ? align_up(tc_packed_weight_bytes(dtype, Cout, Cin), 256) : 0;
     p.off_partial = o;     o += align_up((size_t)p.splits * kTaps * Cin * Cout * 4, 256);
     p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N) * Cout * 4, 256);
+    p.off_dys = o;         o += p.tensor_core ? align_up(tc_wgrad_sorted_dy_bytes(N, Cout), 256) : 0;
     (void)wbytes;
     p.total = o;
     *P = p;
@@ -115,7 +116,7 @@ int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, in
     info[0] = p.tensor_core;
     info[1] = p.splits;
     info[2] = N > 0 ? (p.tensor_core ? tc_fwd_launches() : 1) : 0;
-    info[3] = N > 0 ? (p.tensor_core ? tc_bwd_launches() : 1 + 2 + 2) : 0;
+    info[3] = N > 0 ? (p.tensor_core ? tc_bwd_launches(Cout) : 1 + 2 + 2) : 0;
     return VG_OK;
 }
 
@@ -243,6 +244,7 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         w.db = grad_bias;
         w.partial = reinterpret_cast<float*>(ws + p.off_partial);
         w.partial_db = reinterpret_cast<float*>(ws + p.off_partial_db);
+        w.dy_sorted = ws + p.off_dys;
         w.splits = p.splits;
         w.err = err;
         st = p.tensor_core ? tc_wgrad(w, s) : simt_wgrad(w, s);

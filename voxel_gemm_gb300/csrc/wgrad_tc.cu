@@ -18,9 +18,17 @@
 // Each unit writes an fp32 partial [128 x BN] for its chunk; a second kernel sums
 // the chunks in a fixed order (bitwise deterministic).
 //
-// Warp roles as in the forward kernel: warps 0-3 gather A and B with 16-byte
-// cp.async (zero fill; each thread's copies arrive on the stage barrier by
-// themselves), warp 4 issues tcgen05.mma, warps 5-8 store the partials.
+// Warp roles as in the forward kernel: warps 0-3 gather A with 16-byte cp.async
+// (zero fill; each thread's copies arrive on the stage barrier by themselves),
+// warp 4 issues tcgen05.mma, warps 5-8 store the partials.  B (dY) rows are
+// consecutive sorted rows: for Cout >= 128 they are first copied into
+// processing order (one streaming pass) and each stage's B tile is then one
+// TMA tile load per 64 columns, which halves the per-SM cp.async traffic;
+// for Cout = 64 the gather threads fetch them with cp.async as well.
+#include <cuda.h>
+
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -108,13 +116,14 @@ struct Meta {
     uint32_t i[RQ], j0[MU][RQ], j1[MU][RQ];
 };
 
-template <int MU, int RQ>
+// The dY row index is needed only when the gather threads fetch B themselves (WANT_I).
+template <int MU, int RQ, bool WANT_I>
 __device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit (&mu)[MU], int64_t row0, int p,
                                           Meta<MU, RQ>& m) {
 #pragma unroll
     for (int q = 0; q < RQ; ++q) {
         const int64_t r = row0 + (p >> 3) + 16 * q;  // r < num_tiles * 128 always
-        m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
+        if (WANT_I) m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
 #pragma unroll
         for (int u = 0; u < MU; ++u) {
             m.j0[u][q] = mu[u].tap0 >= 0 ? a.sorted_nbr[r * kTaps + mu[u].tap0] : kNone;
@@ -148,8 +157,34 @@ __device__ __forceinline__ int64_t next_tile(const WgArgs& a, TileCursor& c, int
     return c.base + b;
 }
 
+// 2D TMA tile load (box of 64 columns x R rows, 128-byte swizzle) completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// dst[r] = src[sorted_idx[r]] for r < n, zero rows up to rows_pad (16-bit rows of C values).
+__global__ void __launch_bounds__(256)
+k_sort_rows(const uint16_t* __restrict__ src, const uint32_t* __restrict__ sorted_idx, int64_t n, int64_t rows_pad,
+            int C, const uint32_t* __restrict__ nbr_status, uint16_t* __restrict__ dst) {
+    if (*nbr_status) return;
+    const int cpr = C / 8;  // 16-byte chunks per row
+    const int64_t total = rows_pad * cpr;
+    for (int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x; e < total; e += (int64_t)gridDim.x * 256) {
+        const int64_t r = e / cpr;
+        const int c = (int)(e - r * cpr);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n) v = reinterpret_cast<const uint4*>(src + (int64_t)sorted_idx[r] * C)[c];
+        reinterpret_cast<uint4*>(dst + r * C)[c] = v;
+    }
+}
+
 template <int BN, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
+    // B by TMA from the sorted dY copy when the tile is wide (R = 64 rows, box 64 x 64)
+    constexpr bool kTmaB = BN >= 128;
     using C = WCfg<BN>;
     constexpr int S = C::S;
     constexpr int MU = C::MU;
@@ -228,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
             Meta<MU, RQ> mc, mn;
             bool null_stage = false;
             if (t >= 0) {
-                load_meta<MU, RQ>(a, mu, t * 128, p, mc);
+                load_meta<MU, RQ, !kTmaB>(a, mu, t * 128, p, mc);
             } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
                 null_stage = true;
                 for (int q = 0; q < RQ; ++q) {
@@ -248,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     tn = next_tile(a, cur, t_first, umask, lane);
                     hn = 0;
                 }
-                if (tn >= 0) load_meta<MU, RQ>(a, mu, tn * 128 + hn * R, p, mn);
+                if (tn >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, tn * 128 + hn * R, p, mn);
                 const uint32_t stage = it % S, ph = (it / S) & 1u;
                 // warp-uniform decision: the tile cursor uses warp-wide ballots
                 if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort))) {
@@ -256,11 +291,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                     *s_abort = 1;
                     break;
                 }
+                uint8_t* st = stages + (size_t)stage * C::kStageBytes;
                 if (p == 0) {  // published by thread 0's own release arrival below
                     s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
-                    mbar_arrive(full0 + 8 * stage);
+                    if constexpr (kTmaB) {
+                        const uint32_t bytes = t >= 0 ? NBB * kBlk : 0u;
+                        mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
+                        if (t >= 0) {
+                            const uint32_t b_base = smem_u32(st + MU * kABytes);
+#pragma unroll
+                            for (int blk = 0; blk < NBB; ++blk)
+                                tma_load_2d(b_base + blk * kBlk, &tmB, nb * BN + blk * 64, (int)(t * 128 + h * R),
+                                            full0 + 8 * stage);
+                        }
+                    } else {
+                        mbar_arrive(full0 + 8 * stage);
+                    }
                 }
-                uint8_t* st = stages + (size_t)stage * C::kStageBytes;
 #pragma unroll
                 for (int v = 0; v < MU; ++v) {
                     const uint32_t a_base = smem_u32(st + v * kABytes);
@@ -277,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a) {
                 }
                 const uint32_t b_base = smem_u32(st + MU * kABytes);
 #pragma unroll
-                for (int e = 0; e < NBB * RQ; ++e) {  // B: block e / RQ, the same rows
+                for (int e = 0; e < (kTmaB ? 0 : NBB * RQ); ++e) {  // B: block e / RQ, the same rows
                     const int q = e % RQ, blk = e / RQ;
                     const int row = (p >> 3) + 16 * q;
                     const uint32_t i = mc.i[q];
@@ -410,16 +457,48 @@ int sm_count_w() {
     return n > 0 ? n : 1;
 }
 
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// cuTensorMapEncodeTiled from the driver, looked up once (null if unavailable).
+EncodeTiled encode_tiled() {
+    static const EncodeTiled fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiled>(p);
+    }();
+    return fn;
+}
+
 template <int BN, bool BF16>
-int launch_wgrad(const WgArgs& a, cudaStream_t s) {
+int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, cudaStream_t s) {
     using C = WCfg<BN>;
     auto kern = k_wgrad_tc<BN, BF16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
+    CUtensorMap tm;
+    memset(&tm, 0, sizeof(tm));
+    if (BN >= 128) {
+        // [rows_pad][Cout] 16-bit, box = 64 columns x R rows, 128-byte swizzle (the MN-major B layout)
+        const EncodeTiled enc = encode_tiled();
+        if (!enc || !dy_sorted) return VG_ERR_CUDA;
+        const cuuint64_t dims[2] = {(cuuint64_t)a.Cout, (cuuint64_t)(a.num_tiles * kTileRows)};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.Cout * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)C::R};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(dy_sorted), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return VG_ERR_CUDA;
+    }
     const int MG = (num_munits(a.Cin) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, sm_count_w());
-    kern<<<grid, kThreads, C::kSmem, s>>>(a);
+    kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
     return VG_OK;
 }
 
@@ -441,6 +520,12 @@ int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
     return (int)((T + tpc - 1) / tpc);
 }
 
+size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout) {
+    if (wg_bn(Cout) < 128) return 0;
+    const int64_t rows = (n + kTileRows - 1) / kTileRows * kTileRows;
+    return (size_t)rows * Cout * 2;
+}
+
 int tc_wgrad(const WgradPass& p, cudaStream_t s) {
     if (p.n == 0) return VG_OK;
     if (p.dW) {
@@ -460,11 +545,20 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.partial = p.partial;
         a.err = p.err;
         const bool bf16 = p.dtype == VG_BF16;
+        const int bn = wg_bn(p.Cout);
+        uint16_t* dys = static_cast<uint16_t*>(p.dy_sorted);
+        if (bn >= 128) {
+            if (!dys) return VG_ERR_INVALID_ARG;
+            const int64_t rows_pad = a.num_tiles * kTileRows;
+            const int64_t chunks = rows_pad * (p.Cout / 8);
+            const unsigned blocks = (unsigned)std::min<int64_t>((chunks + 255) / 256, 16 * 152);
+            k_sort_rows<<<blocks, 256, 0, s>>>(a.dy, p.sorted_idx, p.n, rows_pad, p.Cout, p.nbr_status, dys);
+        }
         int st;
-        switch (wg_bn(p.Cout)) {
-            case 256: st = bf16 ? launch_wgrad<256, true>(a, s) : launch_wgrad<256, false>(a, s); break;
-            case 128: st = bf16 ? launch_wgrad<128, true>(a, s) : launch_wgrad<128, false>(a, s); break;
-            default: st = bf16 ? launch_wgrad<64, true>(a, s) : launch_wgrad<64, false>(a, s); break;
+        switch (bn) {
+            case 256: st = bf16 ? launch_wgrad<256, true>(a, dys, s) : launch_wgrad<256, false>(a, dys, s); break;
+            case 128: st = bf16 ? launch_wgrad<128, true>(a, dys, s) : launch_wgrad<128, false>(a, dys, s); break;
+            default: st = bf16 ? launch_wgrad<64, true>(a, dys, s) : launch_wgrad<64, false>(a, dys, s); break;
         }
         if (st != VG_OK) return st;
         launch_reduce_splits(p.partial, p.splits, (int64_t)kTaps * p.Cin * p.Cout, p.dW, p.dtype, p.nbr_status, s);
@@ -473,6 +567,7 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
     return VG_OK;
 }
 
-int tc_bwd_launches() { return 2 + 2 + 2; }  // dgrad (pack, gemm), wgrad (gemm, reduce), dbias (partial, reduce)
+// dgrad (pack, gemm), wgrad (sorted dY copy when Cout >= 128, gemm, reduce), dbias (partial, reduce)
+int tc_bwd_launches(int Cout) { return 2 + (wg_bn(Cout) >= 128 ? 3 : 2) + 2; }
 
 }  // namespace vg
