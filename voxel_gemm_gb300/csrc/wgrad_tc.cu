@@ -504,8 +504,10 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, cudaStream_t s) {
 
 }  // namespace
 
-// Split-K chunk count: about four work units per SM, at least 4 tiles per chunk
-// (every chunk non-empty), partial sums capped at 1 GiB.
+// Split-K chunk count: about four work units per SM and chunks of at most 256
+// tiles (the units running side by side then stream the same rows through L2;
+// measured at 602k voxels, C = 1024: 2 chunks 17.6 ms, 8 chunks 16.1 ms), at
+// least 4 tiles per chunk (every chunk non-empty), partial sums capped at 1 GiB.
 int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
     const int bn = wg_bn(Cout);
     const int mu = bn == 64 ? WCfg<64>::MU : (bn == 128 ? WCfg<128>::MU : WCfg<256>::MU);
@@ -513,6 +515,7 @@ int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
     const int64_t MG = (num_munits(Cin) + mu - 1) / mu;
     const int64_t per_split = MG * (Cout / bn);
     int64_t S = std::max<int64_t>(1, (4 * 152 + per_split - 1) / per_split);
+    S = std::max<int64_t>(S, (T + 255) / 256);
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
