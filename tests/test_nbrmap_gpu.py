@@ -23,7 +23,7 @@ def gpu_map(coords_np, grid, flags=0):
 
 
 def order_keys(coords, mask, grid):
-    """The documented sort key: 128^3 Morton blocks, the tap mask, then the 8^3 sub-block."""
+    """The documented sort key: 128^3 Morton blocks, the tap mask, then the top G fine Morton bits."""
     B, X, Y, Z = grid
     L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
     c = coords.astype(np.uint64)
@@ -31,8 +31,13 @@ def order_keys(coords, mask, grid):
     for b in range(L):
         for col, pos in ((1, 2), (2, 1), (3, 0)):
             m |= ((c[:, col] >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b + pos)
-    F = np.uint64(min(3 * L, 21))
-    G = np.uint64(min(3 * L, 21, 6))
+    lb = int(np.ceil(np.log2(B))) if B > 1 else 0
+    F = min(3 * L, 21)
+    G = min(F, 6)
+    coarse = lb + 3 * L - F
+    if coarse + 27 + G > 32 and coarse + 27 <= 32:
+        G = 32 - 27 - coarse
+    F, G = np.uint64(F), np.uint64(G)
     fine = (m & ((np.uint64(1) << F) - np.uint64(1))) >> (F - G)
     return ((m >> F) << (np.uint64(27) + G)) | (mask.astype(np.uint64) << G) | fine
 

@@ -42,6 +42,7 @@ struct NbrLayout {
     int key64 = 0;          // hash keys are 64-bit
     int sort64 = 0;         // Morton sort keys are 64-bit
     int sort_bits = 0;      // significant bits of the Morton key
+    int fine_keep = 0;      // G: fine Morton bits kept below the tap mask
     int cap_log2 = 0;       // hash capacity = 2^cap_log2
     int64_t num_tiles = 0;  // ceil(n / 128)
     int64_t sort_blocks = 0;
@@ -56,6 +57,6 @@ constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digi
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 constexpr int kFineOrderBits = 21;                    // fine Morton bits below the tap mask (128^3 blocks)
-constexpr int kKeptFineBits = 6;                      // of those, the top ones kept in the key (4x4x4 split of a block)
+constexpr int kKeptFineBits = 6;                      // of those, at most this many kept in the key (4x4x4 split of a block)
 
 }  // namespace vg

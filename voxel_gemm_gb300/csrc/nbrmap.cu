@@ -76,7 +76,7 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
 // the top G fine Morton bits (a 4x4x4 split of the block).  Below that the stable sort keeps
 // the input order; dropping the low Morton bits saves radix passes, and rows with
 // equal masks in one sub-block are gathered alike whatever their order.
-__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
+__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L, int G) {
     uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
     for (int b = 0; b < L; ++b) {
         m |= (uint64_t)(((uint32_t)c.y >> b) & 1u) << (3 * b + 2);
@@ -84,7 +84,6 @@ __device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L) {
         m |= (uint64_t)(((uint32_t)c.w >> b) & 1u) << (3 * b);
     }
     const int F = min(3 * L, kFineOrderBits);
-    const int G = min(F, kKeptFineBits);
     const uint64_t fine = (m & ((uint64_t(1) << F) - 1)) >> (F - G);
     return ((m >> F) << (kTaps + G)) | ((uint64_t)mask << G) | fine;
 }
@@ -149,7 +148,7 @@ __device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
 // MMA) while a block's rows stay spatially close (neighbours reused from L2).
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
-k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L,
+k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L, int G,
                  int passes, uint32_t* __restrict__ mask, SK* __restrict__ keys, uint32_t* __restrict__ ghist) {
     __shared__ uint32_t h[kMaxSortPasses][kRadix];
     const int t = threadIdx.x;
@@ -158,7 +157,7 @@ k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ n
     for (int64_t i = (int64_t)blockIdx.x * kSortThreads + t; i < n; i += (int64_t)gridDim.x * kSortThreads) {
         const uint32_t m = row_mask(nbr + i * kTaps);
         mask[i] = m;
-        const SK key = (SK)order_key(coords[i], m, L);
+        const SK key = (SK)order_key(coords[i], m, L, G);
         keys[i] = key;
         for (int p = 0; p < passes; ++p) atomicAdd(&h[p][(uint32_t)(key >> (p * kRadixBits)) & (kRadix - 1)], 1u);
     }
@@ -366,7 +365,11 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     const int lg = ceil_log2(std::max(X, std::max(Y, Z)));
     // Morton code without its low F - G fine bits, plus the 27-bit valid-tap mask
     const int fine = std::min(3 * lg, kFineOrderBits);
-    l.sort_bits = lb + 3 * lg - (fine - std::min(fine, kKeptFineBits)) + kTaps;
+    // G = min(F, 6) fine bits, fewer when that lets the whole key fit 32 bits
+    const int coarse = lb + 3 * lg - fine;
+    l.fine_keep = std::min(fine, kKeptFineBits);
+    if (coarse + kTaps + l.fine_keep > 32 && coarse + kTaps <= 32) l.fine_keep = 32 - kTaps - coarse;
+    l.sort_bits = coarse + kTaps + l.fine_keep;
     if (l.sort_bits > 64) return VG_ERR_UNSUPPORTED;
     l.sort64 = l.sort_bits > 32 ? 1 : 0;
     if (flags & VG_TEST_SMALL_HASH) {
@@ -433,7 +436,7 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
     const unsigned g = (unsigned)l.sort_blocks;
     cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)passes - l.off_hist, s);  // counts, status, tickets
     const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * 152);
-    k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, passes, mask, ka, hist);
+    k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, passes, mask, ka, hist);
     const uint32_t* vin = nullptr;
     const size_t smem = (size_t)kSortThreads * l.sort_items * (sizeof(SK) + 4);
     cudaFuncSetAttribute(k_onesweep<SK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
