@@ -255,18 +255,46 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
 
+    # The copies run on two more streams (host-to-device and device-to-host) where
+    # the data dependences allow: features and weights go up while the neighbour
+    # map (which needs only the coordinates) is built, dY while the forward runs;
+    # `out` comes back during the backward and dX during the weight gradient (the
+    # backward is issued as its two C-ABI calls: input gradient, then dW and db).
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+
     def e2e_eager():
+        ev_fwd_in, ev_bwd_in, ev_fwd, ev_dx = (torch.cuda.Event() for _ in range(4))
         with torch.cuda.stream(stream):
             coords.copy_(h_coords, non_blocking=True)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
             f.copy_(h_f, non_blocking=True)
             W.copy_(h_W, non_blocking=True)
             b.copy_(h_b, non_blocking=True)
+            ev_fwd_in.record(up)
             dY.copy_(h_dY, non_blocking=True)
-            eager_step()
+            ev_bwd_in.record(up)
+        with torch.cuda.stream(stream):
+            m.build(coords, stream)
+            stream.wait_event(ev_fwd_in)
+            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
+            ev_fwd.record(stream)
+            stream.wait_event(ev_bwd_in)
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws, stream=stream)
+            ev_dx.record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_fwd)
             h_out.copy_(out, non_blocking=True)
+            down.wait_event(ev_dx)
             h_dX.copy_(dX, non_blocking=True)
+        with torch.cuda.stream(stream):
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws, stream=stream)
             h_dW.copy_(dW, non_blocking=True)
             h_db.copy_(db, non_blocking=True)
+            stream.wait_stream(up)
+            stream.wait_stream(down)
 
     e2e_step = graphed(e2e_eager)
 
