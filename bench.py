@@ -165,10 +165,30 @@ def run_ours(args, rank, world, local_rank):
         db = torch.empty(wl.cout, dtype=dt, device=dev)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
+    # The three convolution passes depend only on the map and the inputs, so after
+    # the map build they run on three streams (each with its own conv workspace);
+    # a pass's tail then overlaps the next one's start.  --one-stream issues them
+    # one after the other on the timed stream instead.
+    one_stream = args.one_stream
+    with torch.cuda.stream(stream):
+        ws_dx = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
+        ws_dw = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
+    s_dx = torch.cuda.Stream(device=dev)
+    s_dw = torch.cuda.Stream(device=dev)
+
     def step():
         m.build(coords, stream)
+        if one_stream:
+            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=stream)
+            return
+        s_dx.wait_stream(stream)
+        s_dw.wait_stream(stream)
         ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=stream)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws_dx, stream=s_dx)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws_dw, stream=s_dw)
+        stream.wait_stream(s_dx)
+        stream.wait_stream(s_dw)
 
     def timed(fn, k, ev_list):
         for _ in range(k):
@@ -224,6 +244,7 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(b_) for a, b_ in evs]
     tot_ms = max_over_ranks(sum(step_ms), world, dev)
     assert m.status(stream) == ops.VG_OK and ops.vg_conv_status(ws, stream) == ops.VG_OK
+    assert ops.vg_conv_status(ws_dx, stream) == ops.VG_OK and ops.vg_conv_status(ws_dw, stream) == ops.VG_OK
     ms_per_step = tot_ms / args.steps
 
     # ---- per-pass timings (same stream, same flush rule), for the roofline
@@ -258,8 +279,8 @@ def run_ours(args, rank, world, local_rank):
     # The copies run on two more streams (host-to-device and device-to-host) where
     # the data dependences allow: features and weights go up while the neighbour
     # map (which needs only the coordinates) is built, dY while the forward runs;
-    # `out` comes back during the backward and dX during the weight gradient (the
-    # backward is issued as its two C-ABI calls: input gradient, then dW and db).
+    # `out` comes back during the backward and dX during the weight gradient.  The
+    # conv passes use the same streams as the device-only step.
     up = torch.cuda.Stream(device=dev)
     down = torch.cuda.Stream(device=dev)
 
@@ -276,25 +297,32 @@ def run_ours(args, rank, world, local_rank):
             ev_fwd_in.record(up)
             dY.copy_(h_dY, non_blocking=True)
             ev_bwd_in.record(up)
-        with torch.cuda.stream(stream):
-            m.build(coords, stream)
-            stream.wait_event(ev_fwd_in)
-            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
-            ev_fwd.record(stream)
-            stream.wait_event(ev_bwd_in)
-            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws, stream=stream)
-            ev_dx.record(stream)
+        m.build(coords, stream)
+        dx_stream = stream if one_stream else s_dx
+        dw_stream = stream if one_stream else s_dw
+        dx_ws = ws if one_stream else ws_dx
+        dw_ws = ws if one_stream else ws_dw
+        if not one_stream:
+            s_dx.wait_stream(stream)
+            s_dw.wait_stream(stream)
+        stream.wait_event(ev_fwd_in)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
+        ev_fwd.record(stream)
+        dx_stream.wait_event(ev_bwd_in)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, dx_ws, stream=dx_stream)
+        ev_dx.record(dx_stream)
         with torch.cuda.stream(down):
             down.wait_event(ev_fwd)
             h_out.copy_(out, non_blocking=True)
             down.wait_event(ev_dx)
             h_dX.copy_(dX, non_blocking=True)
-        with torch.cuda.stream(stream):
-            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws, stream=stream)
+        dw_stream.wait_event(ev_bwd_in)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, dw_ws, stream=dw_stream)
+        with torch.cuda.stream(dw_stream):
             h_dW.copy_(dW, non_blocking=True)
             h_db.copy_(db, non_blocking=True)
-            stream.wait_stream(up)
-            stream.wait_stream(down)
+        for st in (up, down) if one_stream else (up, down, s_dx, s_dw):
+            stream.wait_stream(st)
 
     e2e_step = graphed(e2e_eager)
 
@@ -348,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
                    "cout": wl.cout, "step": "nbrmap build + fwd + dgrad + wgrad + dbias",
                    "l2": "flushed between steps (256 MiB write, outside the per-step events)",
                    "parallelism": f"replicas x{world}",
-                   "launch": "eager" if args.no_graph else "CUDA graph replay of the step's C-ABI calls"},
+                   "launch": ("eager" if args.no_graph else "CUDA graph replay of the step's C-ABI calls")
+                   + ("" if one_stream else "; fwd, dgrad and wgrad+db on three streams after the map build")},
         "tflops": world * total_fl / (ms_per_step * 1e-3) / 1e12,
         "roofline_step_frac": t_roof / (ms_per_step * 1e-3),
         "roofline": roof,
@@ -447,6 +476,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--one-stream", action="store_true",
+                    help="issue the step's conv passes one after the other on one stream")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
