@@ -32,7 +32,7 @@ def order_keys(coords, mask, grid):
         for col, pos in ((1, 2), (2, 1), (3, 0)):
             m |= ((c[:, col] >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b + pos)
     lb = int(np.ceil(np.log2(B))) if B > 1 else 0
-    F = min(3 * L, 24)
+    F = min(3 * L, 27)
     G = min(F, 6)
     coarse = lb + 3 * L - F
     if coarse + 27 + G > 32 and coarse + 27 <= 32:
