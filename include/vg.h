@@ -122,10 +122,11 @@ VG_API int vg_nbrmap_status(const void* ws, void* stream);
  *                (the page's sorted_idx).  Stable sort by the key
  *                ((m >> F) << (27 + G)) | (mask << G) | ((m & (2^F - 1)) >> (F - G)),
  *                where m = (b << 3L) | bit-interleave(x, y, z) is the Morton code,
- *                L = ceil(log2(max(X,Y,Z))), F = min(3L, 21) and G = min(F, 6),
+ *                L = ceil(log2(max(X,Y,Z))), F = min(3L, 30) and G = min(F, 6),
  *                lowered to 32 - 27 - (bits of m above F) when that makes the
  *                whole key fit 32 bits (4 radix passes instead of 5):
- *                128^3-voxel Morton blocks, then the valid-tap mask, then the
+ *                batch element (or 1024^3-voxel Morton block of a larger grid),
+ *                then the valid-tap mask, then the
  *                top G fine Morton bits (at most a 4x4x4 split of the block), then the
  *                input order (stable).
  *   tile_mask  [ceil(N/128)] uint32 — OR of mask over sorted rows [128t, 128t+128) */

@@ -55,7 +55,7 @@ def test_host_only_queries(ops):
     # sort-key width of the documented row order: bits of m above F + the 27-bit tap
     # mask + G kept fine bits (G = 6, or fewer so that the key fits 32 bits); 8-bit digits
     for (B, R, bits) in [(4, 64, 2 + 27 + 3), (2, 256, 1 + 27 + 4),
-                         (1, 512, 0 + 27 + 5), (1, 1024, 3 + 27 + 2), (1, 2, 0 + 27 + 3)]:
+                         (1, 512, 0 + 27 + 5), (1, 1024, 0 + 27 + 5), (1, 2, 0 + 27 + 3)]:
         d = ops.vg_nbrmap_describe(1000, B, R, R, R)
         assert d["sort_bits"] == bits and d["sort_passes"] == (bits + 7) // 8, (B, R, d)
 

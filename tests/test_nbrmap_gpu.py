@@ -23,7 +23,7 @@ def gpu_map(coords_np, grid, flags=0):
 
 
 def order_keys(coords, mask, grid):
-    """The documented sort key: 128^3 Morton blocks, the tap mask, then the top G fine Morton bits."""
+    """The documented sort key: batch element (1024^3 Morton block), the tap mask, then the top G fine Morton bits."""
     B, X, Y, Z = grid
     L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
     c = coords.astype(np.uint64)
@@ -32,7 +32,7 @@ def order_keys(coords, mask, grid):
         for col, pos in ((1, 2), (2, 1), (3, 0)):
             m |= ((c[:, col] >> np.uint64(b)) & np.uint64(1)) << np.uint64(3 * b + pos)
     lb = int(np.ceil(np.log2(B))) if B > 1 else 0
-    F = min(3 * L, 27)
+    F = min(3 * L, 30)
     G = min(F, 6)
     coarse = lb + 3 * L - F
     if coarse + 27 + G > 32 and coarse + 27 <= 32:

@@ -56,7 +56,7 @@ constexpr int kSortThreads = 256;
 constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digits
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
-constexpr int kFineOrderBits = 27;                    // fine Morton bits below the tap mask (512^3 blocks)
-constexpr int kKeptFineBits = 6;                      // of those, at most this many kept in the key (4x4x4 split of a block)
+constexpr int kFineOrderBits = 30;                    // Morton bits below the tap mask (1024^3 blocks)
+constexpr int kKeptFineBits = 6;                      // of those, at most this many kept in the key (4x4x4 split)
 
 }  // namespace vg

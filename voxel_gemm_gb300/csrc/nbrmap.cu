@@ -141,11 +141,13 @@ __device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
 // Row-order sort key of every voxel, its valid-tap mask, and the digit
 // histograms of every radix pass (all passes in one read of the keys):
 //   m   = (b << 3L) | interleave(x, y, z)            Morton (z-order) code
-//   key = ((m >> F) << (27 + F)) | (mask << F) | (m & (2^F - 1)),  F = min(3L, 21)
-// i.e. coarse Morton block of 128^3 voxels, then the valid-tap mask, then the
-// fine Morton order (the page's sorted_idx groups rows for the masked GEMM).
-// Rows of one tile then share most of their taps (few zero-filled rows in the
-// MMA) while a block's rows stay spatially close (neighbours reused from L2).
+//   key = ((m >> F) << (27 + G)) | (mask << G) | ((m mod 2^F) >> (F - G))
+// with F = min(3L, 30): the batch element (a 1024^3 block of a larger grid),
+// then the valid-tap mask, then the top G fine Morton bits (the page's
+// sorted_idx groups rows for the masked GEMM).  Rows of one tile then share
+// nearly all of their taps (few zero-filled rows in the MMA: 88 % of the rows
+// useful on a 512^3 surface, 95 % on 1024^3) while rows of one mask stay in
+// Morton order (neighbours of consecutive tiles reused from L2).
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
 k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L, int G,
