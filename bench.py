@@ -1,9 +1,12 @@
 """Benchmark: one step = the whole submanifold-conv hot path on one batch of
 seeded synthetic voxels, through the C ABI:
-    neighbour-map build (hash, probe, Morton sort, tile masks)
-    -> forward -> input gradient -> weight and bias gradient.
+    neighbour-map build (hash, probe, row-order sort, tile masks)
+    -> forward, input gradient, weight and bias gradient (three streams after
+       the map build, each call with its own conv workspace; --one-stream runs
+       them one after the other).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                [--no-graph] [--one-stream] [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0).  ``value`` = voxels/s over all ranks (each rank
 runs its own independent replica of the workload: weak scaling, no data-path
