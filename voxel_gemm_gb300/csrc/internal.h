@@ -22,6 +22,11 @@ inline size_t sorted_nbr_offset(int64_t N) {
     const size_t tiles = (size_t)((N + 127) / 128);
     return tile_mask_offset(N) + ((4 * tiles + 255) / 256) * 256;
 }
+// Tile visiting order of the weight gradient (tiles grouped by spatial region).
+inline size_t tile_order_offset(int64_t N) {
+    const size_t tiles = (size_t)((N + 127) / 128);
+    return sorted_nbr_offset(N) + ((4 * 27 * 128 * tiles + 255) / 256) * 256;
+}
 
 // ---- convolution passes (all asynchronous on stream s) ----
 // One "gather GEMM" pass over the sorted rows:
@@ -53,6 +58,7 @@ struct WgradPass {
     const uint32_t* sorted_idx;
     const uint32_t* tile_mask;
     const uint32_t* sorted_nbr;
+    const uint32_t* tile_order;  // [tiles] visiting order: tiles grouped by spatial region
     const uint32_t* nbr;
     const uint32_t* mask;
     const uint32_t* nbr_status;

@@ -76,13 +76,19 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
 // the top G fine Morton bits (a 4x4x4 split of the block).  Below that the stable sort keeps
 // the input order; dropping the low Morton bits saves radix passes, and rows with
 // equal masks in one sub-block are gathered alike whatever their order.
-__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L, int G) {
+// Morton (z-order) code (b << 3L) | interleave(x, y, z) of a voxel.
+__device__ __forceinline__ uint64_t morton(int4 c, int L) {
     uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
     for (int b = 0; b < L; ++b) {
         m |= (uint64_t)(((uint32_t)c.y >> b) & 1u) << (3 * b + 2);
         m |= (uint64_t)(((uint32_t)c.z >> b) & 1u) << (3 * b + 1);
         m |= (uint64_t)(((uint32_t)c.w >> b) & 1u) << (3 * b);
     }
+    return m;
+}
+
+__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L, int G) {
+    const uint64_t m = morton(c, L);
     const int F = min(3 * L, kFineOrderBits);
     const uint64_t fine = (m & ((uint64_t(1) << F) - 1)) >> (F - G);
     return ((m >> F) << (kTaps + G)) | ((uint64_t)mask << G) | fine;
@@ -317,10 +323,15 @@ k_onesweep(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK* __r
 // Per 128-row tile of the processing order: the OR of the rows' tap masks, and
 // the tile's neighbour lists copied into processing order,
 // sorted_nbr[r][k] = nbr[sorted_idx[r]][k] (VG_NONE for padding rows past n).
+// Also the tile's region key (Morton bits above F - G of its first row: the
+// spatial region its rows were sorted within) and that key's digit counts for
+// the tile sort that orders the weight gradient's tiles region by region.
 __global__ void __launch_bounds__(kTileRows)
 k_tile_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
             const uint32_t* __restrict__ mask, int64_t n, uint32_t* __restrict__ tmask,
-            uint32_t* __restrict__ sorted_nbr) {
+            uint32_t* __restrict__ sorted_nbr, const int4* __restrict__ coords, int L, int G,
+            int tile_passes, uint32_t* __restrict__ tkey, uint32_t* __restrict__ thist,
+            uint32_t* __restrict__ torder) {
     __shared__ uint32_t rows[kTileRows];
     __shared__ uint32_t w[kTileRows / 32];
     const int64_t r = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
@@ -334,6 +345,15 @@ k_tile_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict_
         uint32_t o = 0;
         for (int i = 0; i < kTileRows / 32; ++i) o |= w[i];
         tmask[blockIdx.x] = o;
+        if (tile_passes == 0) {  // no tile sort: the visiting order is the sorted order
+            torder[blockIdx.x] = blockIdx.x;
+        } else {
+            const int F = min(3 * L, kFineOrderBits);
+            const uint32_t key = (uint32_t)(morton(coords[rows[0]], L) >> (F - G));  // rows[0] < n always
+            tkey[blockIdx.x] = key;
+            for (int p = 0; p < tile_passes; ++p)
+                atomicAdd(&thist[p * kRadix + ((key >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+        }
     }
     uint32_t* dst = sorted_nbr + (int64_t)blockIdx.x * kTileRows * kTaps;
     for (int e = threadIdx.x; e < kTileRows * kTaps; e += kTileRows) {
@@ -402,16 +422,29 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     l.off_sorted = o;   o += align_up(4 * (size_t)N, 256);
     l.off_tmask = o;    o += align_up(4 * (size_t)l.num_tiles, 256);
     l.off_nbr_sorted = o; o += align_up(4 * (size_t)kTaps * kTileRows * l.num_tiles, 256);
+    l.off_torder = o;   o += align_up(4 * (size_t)l.num_tiles, 256);  // offset depends on N only
+    l.off_tkey_a = o;   o += align_up(4 * (size_t)l.num_tiles, 256);
+    l.off_tkey_b = o;   o += align_up(4 * (size_t)l.num_tiles, 256);
+    l.off_torder_b = o; o += align_up(4 * (size_t)l.num_tiles, 256);
     l.off_table = o;    o += align_up(slot * cap, 256);
     l.off_skeys_a = o;  o += align_up(ss * (size_t)N, 256);
     l.off_skeys_b = o;  o += align_up(ss * (size_t)N, 256);
     l.off_svals_b = o;  o += align_up(4 * (size_t)N, 256);
     // one-sweep radix sort: global digit counts of every pass, then per pass the
     // tiles' published counts and a ticket counter (all zeroed by one memset)
+    // (the tile region sort's passes follow the row sort's in the same arrays)
+    // (up to 2^17 voxels the features of a layer stay in L2 whatever the order:
+    // no tile sort, the visiting order is the sorted order)
+    const int region_bits = std::min(32, coarse + l.fine_keep);
+    l.tile_passes = N <= (int64_t(1) << 17) ? 0 : std::max(1, (region_bits + kRadixBits - 1) / kRadixBits);
+    l.tile_blocks = std::max<int64_t>(1, (l.num_tiles + (int64_t)kSortThreads * l.sort_items - 1) /
+                                             ((int64_t)kSortThreads * l.sort_items));
     const int passes = std::max(1, (l.sort_bits + kRadixBits - 1) / kRadixBits);
-    l.off_hist = o;     o += align_up(4 * (size_t)kRadix * passes, 256);
-    l.off_status = o;   o += align_up(8 * (size_t)kRadix * l.sort_blocks * passes, 256);
-    l.off_tickets = o;  o += align_up(4 * (size_t)passes, 256);
+    const int all = passes + l.tile_passes;
+    const int64_t sblocks = std::max(l.sort_blocks, l.tile_blocks);
+    l.off_hist = o;     o += align_up(4 * (size_t)kRadix * all, 256);
+    l.off_status = o;   o += align_up(8 * (size_t)kRadix * sblocks * all, 256);
+    l.off_tickets = o;  o += align_up(4 * (size_t)all, 256);
     l.total = o;
     *L = l;
     return VG_OK;
@@ -441,7 +474,9 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
         coords, n, X, Y, Z, table, l.cap_log2, nbr);
     const int passes = nbr_sort_passes(l);
     const unsigned g = (unsigned)l.sort_blocks;
-    cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)passes - l.off_hist, s);  // counts, status, tickets
+    const int all = passes + l.tile_passes;
+    const int64_t sblocks = std::max(l.sort_blocks, l.tile_blocks);
+    cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)all - l.off_hist, s);  // counts, status, tickets
     const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * 152);
     k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, passes, mask, ka, hist);
     const uint32_t* vin = nullptr;
@@ -453,13 +488,33 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
         uint32_t* vout = ((passes - 1 - p) % 2 == 0) ? v0 : v1;
         k_onesweep<SK><<<g, kSortThreads, smem, s>>>(
             kin, vin, kout, vout, n, p * kRadixBits, hist + p * kRadix,
-            reinterpret_cast<uint64_t*>(ws + l.off_status) + (size_t)p * kRadix * l.sort_blocks,
+            reinterpret_cast<uint64_t*>(ws + l.off_status) + (size_t)p * kRadix * sblocks,
             reinterpret_cast<uint32_t*>(ws + l.off_tickets) + p, l.sort_items, status);
         vin = vout;
     }
+    uint32_t* tka = reinterpret_cast<uint32_t*>(ws + l.off_tkey_a);
+    uint32_t* tkb = reinterpret_cast<uint32_t*>(ws + l.off_tkey_b);
+    uint32_t* to0 = reinterpret_cast<uint32_t*>(ws + l.off_torder);
+    uint32_t* to1 = reinterpret_cast<uint32_t*>(ws + l.off_torder_b);
     k_tile_rows<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
         v0, nbr, mask, n, reinterpret_cast<uint32_t*>(ws + l.off_tmask),
-        reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted));
+        reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted), coords, L, l.fine_keep, l.tile_passes, tka,
+        hist + passes * kRadix, to0);
+    // stable sort of the tiles by region key: the weight gradient's visiting order
+    const size_t tsmem = (size_t)kSortThreads * l.sort_items * (sizeof(uint32_t) + 4);
+    cudaFuncSetAttribute(k_onesweep<uint32_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tsmem);
+    const uint32_t* tvin = nullptr;
+    for (int p = 0; p < l.tile_passes; ++p) {
+        const int q = passes + p;
+        const uint32_t* kin = (p % 2 == 0) ? tka : tkb;
+        uint32_t* kout = (p % 2 == 0) ? tkb : tka;
+        uint32_t* vout = ((l.tile_passes - 1 - p) % 2 == 0) ? to0 : to1;
+        k_onesweep<uint32_t><<<(unsigned)l.tile_blocks, kSortThreads, tsmem, s>>>(
+            kin, tvin, kout, vout, l.num_tiles, p * kRadixBits, hist + q * kRadix,
+            reinterpret_cast<uint64_t*>(ws + l.off_status) + (size_t)q * kRadix * sblocks,
+            reinterpret_cast<uint32_t*>(ws + l.off_tickets) + q, l.sort_items, status);
+        tvin = vout;
+    }
 }
 
 int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,

@@ -105,7 +105,8 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     info[0] = l.key64;
     info[1] = l.sort_bits;
     info[2] = passes;
-    info[3] = N > 0 ? 3 + passes + 1 : 0;  // insert, probe, keys + digit counts, passes, tile rows
+    // insert, probe, keys + digit counts, passes, tile rows, tile-order passes
+    info[3] = N > 0 ? 4 + passes + l.tile_passes : 0;
     return VG_OK;
 }
 
@@ -231,6 +232,7 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         w.sorted_idx = vg_nbrmap_sorted_idx(nbr_ws);
         w.tile_mask = vg_nbrmap_tile_mask(nbr_ws, N);
         w.sorted_nbr = vg_nbrmap_sorted_nbr(nbr_ws, N);
+        w.tile_order = reinterpret_cast<const uint32_t*>(static_cast<const char*>(nbr_ws) + tile_order_offset(N));
         w.nbr = nbr;
         w.mask = mask;
         w.nbr_status = nbr_status;

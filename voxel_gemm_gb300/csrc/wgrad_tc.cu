@@ -13,8 +13,10 @@
 // Both operands are stored as rows of the sorted order, i.e. MN-major: a row
 // holds 64 consecutive channels (128 B, swizzled).  M = 128 covers two 64-channel
 // blocks, each a (tap, 64 channels) slot; slots are paired in tap-major order.
-// A work unit = (M block, N block, row chunk); a row chunk's 128-row tiles whose
-// tile mask has none of the unit's taps are skipped (their A rows would be zero).
+// A work unit = (M block, N block, row chunk); a row chunk is a range of the
+// tile visiting order (the sorted row tiles regrouped by spatial region, so a
+// chunk's gathers stay within a few regions of the grid), and a chunk's tiles
+// whose tile mask has none of the unit's taps are skipped (their A rows would be zero).
 // Each unit writes an fp32 partial [128 x BN] for its chunk; a second kernel sums
 // the chunks in a fixed order (bitwise deterministic).
 //
@@ -66,6 +68,7 @@ struct WCfg {
 struct WgArgs {
     const uint32_t* sorted_idx;
     const uint32_t* tile_mask;
+    const uint32_t* tile_order;  // position -> tile
     const uint32_t* sorted_nbr;
     const uint32_t* nbr_status;
     int64_t n;
@@ -132,19 +135,20 @@ __device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit (&mu)[MU]
     }
 }
 
-// Walks the active 128-row tiles of one chunk, 32 tile masks per coalesced warp load.
+// Walks the active tiles of one chunk (positions [base, end) of the tile visiting
+// order), 32 positions per warp-wide load.
 struct TileCursor {
     int64_t base, end;
-    uint32_t bits;  // active tiles in [base, base + 32) not yet returned
+    uint32_t bits;  // active positions in [base, base + 32) not yet returned
 };
 __device__ __forceinline__ uint32_t window_bits(const WgArgs& a, int64_t base, int64_t end, int64_t first,
                                                 uint32_t umask, int lane) {
-    const int64_t t = base + lane;
+    const int64_t pos = base + lane;
     bool act = false;
-    if (t < end) act = (a.tile_mask[t] & umask) != 0u || t == first;
+    if (pos < end) act = (a.tile_mask[a.tile_order[pos]] & umask) != 0u || pos == first;
     return __ballot_sync(0xffffffffu, act);
 }
-// Next active tile (or -1); all lanes of the warp call it together.
+// Tile index of the next active position (or -1); all lanes of the warp call it together.
 __device__ __forceinline__ int64_t next_tile(const WgArgs& a, TileCursor& c, int64_t first, uint32_t umask,
                                              int lane) {
     while (c.bits == 0u) {
@@ -154,7 +158,7 @@ __device__ __forceinline__ int64_t next_tile(const WgArgs& a, TileCursor& c, int
     }
     const int b = __ffs(c.bits) - 1;
     c.bits &= c.bits - 1u;
-    return c.base + b;
+    return (int64_t)a.tile_order[c.base + b];
 }
 
 // 2D TMA tile load (box of 64 columns x R rows, 128-byte swizzle) completing on an mbarrier.
@@ -536,6 +540,7 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.sorted_idx = p.sorted_idx;
         a.tile_mask = p.tile_mask;
         a.sorted_nbr = p.sorted_nbr;
+        a.tile_order = p.tile_order;
         a.nbr_status = p.nbr_status;
         a.n = p.n;
         a.num_tiles = (p.n + kTileRows - 1) / kTileRows;

@@ -231,4 +231,4 @@ def conv_workspace(N, Cin, Cout, dtype, device="cuda", flags=0) -> torch.Tensor:
     nb = vg_conv_workspace_bytes(N, Cin, Cout, dtype, flags)
     if nb == 0:
         raise VGError(VG_ERR_UNSUPPORTED, "vg_conv_workspace_bytes")
-    return torch.empty(nb, dtype=torch.uint8, device=device)
+    return torch.zeros(nb, dtype=torch.uint8, device=device)  # zero error record before any call
