@@ -518,6 +518,15 @@ def main():
                                    "sample": f"full map of N={coords_np.shape[0]}, fwd+dgrad+wgrad over "
                                              f"{info['rows']} sampled rows ({info['t_map_s']:.2f}s map, "
                                              f"{info['t_conv_s']:.2f}s conv)"}
+            # the same oracle on one host core, over a smaller row sample (about 3 s)
+            cores = oracle.num_threads()
+            oracle.set_num_threads(1)
+            try:
+                v1, info1 = oracle_sample(wl, coords_np, max(64, rows_budget(wl) // 8), min_seconds=3.0)
+            finally:
+                oracle.set_num_threads(cores)
+            res["cpu_baseline"]["value_1core"] = v1
+            res["cpu_baseline"]["sample_1core"] = f"{info1['rows']} sampled rows ({info1['t_conv_s']:.2f}s conv)"
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
