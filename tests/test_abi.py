@@ -58,6 +58,32 @@ def test_host_only_queries(ops):
                          (1, 512, 0 + 27 + 5), (1, 1024, 0 + 27 + 5), (1, 2, 0 + 27 + 3)]:
         d = ops.vg_nbrmap_describe(1000, B, R, R, R)
         assert d["sort_bits"] == bits and d["sort_passes"] == (bits + 7) // 8, (B, R, d)
+    # kernels per build: insert, probe, keys, the radix passes, tile rows, and above
+    # 2^17 voxels one more pass ordering the tiles region by region
+    assert ops.vg_nbrmap_describe(1 << 17, 1, 512, 512, 512)["launches"] == 4 + 4
+    assert ops.vg_nbrmap_describe((1 << 17) + 1, 1, 512, 512, 512)["launches"] == 4 + 4 + 1
+    # the 64-bit hash path leaves the plan otherwise unchanged
+    d32 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY32)
+    d64 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY64)
+    assert (d32["key64"], d64["key64"]) == (0, 1) and d32["sort_passes"] == d64["sort_passes"]
+
+
+def test_split_k_plan(ops):
+    """Split-K chunks of the tensor-core weight gradient: about four work units per SM,
+    at most 256 tiles per chunk, at least 4 tiles per chunk when there are enough,
+    and fp32 partial sums of at most 1 GiB."""
+    for N, C in [(25179, 64), (319057, 128), (602492, 256), (602492, 512), (602492, 1024),
+                 (4915386, 64), (1000, 64), (128, 256)]:
+        d = ops.vg_conv_describe(N, C, C, ops.VG_BF16)
+        assert d["tensor_core"] == 1
+        S, T = d["splits"], (N + 127) // 128
+        tpc = (T + S - 1) // S  # tiles per chunk
+        assert 1 <= S <= T and (S - 1) * tpc < T, (N, C, S)  # every chunk non-empty
+        assert S * 27 * C * C * 4 <= (1 << 30) or S == 1, (N, C, S)
+        if T >= 4:
+            assert tpc >= 4 or S == 1, (N, C, S)
+        if (T + 255) // 256 * 27 * C * C * 4 <= (1 << 30):  # 256-tile chunks fit the cap
+            assert tpc <= 256, (N, C, S)
 
 
 def test_argument_errors_return_before_any_launch(ops):
