@@ -180,3 +180,58 @@ def test_cuda_graph_capture_matches_eager():
         outs[mode] = [t_.clone() for t_ in (out, dX, dW, db)]
     for a_, b_ in zip(outs["eager"], outs["graph"]):
         assert torch.equal(a_, b_)
+
+
+@pytest.mark.parametrize("name", ["b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16"])
+def test_three_streams_match_one_stream(name):
+    # the benchmark's step: after the map build, forward, input gradient and weight
+    # gradient run on three streams, each with its own conv workspace, sharing the map;
+    # replayed from a CUDA graph it must give the same bits as the calls on one stream
+    wl = synth.WORKLOADS[name]
+    coords = torch.from_numpy(coords_of(name)).cuda()
+    N = coords.shape[0]
+    f, W, b, dY = (t.cuda() for t in synth.make_tensors(wl, N))
+    m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag)
+    ws = [ops.conv_workspace(N, wl.cin, wl.cout, f.dtype) for _ in range(3)]
+    s0, s1, s2 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def outputs():
+        return (torch.empty(N, wl.cout, dtype=f.dtype, device="cuda"),
+                torch.empty(N, wl.cin, dtype=f.dtype, device="cuda"),
+                torch.empty_like(W), torch.empty_like(b))
+
+    ref = outputs()
+    with torch.cuda.stream(s0):
+        m.build(coords, s0)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, ref[0], ws[0], stream=s0)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, ref[1], ref[2], ref[3], ws[0], stream=s0)
+    s0.synchronize()
+    got = outputs()
+
+    def step():
+        m.build(coords, s0)
+        s1.wait_stream(s0)
+        s2.wait_stream(s0)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, got[0], ws[0], stream=s0)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, got[1], None, None, ws[1], stream=s1)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, got[2], got[3], ws[2], stream=s2)
+        s0.wait_stream(s1)
+        s0.wait_stream(s2)
+
+    with torch.cuda.stream(s0):
+        step()  # eager, also sets kernel attributes before the capture
+    s0.synchronize()
+    for t_, r_ in zip(got, ref):
+        assert torch.equal(t_, r_)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s0):
+        step()
+    for t_ in got:
+        t_.zero_()
+    with torch.cuda.stream(s0):
+        g.replay()
+    s0.synchronize()
+    assert m.status(s0) == ops.VG_OK
+    assert all(ops.vg_conv_status(w, s0) == ops.VG_OK for w in ws)
+    for t_, r_ in zip(got, ref):
+        assert torch.equal(t_, r_)
