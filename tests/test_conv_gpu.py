@@ -235,3 +235,14 @@ def test_three_streams_match_one_stream(name):
     assert all(ops.vg_conv_status(w, s0) == ops.VG_OK for w in ws)
     for t_, r_ in zip(got, ref):
         assert torch.equal(t_, r_)
+
+
+@pytest.mark.parametrize("dtype,cin,cout", [("f16", 64, 128), ("f32", 24, 16)])
+def test_anisotropic_grid(dtype, cin, cout):
+    # three different grid extents and three batch elements: the linearisation,
+    # the tap offsets and the row order must keep the axes apart
+    grid = (3, 5, 9, 13)
+    coords = synth.random_coords(77, 700, *grid)
+    wl = synth.Workload("t", 3, 13, 0, ("sphere",), cin, cout, dtype, 11, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    full_check(coords, grid, f, W, b, dY, TOL[dtype])

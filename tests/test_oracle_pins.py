@@ -43,7 +43,20 @@ def _sphere_case(cin=4, cout=6, seed=3):
     return coords, wl.grid, f, W, b, dY
 
 
-CASES = {"random8": _small_case, "sphere16": _sphere_case}
+def _aniso_case(seed=7, n=300, cin=3, cout=4):
+    # a grid with three different extents and three batch elements, so a mix-up of
+    # the axes in the linearisation or in the tap offsets cannot go unnoticed
+    grid = (3, 5, 9, 13)
+    coords = synth.random_coords(seed, n, *grid)
+    rng = np.random.default_rng(seed + 100)
+    f = rng.standard_normal((coords.shape[0], cin))
+    W = rng.standard_normal((27, cin, cout))
+    b = rng.standard_normal(cout)
+    dY = rng.standard_normal((coords.shape[0], cout))
+    return coords, grid, f, W, b, dY
+
+
+CASES = {"random8": _small_case, "sphere16": _sphere_case, "aniso_3x5x9x13": _aniso_case}
 
 
 def _brute_nbr(coords, grid):
