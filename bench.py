@@ -3,15 +3,23 @@ seeded synthetic voxels, through the C ABI:
     neighbour-map build (hash, probe, row-order sort, tile masks)
     -> forward, input gradient, weight and bias gradient (three streams after
        the map build, each call with its own conv workspace; --one-stream runs
-       them one after the other).
+       them one after the other)
+    -> with N > 1 ranks: the weight and bias gradients of all ranks summed in
+       rank order (the data-parallel exchange step; every rank ends with the
+       same bits).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                [--no-graph] [--one-stream] [--no-cpu-baseline]
+                [--no-graph] [--one-stream] [--no-cpu-baseline] [--no-sweep]
 
-Prints ONE JSON line (rank 0).  ``value`` = voxels/s over all ranks (each rank
-runs its own independent replica of the workload: weak scaling, no data-path
-collective).  Per-step device time comes from CUDA events on the launch
-stream; L2 is flushed (256 MiB write) between steps, outside the events.
+Prints ONE JSON line (rank 0).  The headline workload (default: batch 1, 512^3
+grid, Cin = Cout = 1024, bf16) gets the full record: step time, per-pass
+roofline, end-to-end time with host buffers, clocks, CPU oracle baseline.
+``sweep`` holds one shorter record per other workload (ms/step, per-pass ms
+and roofline fractions).  ``value`` = voxels/s over all ranks: each rank runs
+its own batch element(s) of the same shape (weak scaling, weights
+replicated, gradients summed across ranks).  Per-step device time comes from
+CUDA events on the launch stream; L2 is flushed (256 MiB write) between
+steps, outside the events.
 """
 from __future__ import annotations
 
@@ -27,8 +35,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "submanifold conv3d fwd+bwd voxels/s & TFLOP/s (valid pairs), % of GB300 roofline"
-DEFAULT_WORKLOAD = "b4_r64_spheres_c64_f16"
+DEFAULT_WORKLOAD = "b1_r512_shapes_c1024_bf16"
+SWEEP = ["b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16",
+         "b1_r512_shapes_c512_bf16", "b1_r1024_shapes_c64_f16"]
+STEP = "nbrmap build + fwd + dgrad + wgrad + dbias"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 << 20
 
 
 def load_peaks():
@@ -44,15 +56,21 @@ def load_peaks():
 
 # ------------------------------------------------------------------ work model
 def pass_work(N, P, cin, cout, s, splits):
-    """Algorithmic FLOPs and gathered+written bytes per pass (valid pairs only)."""
+    """Algorithmic FLOPs and gathered+written bytes per pass (valid pairs only).
+    The weight gradient's bytes include its split-K partial sums (written once,
+    read once by the reduce); ``splitk_bytes`` gives that share separately."""
     nbr_bytes = 4 * 28 * N  # nbr [N,27] + mask [N]
     w = 27 * cin * cout * s
     return {
         "fwd": (2.0 * P * cin * cout, P * cin * s + N * cout * s + nbr_bytes + w),
         "dgrad": (2.0 * P * cin * cout, P * cout * s + N * cin * s + nbr_bytes + w),
-        "wgrad": (2.0 * P * cin * cout, P * cin * s + P * cout * s + 2 * splits * 27 * cin * cout * 4
+        "wgrad": (2.0 * P * cin * cout, P * cin * s + P * cout * s + splitk_bytes(cin, cout, splits)
                   + 27 * cin * cout * s + N * cout * s),
     }
+
+
+def splitk_bytes(cin, cout, splits):
+    return 2 * splits * 27 * cin * cout * 4
 
 
 def unique_bytes(N, cin, cout, s):
@@ -66,6 +84,26 @@ def nbrmap_bytes(N):
     return 16 * N * 3 + 27 * 12 * N + 4 * 28 * N
 
 
+def count_pairs(mask_u32) -> int:
+    """P = number of valid (voxel, tap) pairs = total popcount of the tap masks."""
+    import numpy as np
+    m = np.asarray(mask_u32, dtype=np.uint32)
+    return int(sum(int(((m >> k) & 1).sum()) for k in range(27)))
+
+
+def workload_config(wl, N, P, world):
+    """The workload description both arms print (identical dicts)."""
+    s = 4 if wl.dtype == "f32" else 2
+    in_bytes = N * (wl.cin + wl.cout) * s
+    l2 = ("flushed between steps (256 MiB write, outside the per-step events); inputs "
+          + ("larger than L2" if in_bytes > L2_BYTES else "smaller than L2")
+          + f" ({in_bytes / 1e6:.1f} MB of features + grad_out)")
+    return {"workload": wl.name, "B": wl.B, "res": wl.res, "N": int(N), "P": int(P), "cin": wl.cin,
+            "cout": wl.cout, "dtype": wl.dtype, "global_batch": wl.B * world, "step": STEP, "l2": l2,
+            "parallelism": "single GPU" if world == 1 else f"data-parallel x{world} (batch-sharded, "
+                           "weights replicated, rank-ordered gradient sum)"}
+
+
 # ------------------------------------------------------------------ ncu traffic
 def source_digest(kernel: str) -> str:
     import hashlib
@@ -76,19 +114,22 @@ def source_digest(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str, kernel: str):
-    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary
-    profiles/traffic.json, or None if absent or taken on a different kernel source."""
+def measured_traffic(workload: str, kernel: str, P: int):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the committed
+    ncu summary profiles/traffic.json (captured on a smaller case of the same kernel and
+    channel count, scaled by valid pairs), or None if absent or taken on other sources."""
     try:
-        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[workload][kernel]
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["kernels"][workload][kernel]
     except Exception:
         return None
-    return rec["dram_bytes_per_launch"] if rec.get("source_digest") == source_digest(kernel) else None
+    if rec.get("source_digest") != source_digest(kernel):
+        return None
+    return rec["dram_bytes_per_pair"] * P
 
 
 # ------------------------------------------------------------------ ranks
 def max_over_ranks(value: float, world: int, device=None) -> float:
-    """Slowest rank's value (the timed region ends when every replica is done)."""
+    """Slowest rank's value (the timed region ends when every rank is done)."""
     if world <= 1:
         return float(value)
     import torch
@@ -99,7 +140,7 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 
 
 def aggregate_voxels_per_s(n_per_rank: int, world: int, ms_per_step: float) -> float:
-    """Whole-job throughput: every rank processes its own replica of n_per_rank voxels."""
+    """Whole-job throughput: every rank processes its own batch element(s) of n_per_rank voxels."""
     return world * n_per_rank / (ms_per_step * 1e-3)
 
 
@@ -112,92 +153,120 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.out = None
+        self.path = os.path.join("/tmp", f"vg_clocks_{os.getpid()}_{gpu_index}.csv")
+        self.mark = 0
 
-    def start(self):
+    def start(self, wait_s=3.0):
+        """Start nvidia-smi sampling every 100 ms and return once it has written a sample."""
         try:
-            self.out = open(os.devnull if False else os.path.join("/tmp", f"vg_clocks_{os.getpid()}.csv"), "w")
+            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100", "-i", str(self.gpu)], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < wait_s and os.path.getsize(self.path) == 0:
+            time.sleep(0.05)
+
+    def begin_region(self):
+        if self.proc is None:
+            return
+        self.out.flush()
+        self.mark = os.path.getsize(self.path)
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)  # let the sample that covers the end of the region land
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.out.close()
-        rows = []
-        for line in open(self.out.name):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
-        os.unlink(self.out.name)
+        with open(self.path) as fh:
+            fh.seek(self.mark)
+            lines = fh.read().splitlines()
+        os.unlink(self.path)
+        rows = [[p.strip() for p in ln.split(",")] for ln in lines]
+        rows = [r for r in rows if len(r) >= 9]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        num = lambda v: v.replace(".", "").isdigit()  # noqa: E731
+        sm = [float(r[1]) for r in rows if num(r[1])]
+        mx = [float(r[2]) for r in rows if num(r[2])]
+        pw = [float(r[3]) for r in rows if num(r[3])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+class Problem:
+    """Device buffers of one workload on one rank (inputs, map, workspaces, outputs)."""
+
+    def __init__(self, wl, rank, dev, stream):
+        import torch
+        from voxel_gemm_gb300 import ops, synth, shard
+        self.wl = wl
+        self.dev = dev
+        self.stream = stream
+        self.coords_np = shard.rank_coords(wl, rank)
+        N = self.N = self.coords_np.shape[0]
+        self.s = 4 if wl.dtype == "f32" else 2
+        dt = self.dt = synth.torch_dtype(wl.dtype)
+        with torch.cuda.stream(stream):
+            self.coords = torch.from_numpy(self.coords_np).to(dev)
+            self.f, self.W, self.b, self.dY = synth.make_tensors(wl, N, device=dev)
+            if rank > 0:  # every rank's batch element has its own features; weights are replicated
+                g = torch.Generator(device=dev)
+                g.manual_seed(7919 * rank + wl.seed)
+                self.f = torch.randn(N, wl.cin, generator=g, device=dev).to(dt)
+                self.dY = torch.randn(N, wl.cout, generator=g, device=dev).to(dt)
+            self.m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag, device=dev)
+            self.ws = [ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev) for _ in range(3)]
+            self.out = torch.empty(N, wl.cout, dtype=dt, device=dev)
+            self.dX = torch.empty(N, wl.cin, dtype=dt, device=dev)
+            self.dW = torch.empty(27, wl.cin, wl.cout, dtype=dt, device=dev)
+            self.db = torch.empty(wl.cout, dtype=dt, device=dev)
+        self.s_dx = torch.cuda.Stream(device=dev)
+        self.s_dw = torch.cuda.Stream(device=dev)
+
+
+def run_workload(args, wl, rank, world, dev, flush, full):
+    """Time K steps of workload `wl`; `full` adds the end-to-end and roofline records."""
     import torch
-    import torch.distributed as dist
-    from voxel_gemm_gb300 import ops, synth
+    from voxel_gemm_gb300 import ops, shard
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wl = synth.WORKLOADS[args.workload]
-    coords_np = synth.make_coords(wl)
-    N = coords_np.shape[0]
-    s = 4 if wl.dtype == "f32" else 2
-    dt = synth.torch_dtype(wl.dtype)
     stream = torch.cuda.Stream(device=dev)
-    with torch.cuda.stream(stream):
-        coords = torch.from_numpy(coords_np).to(dev)
-        f, W, b, dY = synth.make_tensors(wl, N, device=dev)
-        m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag, device=dev)
-        ws = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
-        out = torch.empty(N, wl.cout, dtype=dt, device=dev)
-        dX = torch.empty(N, wl.cin, dtype=dt, device=dev)
-        dW = torch.empty(27, wl.cin, wl.cout, dtype=dt, device=dev)
-        db = torch.empty(wl.cout, dtype=dt, device=dev)
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    # The three convolution passes depend only on the map and the inputs, so after
-    # the map build they run on three streams (each with its own conv workspace);
-    # a pass's tail then overlaps the next one's start.  --one-stream issues them
-    # one after the other on the timed stream instead.
+    pb = Problem(wl, rank, dev, stream)
+    m, N = pb.m, pb.N
     one_stream = args.one_stream
-    with torch.cuda.stream(stream):
-        ws_dx = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
-        ws_dw = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
-    s_dx = torch.cuda.Stream(device=dev)
-    s_dw = torch.cuda.Stream(device=dev)
+    reducer = shard.GradientSum(world, pb.dW, pb.db, dev) if world > 1 else None
 
     def step():
-        m.build(coords, stream)
+        m.build(pb.coords, stream)
         if one_stream:
-            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
-            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=stream)
-            return
-        s_dx.wait_stream(stream)
-        s_dw.wait_stream(stream)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws_dx, stream=s_dx)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws_dw, stream=s_dw)
-        stream.wait_stream(s_dx)
-        stream.wait_stream(s_dw)
+            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0], stream=stream)
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, pb.dX, pb.dW, pb.db, pb.ws[0],
+                                   stream=stream)
+        else:
+            # the three passes depend only on the map and the inputs: after the map build
+            # they run on three streams (each with its own conv workspace)
+            pb.s_dx.wait_stream(stream)
+            pb.s_dw.wait_stream(stream)
+            ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0], stream=stream)
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, pb.dX, None, None, pb.ws[1],
+                                   stream=pb.s_dx)
+            ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, None, pb.dW, pb.db, pb.ws[2],
+                                   stream=pb.s_dw)
+            stream.wait_stream(pb.s_dx)
+            stream.wait_stream(pb.s_dw)
+        if reducer is not None:  # data-parallel exchange: rank-ordered sum of dW and db
+            reducer(stream)
 
     def timed(fn, k, ev_list):
         for _ in range(k):
@@ -210,14 +279,18 @@ def run_ours(args, rank, world, local_rank):
             e1.record(stream)
             ev_list.append((e0, e1))
 
-    for _ in range(args.warmup):
+    warmup = args.warmup if full else 3
+    steps = args.steps if full else max(3, min(args.steps, 10))
+    for _ in range(warmup):
         step()
     stream.synchronize()
     assert m.status(stream) == ops.VG_OK
 
+    use_graph = not args.no_graph and world == 1  # collectives stay eager
+
     def graphed(fn):
         """Capture fn (stream-ordered C-ABI calls on `stream`) once; replay per step."""
-        if args.no_graph:
+        if not use_graph:
             return fn
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -229,44 +302,48 @@ def run_ours(args, rank, world, local_rank):
                 g.replay()
         return replay
 
-    eager_step = step
-    step = graphed(eager_step)
+    gstep = graphed(step)
     for _ in range(3):
-        step()
+        gstep()
     stream.synchronize()
-    P = int(torch.stack([(m.mask >> k) & 1 for k in range(27)]).sum().item())
+    P = count_pairs(m.mask.cpu().numpy().view("uint32"))
 
     # ---- timed region: exactly K steps
+    sampler = ClockSampler(dev.index) if full else None
+    if sampler:
+        sampler.start()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local_rank)
-    sampler.start()
+    if sampler:
+        sampler.begin_region()
     evs = []
     t_wall0 = time.perf_counter()
-    timed(step, args.steps, evs)
+    timed(gstep, steps, evs)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
-    clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b_) for a, b_ in evs]
-    tot_ms = max_over_ranks(sum(step_ms), world, dev)
-    assert m.status(stream) == ops.VG_OK and ops.vg_conv_status(ws, stream) == ops.VG_OK
-    if not one_stream:  # the other two workspaces are only used (and their error records set) then
-        assert ops.vg_conv_status(ws_dx, stream) == ops.VG_OK and ops.vg_conv_status(ws_dw, stream) == ops.VG_OK
-    ms_per_step = tot_ms / args.steps
+    clocks = sampler.stop() if sampler else None
+    tot_ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in evs), world, dev)
+    assert m.status(stream) == ops.VG_OK
+    for w_ in pb.ws:
+        assert ops.vg_conv_status(w_, stream) == ops.VG_OK
+    ms_per_step = tot_ms / steps
 
     # ---- per-pass timings (same stream, same flush rule), for the roofline
     phases = {}
-    kph = max(3, min(args.steps, 50))
+    kph = max(3, min(steps, 20))
     calls = {
-        "nbrmap": lambda: m.build(coords, stream),
-        "fwd": lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream),
-        "dgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws,
-                                                stream=stream),
-        "wgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws,
-                                                stream=stream),
+        "nbrmap": lambda: m.build(pb.coords, stream),
+        "fwd": lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0],
+                                              stream=stream),
+        "dgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, pb.dX, None, None,
+                                                pb.ws[0], stream=stream),
+        "wgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, None, pb.dW, pb.db,
+                                                pb.ws[0], stream=stream),
     }
     for name, fn in calls.items():
         ev = []
@@ -276,81 +353,12 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         phases[name] = sum(a.elapsed_time(b_) for a, b_ in ev) / kph
 
-    # ---- end to end through the public API with host buffers (pinned), copies inside the region
-    h_coords = torch.from_numpy(coords_np).pin_memory()
-    h_f, h_W, h_b, h_dY = (t.to("cpu").pin_memory() for t in (f, W, b, dY))
-    h_out = torch.empty(out.shape, dtype=dt).pin_memory()
-    h_dX = torch.empty(dX.shape, dtype=dt).pin_memory()
-    h_dW = torch.empty(dW.shape, dtype=dt).pin_memory()
-    h_db = torch.empty(db.shape, dtype=dt).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
-
-    # The copies run on two more streams (host-to-device and device-to-host) where
-    # the data dependences allow: features and weights go up while the neighbour
-    # map (which needs only the coordinates) is built, dY while the forward runs;
-    # `out` comes back during the backward and dX during the weight gradient.  The
-    # conv passes use the same streams as the device-only step.
-    up = torch.cuda.Stream(device=dev)
-    down = torch.cuda.Stream(device=dev)
-
-    def e2e_eager():
-        ev_fwd_in, ev_bwd_in, ev_fwd, ev_dx = (torch.cuda.Event() for _ in range(4))
-        with torch.cuda.stream(stream):
-            coords.copy_(h_coords, non_blocking=True)
-        up.wait_stream(stream)
-        down.wait_stream(stream)
-        with torch.cuda.stream(up):
-            f.copy_(h_f, non_blocking=True)
-            W.copy_(h_W, non_blocking=True)
-            b.copy_(h_b, non_blocking=True)
-            ev_fwd_in.record(up)
-            dY.copy_(h_dY, non_blocking=True)
-            ev_bwd_in.record(up)
-        m.build(coords, stream)
-        dx_stream = stream if one_stream else s_dx
-        dw_stream = stream if one_stream else s_dw
-        dx_ws = ws if one_stream else ws_dx
-        dw_ws = ws if one_stream else ws_dw
-        if not one_stream:
-            s_dx.wait_stream(stream)
-            s_dw.wait_stream(stream)
-        stream.wait_event(ev_fwd_in)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream)
-        ev_fwd.record(stream)
-        dx_stream.wait_event(ev_bwd_in)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, dx_ws, stream=dx_stream)
-        ev_dx.record(dx_stream)
-        with torch.cuda.stream(down):
-            down.wait_event(ev_fwd)
-            h_out.copy_(out, non_blocking=True)
-            down.wait_event(ev_dx)
-            h_dX.copy_(dX, non_blocking=True)
-        dw_stream.wait_event(ev_bwd_in)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, dw_ws, stream=dw_stream)
-        with torch.cuda.stream(dw_stream):
-            h_dW.copy_(dW, non_blocking=True)
-            h_db.copy_(db, non_blocking=True)
-        for st in (up, down) if one_stream else (up, down, s_dx, s_dw):
-            stream.wait_stream(st)
-
-    e2e_step = graphed(e2e_eager)
-
-    ke = max(3, min(args.steps, 100))
-    for _ in range(2):
-        e2e_step()
-    stream.synchronize()
-    ev = []
-    timed(e2e_step, ke, ev)
-    stream.synchronize()
-    e2e_ms = sum(a.elapsed_time(b_) for a, b_ in ev) / ke
-
-    # ---- roofline of the dominant kernel pass
+    # ---- roofline per pass and of the dominant pass
     peaks = load_peaks()
-    cplan = ops.vg_conv_describe(N, wl.cin, wl.cout, dt)
+    cplan = ops.vg_conv_describe(N, wl.cin, wl.cout, pb.dt)
     nplan = ops.vg_nbrmap_describe(N, *wl.grid, wl.key_flag)
     splits = cplan["splits"]
-    work = pass_work(N, P, wl.cin, wl.cout, s, splits)
+    work = pass_work(N, P, wl.cin, wl.cout, pb.s, splits)
     work["nbrmap"] = (0.0, float(nbrmap_bytes(N)))
     tc_peak = peaks["bf16_tflops"] * 1e12
     bw = peaks["hbm_gbs"] * 1e9
@@ -364,55 +372,168 @@ def run_ours(args, rank, world, local_rank):
                       "tflops": fl / t / 1e12, "gbs": by / t / 1e9,
                       "frac": (by / bw) / t if bound == "hbm" else (fl / tc_peak) / t}
         if name != "nbrmap":  # the same pass against the unique-byte roofline
-            ub = unique_bytes(N, wl.cin, wl.cout, s)
+            ub = unique_bytes(N, wl.cin, wl.cout, pb.s)
             rows[name]["unique_bytes"] = ub
             rows[name]["frac_unique_roofline"] = max(fl / tc_peak, ub / bw) / t
-    # dominant kernel: the slowest convolution pass (each pass is one GEMM kernel plus a
-    # small weight repack / reduce); the map build is a chain of small kernels, reported in "passes"
-    dom = max(("fwd", "dgrad", "wgrad"), key=lambda k: phases[k])
+    sk = splitk_bytes(wl.cin, wl.cout, splits)
+    rows["wgrad"]["splitk_bytes"] = sk
+    if rows["wgrad"]["bound"] == "hbm":  # the same pass without the library's own split-K traffic
+        rows["wgrad"]["frac_excl_splitk"] = ((work["wgrad"][1] - sk) / bw) / (phases["wgrad"] * 1e-3)
+    dom = max(("nbrmap", "fwd", "dgrad", "wgrad"), key=lambda k: phases[k])
+    t_roof = sum(max(fl / tc_peak, by / bw) for fl, by in work.values())
+    total_fl = sum(fl for fl, _ in work.values())
+    tflops = world * total_fl / (ms_per_step * 1e-3) / 1e12
+    rec = {"workload": wl.name, "N": N, "P": P, "ms_per_step": ms_per_step, "steps": steps,
+           "value": aggregate_voxels_per_s(N, world, ms_per_step), "unit": "voxels/s", "tflops": tflops,
+           "tflops_frac_of_bf16_peak": tflops / world / peaks["bf16_tflops"],
+           "roofline_step_frac": t_roof / (ms_per_step * 1e-3), "dominant_pass": dom,
+           "passes": rows}
+    if not full:
+        return rec
+
+    kern = {"nbrmap": "neighbour-map build (k_insert .. k_onesweep .. k_tile_rows)",
+            "wgrad": "k_wgrad_tc", "fwd": "k_gather_gemm_tc", "dgrad": "k_gather_gemm_tc"}[dom]
     d = rows[dom]
-    kern = "k_wgrad_tc" if dom == "wgrad" else "k_gather_gemm_tc"
     roof = {"kernel": f"{kern} ({dom} pass)", "bound": d["bound"],
             "achieved": d["gbs"] if d["bound"] == "hbm" else d["tflops"],
             "peak": peaks["hbm_gbs"] if d["bound"] == "hbm" else peaks["bf16_tflops"],
             "unit": "GB/s" if d["bound"] == "hbm" else "TFLOP/s",
-            "traffic": measured_traffic(wl.name, kern), "peak_source": peaks["source"] + " (burst)",
-            "duration": "CUDA events around the whole pass call (repack + GEMM + reduce), an upper bound"}
+            "traffic": measured_traffic(wl.name, kern, P) if dom != "nbrmap" else None,
+            "peak_source": peaks["source"] + " (burst)",
+            "duration": "CUDA events around the whole pass call (weight repack or split reduce included), "
+                        "an upper bound on the kernel's own time"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     if roof["bound"] == "tensor":  # the same rate against the sustained (power-capped) matmul figure
         roof["frac_vs_sustained"] = roof["achieved"] / peaks["bf16_tflops_sustained"]
-    t_roof = sum(max(fl / tc_peak, by / bw) for fl, by in work.values())
-    total_fl = sum(fl for fl, _ in work.values())
-    res = {
-        "metric": METRIC, "value": aggregate_voxels_per_s(N, world, ms_per_step), "unit": "voxels/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "res": wl.res, "N": N, "P": P, "cin": wl.cin,
-                   "cout": wl.cout, "step": "nbrmap build + fwd + dgrad + wgrad + dbias",
-                   "l2": "flushed between steps (256 MiB write, outside the per-step events)",
-                   "parallelism": f"replicas x{world}",
-                   "launch": ("eager" if args.no_graph else "CUDA graph replay of the step's C-ABI calls")
-                   + ("" if one_stream else "; fwd, dgrad and wgrad+db on three streams after the map build")},
-        "tflops": world * total_fl / (ms_per_step * 1e-3) / 1e12,
-        "roofline_step_frac": t_roof / (ms_per_step * 1e-3),
-        "roofline": roof,
-        "passes": rows,
+    if dom == "wgrad" and "frac_excl_splitk" in d:
+        roof["frac_excl_splitk"] = d["frac_excl_splitk"]
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the region
+    h_coords = torch.from_numpy(pb.coords_np).pin_memory()
+    h_f, h_W, h_b, h_dY = (t.to("cpu").pin_memory() for t in (pb.f, pb.W, pb.b, pb.dY))
+    h_out = torch.empty(pb.out.shape, dtype=pb.dt).pin_memory()
+    h_dX = torch.empty(pb.dX.shape, dtype=pb.dt).pin_memory()
+    h_dW = torch.empty(pb.dW.shape, dtype=pb.dt).pin_memory()
+    h_db = torch.empty(pb.db.shape, dtype=pb.dt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
+    # Copies run on two more streams where the data dependences allow: features and
+    # weights go up while the map (which needs only the coordinates) is built, dY while
+    # the forward runs; `out` comes back during the backward and dX during the weight
+    # gradient.  The conv passes use the same streams as the device-only step.
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+
+    def e2e_eager():
+        ev_fwd_in, ev_bwd_in, ev_fwd, ev_dx = (torch.cuda.Event() for _ in range(4))
+        with torch.cuda.stream(stream):
+            pb.coords.copy_(h_coords, non_blocking=True)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        with torch.cuda.stream(up):
+            pb.f.copy_(h_f, non_blocking=True)
+            pb.W.copy_(h_W, non_blocking=True)
+            pb.b.copy_(h_b, non_blocking=True)
+            ev_fwd_in.record(up)
+            pb.dY.copy_(h_dY, non_blocking=True)
+            ev_bwd_in.record(up)
+        m.build(pb.coords, stream)
+        dx_stream = stream if one_stream else pb.s_dx
+        dw_stream = stream if one_stream else pb.s_dw
+        dx_ws, dw_ws = (pb.ws[0], pb.ws[0]) if one_stream else (pb.ws[1], pb.ws[2])
+        if not one_stream:
+            pb.s_dx.wait_stream(stream)
+            pb.s_dw.wait_stream(stream)
+        stream.wait_event(ev_fwd_in)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0], stream=stream)
+        ev_fwd.record(stream)
+        dx_stream.wait_event(ev_bwd_in)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, pb.dX, None, None, dx_ws,
+                               stream=dx_stream)
+        ev_dx.record(dx_stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_fwd)
+            h_out.copy_(pb.out, non_blocking=True)
+            down.wait_event(ev_dx)
+            h_dX.copy_(pb.dX, non_blocking=True)
+        dw_stream.wait_event(ev_bwd_in)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, None, pb.dW, pb.db, dw_ws,
+                               stream=dw_stream)
+        for st in (up, down) if one_stream else (up, down, pb.s_dx, pb.s_dw):
+            stream.wait_stream(st)
+        if reducer is not None:
+            reducer(stream)
+        with torch.cuda.stream(stream):
+            h_dW.copy_(pb.dW, non_blocking=True)
+            h_db.copy_(pb.db, non_blocking=True)
+
+    e2e_step = graphed(e2e_eager)
+    ke = max(3, min(args.steps, 100))
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    ev = []
+    timed(e2e_step, ke, ev)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev) / ke, world, dev)
+
+    nb_launch = nplan["launches"] + cplan["launches_fwd"] + cplan["launches_bwd"]
+    rec.update({
+        "roofline": roof, "clocks": clocks, "wall_s_timed_region": t_wall,
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "voxels/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (nplan["launches"] + cplan["launches_fwd"] + cplan["launches_bwd"]),
+        "gpu_launches": steps * (nb_launch + (reducer.launches if reducer else 0)),
         "gpu_launches_per_step": {"nbrmap": nplan["launches"], "fwd": cplan["launches_fwd"],
-                                  "bwd": cplan["launches_bwd"]},
+                                  "bwd": cplan["launches_bwd"],
+                                  "gradient_sum": reducer.launches if reducer else 0},
         "path": {"tensor_core": bool(cplan["tensor_core"]), "wgrad_splits": splits,
                  "hash_keys": 64 if nplan["key64"] else 32, "sort_passes": nplan["sort_passes"]},
-        "clocks": clocks,
-        "wall_s_timed_region": t_wall,
+        "launch": ("eager" if not use_graph else "CUDA graph replay of the step's C-ABI calls")
+                  + ("" if one_stream else "; fwd, dgrad and wgrad+db on three streams after the map build"),
+    })
+    return rec
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from voxel_gemm_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    wl = synth.WORKLOADS[args.workload]
+    head = run_workload(args, wl, rank, world, dev, flush, full=True)
+    torch.cuda.empty_cache()
+    sweep = []
+    if not args.no_sweep:
+        for name in SWEEP:
+            if name == wl.name:
+                continue
+            try:
+                sweep.append(run_workload(args, synth.WORKLOADS[name], rank, world, dev, flush, full=False))
+            except Exception as e:  # noqa: BLE001 - a failed sub-record must not hide the headline
+                sweep.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
+            torch.cuda.empty_cache()
+
+    res = {
+        "metric": METRIC, "value": head["value"], "unit": "voxels/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic (seeded voxelised sphere/torus surfaces)",
+        "config": workload_config(wl, head["N"], head["P"], world),
+        "tflops": head["tflops"], "tflops_frac_of_bf16_peak": head["tflops_frac_of_bf16_peak"],
+        "roofline_step_frac": head["roofline_step_frac"],
+        "roofline": head["roofline"], "passes": head["passes"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"], "gpu_launches_per_step": head["gpu_launches_per_step"],
+        "path": head["path"], "launch": head["launch"], "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
+        "sweep": sweep,
     }
     return res
 
 
 # ------------------------------------------------------------------ oracle arm (CPU)
-def oracle_sample(wl, coords_np, budget_rows, seed=0, min_seconds=5.0):
+def oracle_sample(wl, coords_np, budget_rows, seed=0, min_seconds=5.0, nbrmap=None):
     """Time the oracle on a bounded sample of the workload: the full neighbour map
     (scaled per voxel) and fwd + dgrad + wgrad over sampled rows, repeated over
     fresh row samples until at least `min_seconds` of conv work has run."""
@@ -444,74 +565,83 @@ def oracle_sample(wl, coords_np, budget_rows, seed=0, min_seconds=5.0):
         t_conv += time.perf_counter() - t1
         rows_done += R
     per_voxel = t_map / N + t_conv / rows_done
+    if nbrmap is not None:
+        nbrmap.append(mask)
     return 1.0 / per_voxel, {"rows": rows_done, "t_map_s": t_map, "t_conv_s": t_conv}
 
 
-def run_reference(args):
-    from voxel_gemm_gb300 import synth
+def run_reference(args, world):
+    from voxel_gemm_gb300 import shard, synth
     import oracle
     wl = synth.WORKLOADS[args.workload]
-    coords_np = synth.make_coords(wl)
+    coords_np = shard.rank_coords(wl, 0)
     budget = rows_budget(wl)
+    masks = []
     for _ in range(args.warmup):
-        oracle_sample(wl, coords_np, max(64, budget // 8), min_seconds=0.0)
+        oracle_sample(wl, coords_np, max(64, budget // 8), min_seconds=0.0, nbrmap=masks)
     vals = []
     t0 = time.perf_counter()
     for k in range(args.steps):
-        v, _ = oracle_sample(wl, coords_np, budget, seed=k, min_seconds=2.0)
+        v, _ = oracle_sample(wl, coords_np, budget, seed=k, min_seconds=1.0, nbrmap=masks)
         vals.append(v)
     wall = time.perf_counter() - t0
     value = statistics.median(vals)
     cores = oracle.num_threads()
-    sample = (f"full neighbour map of N={coords_np.shape[0]} voxels, then fwd+dgrad+wgrad over "
-              f"{min(budget, coords_np.shape[0])} seeded sampled rows per step; voxels/s = 1 / (map time per "
+    N = int(coords_np.shape[0])
+    P = count_pairs(masks[-1]) if masks else None
+    sample = (f"full neighbour map of N={N} voxels, then fwd+dgrad+wgrad over "
+              f"{min(budget, N)} seeded sampled rows per step; voxels/s = 1 / (map time per "
               f"voxel + conv time per sampled row)")
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": 1,
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "voxels/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "res": wl.res, "N": int(coords_np.shape[0]),
-                       "cin": wl.cin, "cout": wl.cout},
+            "data": "synthetic (seeded voxelised sphere/torus surfaces)",
+            "config": workload_config(wl, N, P, world),
             "cpu_baseline": {"value": value, "unit": "voxels/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "voxels/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def rows_budget(wl):
-    # about 2-4 s of fp64 work per sample on a many-core host
+    # about 1-2 s of fp64 work per sample on a many-core host
     per_row = 3 * 10.6 * wl.cin * wl.cout
-    return int(max(256, min(65536, 4e9 / per_row)))
+    return int(max(256, min(65536, 2e9 / per_row)))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-graph", action="store_true", help="launch each call eagerly instead of replaying a CUDA graph")
     ap.add_argument("--one-stream", action="store_true",
                     help="issue the step's conv passes one after the other on one stream")
     args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_reference(args, world)), flush=True)
         return
     if world > 1:
+        import torch
         import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            from voxel_gemm_gb300 import synth
+            from voxel_gemm_gb300 import shard, synth
             import oracle
             wl = synth.WORKLOADS[args.workload]
-            coords_np = synth.make_coords(wl)
+            coords_np = shard.rank_coords(wl, 0)
             v, info = oracle_sample(wl, coords_np, rows_budget(wl))
             res["cpu_baseline"] = {"value": v, "unit": "voxels/s", "cores": oracle.num_threads(),
                                    "kind": "oracle",

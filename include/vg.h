@@ -73,6 +73,13 @@ extern "C" {
 /* Testing aid: size the hash table below N so that the overflow path
  * (VG_ERR_HASH_FULL) can be exercised from the host. */
 #define VG_TEST_SMALL_HASH  0x100u
+/* Convolution flag: fp32 features may run on the tensor cores as TF32 (inputs
+ * read with a 10-bit mantissa, products accumulated in fp32), as the pages'
+ * allow_tf32 switch does ("From CUDA to Triton: Triton JIT and autotuning",
+ * §六 6.2: allow_tf32 is part of the autotune key and of the kernel arguments).
+ * Applies to fp32 with Cin and Cout multiples of 32; otherwise, and without the
+ * flag, fp32 runs on the exact FFMA path. */
+#define VG_ALLOW_TF32       0x10u
 
 #define VG_NONE 0xFFFFFFFFu        /* missing neighbour in nbr                          */
 #define VG_TILE_ROWS 128           /* rows per tile of the sorted order (tile masks)    */
@@ -137,11 +144,15 @@ VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);
  *                neighbour lists are one contiguous 13.5 KB block). */
 VG_API const uint32_t* vg_nbrmap_sorted_nbr(const void* ws, int64_t N);
 
-/* Host-only description of the build plan (no device access):
+/* Host-only description of the build plan (no device work):
  *   info[0] = 1 if the hash keys are 64-bit, info[1] = significant bits of the
  *   sort key above, info[2] = radix-sort passes, info[3] = kernels launched by
- *   vg_nbrmap_build (memsets not counted).  Returns VG_OK or VG_ERR_INVALID_ARG. */
-VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int info[4]);
+ *   vg_nbrmap_build (memsets not counted).
+ *   sm_count: SMs of the device the plan is for; 0 = the current device's (the
+ *   launch grids and the workspace size follow the SM count; without any CUDA
+ *   device, 0 plans for 152 SMs).  Returns VG_OK or VG_ERR_INVALID_ARG. */
+VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sm_count,
+                              int info[4]);
 
 /* ======================================================================================
  * Convolution (forward, input gradient, weight/bias gradient)
@@ -150,10 +161,12 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
  * contraction V * Ci) and its backward ("Contribution Tasks — JeffreyXiang/FlexGEMM",
  * §二 call flow: the backward reuses the neighbour cache and returns feats.grad
  * and weight.grad).
- *   dtype: VG_F32 (fp32 FFMA path), VG_F16 or VG_BF16 (tensor-core path when
- *          Cin and Cout are multiples of 64, CUDA-core path otherwise).
+ *   dtype: VG_F32 (fp32 FFMA path; with VG_ALLOW_TF32 and Cin, Cout multiples
+ *          of 32 the forward and the input gradient run on the tensor cores as
+ *          TF32), VG_F16 or VG_BF16 (tensor-core path when Cin and Cout are
+ *          multiples of 64, CUDA-core path otherwise).
  *   Cin and Cout must be multiples of 8 (VG_ERR_UNSUPPORTED otherwise); flags
- *   must be 0.
+ *   is 0 or VG_ALLOW_TF32 (other bits: VG_ERR_UNSUPPORTED).
  *   feats [N][Cin], weight [27][Cin][Cout], bias [Cout] (or NULL), out [N][Cout],
  *   all of `dtype`, 16-byte aligned.
  *   nbr_ws/nbr/mask: a map built by vg_nbrmap_build for the same N.
@@ -167,13 +180,17 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
 /* Bytes of conv workspace needed by vg_subm_conv3d_fwd/bwd for these sizes. */
 VG_API size_t vg_conv_workspace_bytes(int64_t N, int Cin, int Cout, int dtype, unsigned flags);
 
-/* Host-only description of the convolution plan (no device access):
- *   info[0] = 1 on the tensor-core path, info[1] = split-K chunks of the weight
+/* Host-only description of the convolution plan (no device work):
+ *   info[0] = 1 on the 16-bit tensor-core path, 2 when the fp32 forward and input
+ *   gradient run on the tensor cores as TF32, else 0, info[1] = split-K chunks of the weight
  *   gradient, info[2] = kernels launched by a forward call, info[3] = kernels
  *   launched by a backward call producing all three gradients (memsets not
- *   counted).  Returns VG_OK or the status vg_subm_conv3d_fwd would return
- *   for these sizes. */
-VG_API int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int info[4]);
+ *   counted).  sm_count as in vg_nbrmap_describe (the split-K chunk count and
+ *   the workspace size follow it; vg_conv_workspace_bytes and the conv calls
+ *   use the current device's).  Returns VG_OK or the status vg_subm_conv3d_fwd
+ *   would return for these sizes. */
+VG_API int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int sm_count,
+                            int info[4]);
 
 VG_API int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask, int64_t N,
                        int dtype, const void* feats, const void* weight, const void* bias,
@@ -198,16 +215,37 @@ VG_API int vg_conv_status(void* conv_ws, void* stream);
 
 
 /* ======================================================================================
+ * Data-parallel gradient exchange
+ * The pages describe a single-GPU operator library and have no multi-GPU step.
+ * When several processes each run the convolution on their own batch elements
+ * with replicated weights, their weight and bias gradients must be summed; this
+ * call is the arithmetic of that exchange, done in a fixed order so that every
+ * process ends with the same bits run after run.  Moving the gradients between
+ * processes (an all-gather) is the caller's.
+ * ====================================================================================== */
+
+/* out[i] = round(parts[0][i] + parts[1][i] + ... + parts[nparts-1][i]) with the
+ * additions done in fp32 in index order (left to right) and one round-to-nearest-
+ * even to `dtype` at the end.  parts: [nparts][count] contiguous, out: [count],
+ * both of `dtype` and aligned to its size; out may not overlap parts.
+ * Asynchronous on `stream`; VG_ERR_INVALID_ARG for nparts <= 0, count < 0, an
+ * unknown dtype, or null/misaligned pointers. */
+VG_API int vg_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, void* out, void* stream);
+
+/* ======================================================================================
  * Forward pass without a caller-provided workspace.
  * The paper has no counterpart to this call.  It is for callers that cannot
  * allocate device memory: code running inside a stream capture (a cudaMalloc there
  * is not part of the graph and can break the capture), plug-ins hosted by a runtime
  * that owns all device memory and forbids allocation after start-up, and hot paths
  * that cannot afford the device-wide synchronisation of cudaMalloc/cudaFree.
- * Arguments and result are those of vg_subm_conv3d_fwd without conv_ws: the scratch
+ * Arguments and output are those of vg_subm_conv3d_fwd without conv_ws: the scratch
  * (repacked weight tiles and the error word) is a fixed __device__ array of
  * 8 MiB + 256 B inside the library, which every GPU that loads the library holds
- * until the process exits.
+ * until the process exits.  The call runs the same kernels as vg_subm_conv3d_fwd,
+ * so the output is bit-identical to it.  A kernel that gives up a bounded wait
+ * is reported by vg_subm_conv3d_fwd_noalloc_status(), not by this call's
+ * return value (which covers argument and launch errors only).
  *  - Returns VG_ERR_WORKSPACE_TOO_SMALL when the repacked weights (27*Cin*Cout*2
  *    bytes on the tensor-core path: 16-bit dtype, Cin and Cout multiples of 64)
  *    exceed 8 MiB, e.g. Cin = Cout = 512.
@@ -221,6 +259,16 @@ VG_API int vg_subm_conv3d_fwd_noalloc(const void* nbr_ws, const uint32_t* nbr, c
                                       int64_t N, int dtype, const void* feats, const void* weight,
                                       const void* bias, void* out, int Cin, int Cout, unsigned flags,
                                       void* stream);
+
+/* Device-side status of the most recent vg_subm_conv3d_fwd_noalloc call on the
+ * current device.  The paper has no counterpart to this call either: it reads
+ * the error word that the no-allocation forward keeps in its fixed array, so a
+ * caller without a conv workspace can still learn that a kernel gave up a
+ * bounded wait.  Synchronises `stream` (the stream of that call), then reads and
+ * clears the word.  Returns VG_ERR_DEVICE_TIMEOUT if a kernel of that call gave
+ * up (its output is then incomplete), VG_OK otherwise, VG_ERR_CUDA if the array's
+ * address cannot be looked up or the copy fails.  Allocates nothing. */
+VG_API int vg_subm_conv3d_fwd_noalloc_status(void* stream);
 
 #ifdef __cplusplus
 }

@@ -68,13 +68,14 @@ def test_host_only_queries(ops):
     assert (d32["key64"], d64["key64"]) == (0, 1) and d32["sort_passes"] == d64["sort_passes"]
 
 
-def test_split_k_plan(ops):
+@pytest.mark.parametrize("sms", [152, 148, 76])
+def test_split_k_plan(ops, sms):
     """Split-K chunks of the tensor-core weight gradient: about four work units per SM,
     at most 256 tiles per chunk, at least 4 tiles per chunk when there are enough,
     and fp32 partial sums of at most 1 GiB."""
     for N, C in [(25179, 64), (319057, 128), (602492, 256), (602492, 512), (602492, 1024),
                  (4915386, 64), (1000, 64), (128, 256)]:
-        d = ops.vg_conv_describe(N, C, C, ops.VG_BF16)
+        d = ops.vg_conv_describe(N, C, C, ops.VG_BF16, sm_count=sms)
         assert d["tensor_core"] == 1
         S, T = d["splits"], (N + 127) // 128
         tpc = (T + S - 1) // S  # tiles per chunk
@@ -111,3 +112,21 @@ def test_argument_errors_return_before_any_launch(ops):
     assert st == ops.VG_ERR_WORKSPACE_TOO_SMALL
     assert L.vg_conv_status(None, None) == ops.VG_ERR_INVALID_ARG
     assert L.vg_nbrmap_status(None, None) == ops.VG_ERR_INVALID_ARG
+
+
+def test_plans_follow_the_sm_count(ops):
+    """The split-K chunk count and the sort grid follow the device's SM count (passed
+    explicitly here; 0 means the current device's)."""
+    # 319k voxels, C = 128: 14 (M group, N block) units per chunk, about 4 units per SM
+    s152 = ops.vg_conv_describe(319057, 128, 128, ops.VG_BF16, sm_count=152)["splits"]
+    s76 = ops.vg_conv_describe(319057, 128, 128, ops.VG_BF16, sm_count=76)["splits"]
+    assert s152 * 14 >= 4 * 152 and s76 * 14 >= 4 * 76 and s76 < s152, (s76, s152)
+    with pytest.raises(ops.VGError):
+        ops.vg_conv_describe(1000, 64, 64, ops.VG_BF16, sm_count=-1)
+    with pytest.raises(ops.VGError):
+        ops.vg_nbrmap_describe(1000, 1, 8, 8, 8, sm_count=-1)
+    # without a device, 0 plans for the default count
+    import torch
+    if not torch.cuda.is_available():
+        assert (ops.vg_conv_describe(319057, 128, 128, ops.VG_BF16)["splits"] == s152)
+

@@ -1,8 +1,8 @@
 """GPU forward / input gradient / weight and bias gradient vs the oracle.
 
 Small workloads are compared element by element in full; the large ones on
-seeded samples the oracle computes one by one (output rows x a column subset
-for fwd and dgrad, full-sum dW entries over ci x co column subsets), in the
+seeded samples the oracle computes one by one (4096 output rows x up to 64
+columns for fwd and dgrad, 27 x 16 x 16 full-sum dW entries, all of db), in the
 same launch configuration the benchmark times.  Bound: relative Frobenius
 error <= 1e-5 (fp32, FFMA) and <= 1e-2 (fp16/bf16 with fp32 accumulation).
 """
@@ -18,7 +18,7 @@ from voxel_gemm_gb300 import ops, synth
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(coords_np, grid, f, W, b, dY, key_flag=0, want=("out", "dX", "dW", "db")):
+def run_gpu(coords_np, grid, f, W, b, dY, key_flag=0, flags=0):
     dev = "cuda"
     c = torch.from_numpy(coords_np).to(dev)
     N = coords_np.shape[0]
@@ -26,23 +26,23 @@ def run_gpu(coords_np, grid, f, W, b, dY, key_flag=0, want=("out", "dX", "dW", "
     fd, Wd, dYd = f.to(dev), W.to(dev), dY.to(dev)
     bd = None if b is None else b.to(dev)
     Cin, Cout = W.shape[1], W.shape[2]
-    ws = ops.conv_workspace(N, Cin, Cout, f.dtype)
+    ws = ops.conv_workspace(N, Cin, Cout, f.dtype, flags=flags)
     res = {}
     out = torch.empty(N, Cout, dtype=f.dtype, device=dev)
-    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, fd, Wd, bd, out, ws)
+    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, fd, Wd, bd, out, ws, flags=flags)
     dX = torch.empty(N, Cin, dtype=f.dtype, device=dev)
     dW = torch.empty(27, Cin, Cout, dtype=f.dtype, device=dev)
     db = torch.empty(Cout, dtype=f.dtype, device=dev)
-    ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dYd, fd, Wd, dX, dW, db, ws)
+    ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dYd, fd, Wd, dX, dW, db, ws, flags=flags)
     assert m.status() == ops.VG_OK
     assert ops.vg_conv_status(ws) == ops.VG_OK
     res.update(out=out.cpu(), dX=dX.cpu(), dW=dW.cpu(), db=db.cpu(), nbr=u32(m.nbr))
     return res
 
 
-def full_check(coords, grid, f, W, b, dY, tol, key_flag=0):
+def full_check(coords, grid, f, W, b, dY, tol, key_flag=0, flags=0):
     nbr_ref, _ = oracle.nbrmap(coords, *grid)
-    r = run_gpu(coords, grid, f, W, b, dY, key_flag)
+    r = run_gpu(coords, grid, f, W, b, dY, key_flag, flags)
     assert np.array_equal(r["nbr"], nbr_ref)
     out_ref = oracle.fwd(nbr_ref, f64(f), f64(W), None if b is None else f64(b))
     dX_ref = oracle.dgrad_scatter(nbr_ref, f64(dY), f64(W))
@@ -84,11 +84,14 @@ def test_workload_sampled(name):
     e_out = rel_fro(f64(r["out"][rows][:, cols_out]), out_ref)
     dX_ref = oracle_dgrad_rows(nbr_ref, rows, cols_in, dY, W)
     e_dx = rel_fro(f64(r["dX"][rows][:, cols_in]), dX_ref)
-    ci = np.sort(rng.choice(wl.cin, size=8, replace=False))
-    co = np.sort(rng.choice(wl.cout, size=8, replace=False))
-    dW_ref, db_ref = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
+    # 27 taps x 16 x 16 = 6912 seeded full-sum dW entries (each a sum over every valid
+    # pair of its tap), and every db entry
+    ci = np.sort(rng.choice(wl.cin, size=16, replace=False))
+    co = np.sort(rng.choice(wl.cout, size=16, replace=False))
+    dW_ref, _ = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
     e_dw = rel_fro(f64(r["dW"][:, ci][:, :, co]), dW_ref)
-    e_db = rel_fro(f64(r["db"][co]), db_ref)
+    _, db_ref = oracle_wgrad_cols(nbr_ref, f[:, :1], dY, np.arange(1), np.arange(wl.cout))
+    e_db = rel_fro(f64(r["db"]), db_ref)
     tol = TOL[wl.dtype]
     assert max(e_out, e_dx, e_dw, e_db) <= tol, (e_out, e_dx, e_dw, e_db)
 
@@ -246,3 +249,44 @@ def test_anisotropic_grid(dtype, cin, cout):
     wl = synth.Workload("t", 3, 13, 0, ("sphere",), cin, cout, dtype, 11, 2.0)
     f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
     full_check(coords, grid, f, W, b, dY, TOL[dtype])
+
+
+# ---------------------------------------------------------------- TF32 (VG_ALLOW_TF32)
+TF32_TOL = 5e-3
+
+
+def test_tf32_sphere_workload():
+    # the fp32 16^3 sphere (Cin = Cout = 32): forward and input gradient on the tensor
+    # cores as TF32, within the TF32 bound of the oracle
+    wl = synth.WORKLOADS["sphere16_c32_f32"]
+    coords = coords_of(wl.name)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    assert ops.vg_conv_describe(coords.shape[0], 32, 32, torch.float32, ops.VG_ALLOW_TF32)["tensor_core"] == 2
+    errs = full_check(coords, wl.grid, f, W, b, dY, TF32_TOL, flags=ops.VG_ALLOW_TF32)
+    assert errs["out"] > 1e-5  # the TF32 path really ran (the FFMA path is ~3e-7 on this case)
+
+
+@pytest.mark.parametrize("cin,cout", [(32, 32), (64, 64), (64, 128), (128, 64), (192, 64), (32, 96), (256, 256)])
+def test_tf32_ragged_and_shapes(cin, cout):
+    coords = synth.random_coords(cin * 5 + cout, 1111, 2, 14, 14, 14)
+    wl = synth.Workload("t", 2, 14, 0, ("sphere",), cin, cout, "f32", 13, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    full_check(coords, (2, 14, 14, 14), f, W, b, dY, TF32_TOL, flags=ops.VG_ALLOW_TF32)
+
+
+def test_tf32_anisotropic_grid():
+    grid = (3, 5, 9, 13)
+    coords = synth.random_coords(78, 700, *grid)
+    wl = synth.Workload("t", 3, 13, 0, ("sphere",), 32, 64, "f32", 12, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    full_check(coords, grid, f, W, b, dY, TF32_TOL, flags=ops.VG_ALLOW_TF32)
+
+
+def test_tf32_flag_falls_back_to_ffma_for_other_channels():
+    # channels that are not multiples of 32 keep the exact FFMA path under the flag
+    coords = synth.random_coords(3, 500, 1, 12, 12, 12)
+    wl = synth.Workload("t", 1, 12, 0, ("sphere",), 24, 40, "f32", 14, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, coords.shape[0])
+    assert ops.vg_conv_describe(coords.shape[0], 24, 40, torch.float32, ops.VG_ALLOW_TF32)["tensor_core"] == 0
+    full_check(coords, (1, 12, 12, 12), f, W, b, dY, TOL["f32"], flags=ops.VG_ALLOW_TF32)
+

@@ -95,7 +95,7 @@ def _dense_fwd_bwd(coords, grid, f, W, b, dY):
     """Dense conv3d(padding=1) on the densified grid, read at the active sites, and its autograd."""
     x = _densify(coords, grid, f).requires_grad_(True)
     w = _dense_torch_w(W).clone().requires_grad_(True)
-    bias = torch.from_numpy(b)
+    bias = torch.from_numpy(b).clone().requires_grad_(True)
     out = torch.nn.functional.conv3d(x, w, bias, padding=1)
     c = torch.from_numpy(coords.astype(np.int64))
     out_sites = out[c[:, 0], :, c[:, 1], c[:, 2], c[:, 3]]
@@ -104,7 +104,7 @@ def _dense_fwd_bwd(coords, grid, f, W, b, dY):
     dX = _read_sites(x.grad, coords)
     cout, cin = w.shape[0], w.shape[1]
     dW = w.grad.reshape(cout, cin, 27).permute(2, 1, 0).numpy()
-    return out_sites.detach().numpy(), dX, dW
+    return out_sites.detach().numpy(), dX, dW, bias.grad.numpy()
 
 
 def _rel(a, b):
@@ -212,7 +212,7 @@ def test_fwd_equals_dense_conv3d(case):
     coords, grid, f, W, b, dY = CASES[case]()
     nbr, _ = oracle.nbrmap(coords, *grid)
     out = oracle.fwd(nbr, f, W, b)
-    ref, _, _ = _dense_fwd_bwd(coords, grid, f, W, b, dY)
+    ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)[0]
     assert _rel(out, ref) < 1e-12
 
 
@@ -264,12 +264,14 @@ def test_permutation_equivariance():
 def test_bwd_equals_dense_autograd(case):
     coords, grid, f, W, b, dY = CASES[case]()
     nbr, _ = oracle.nbrmap(coords, *grid)
-    _, dX_ref, dW_ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)
+    _, dX_ref, dW_ref, db_ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)
     assert _rel(oracle.dgrad_scatter(nbr, dY, W), dX_ref) < 1e-12
     assert _rel(oracle.dgrad_rows(nbr, dY, W), dX_ref) < 1e-12
     dW, db = oracle.wgrad(nbr, f, dY)
     assert _rel(dW, dW_ref) < 1e-12
-    assert _rel(db, dY.sum(axis=0)) < 1e-13
+    # grad_bias from the dense convolution's own autograd (torch's bias gradient of
+    # conv3d reduces over the whole grid; only active sites carry a non-zero dY)
+    assert _rel(db, db_ref) < 1e-12
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -308,7 +310,7 @@ def test_wgrad_finite_differences():
 def test_planted_flipped_taps_is_caught():
     coords, grid, f, W, b, dY = _small_case(seed=21)
     nbr, _ = oracle.nbrmap(coords, *grid)
-    ref, _, _ = _dense_fwd_bwd(coords, grid, f, W, b, dY)
+    ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)[0]
     wrong = oracle.fwd(nbr, f, W[::-1].copy(), b)       # taps in reverse order (o_k -> -o_k)
     assert _rel(wrong, ref) > 1e-2
 
@@ -316,7 +318,7 @@ def test_planted_flipped_taps_is_caught():
 def test_planted_transposed_weight_is_caught():
     coords, grid, f, W, b, dY = _small_case(seed=22, cin=4, cout=4)
     nbr, _ = oracle.nbrmap(coords, *grid)
-    ref, dX_ref, _ = _dense_fwd_bwd(coords, grid, f, W, b, dY)
+    ref, dX_ref, _, _ = _dense_fwd_bwd(coords, grid, f, W, b, dY)
     assert _rel(oracle.fwd(nbr, f, W.transpose(0, 2, 1).copy(), b), ref) > 1e-2
     assert _rel(oracle.dgrad_rows(nbr, dY, W.transpose(0, 2, 1).copy()), dX_ref) > 1e-2
 
@@ -331,5 +333,20 @@ def test_planted_wrong_offset_sign_is_caught():
 def test_planted_dropped_bias_is_caught():
     coords, grid, f, W, b, dY = _small_case(seed=24)
     nbr, _ = oracle.nbrmap(coords, *grid)
-    ref, _, _ = _dense_fwd_bwd(coords, grid, f, W, b, dY)
+    ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)[0]
     assert _rel(oracle.fwd(nbr, f, W, None), ref) > 1e-3
+
+
+def test_planted_masked_bias_gradient_is_caught():
+    # a grad_bias that sums dY only over rows with some neighbour besides the centre
+    # (a plausible slip when db is folded into the per-tap weight-gradient loop)
+    coords, grid, f, W, b, dY = _small_case(seed=25, n=60)
+    nbr, mask = oracle.nbrmap(coords, *grid)
+    db_ref = _dense_fwd_bwd(coords, grid, f, W, b, dY)[3]
+    lonely = mask == (1 << 13)
+    assert lonely.any()
+    wrong = dY[~lonely].sum(axis=0)
+    assert _rel(wrong, db_ref) > 1e-3
+    _, db = oracle.wgrad(nbr, f, dY)
+    assert _rel(db, db_ref) < 1e-12
+

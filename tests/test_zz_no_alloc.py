@@ -1,11 +1,13 @@
-"""vg_subm_conv3d_fwd_noalloc against vg_subm_conv3d_fwd (GPU).
+"""vg_subm_conv3d_fwd_noalloc against vg_subm_conv3d_fwd and the oracle (GPU).
 
 The no-allocation forward serves callers that cannot allocate device memory
-(inside a stream capture, under a runtime that owns all device memory, or on
-paths that cannot pay for cudaMalloc's synchronisation): its scratch is a fixed
-array inside the library instead of a caller workspace.  Its output must match
-the workspace-based forward, and a second call must not see stale state from
-the first, because every call shares that array.  This file is collected last.
+(code inside a stream capture, plug-ins under a runtime that owns all device
+memory, paths that cannot pay for cudaMalloc's synchronisation): its scratch
+is a fixed array inside the library instead of a caller workspace.  It runs the
+same kernels as the workspace forward, so its output must be bit-identical to
+it; a second call must not see stale state from the first, because every call
+shares that array; and its device-side status word must read back VG_OK.
+This file is collected last.
 """
 import ctypes
 
@@ -13,7 +15,8 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import TOL, f64, rel_fro
+import oracle
+from helpers import TOL, f64, rel_fro, u32
 from voxel_gemm_gb300 import ops, synth
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +27,7 @@ def _case(seed, cin, cout, dtype, n=3000):
     wl = synth.Workload("noalloc", 2, 20, 0, ("sphere",), cin, cout, dtype, seed, 2.0)
     f, W, b, _ = synth.make_tensors(wl, coords.shape[0])
     m = ops.NbrMap.alloc(coords.shape[0], (2, 20, 20, 20)).build(torch.from_numpy(coords).cuda())
-    return m, f.cuda(), W.cuda(), b.cuda()
+    return coords, m, f.cuda(), W.cuda(), b.cuda()
 
 
 def _noalloc_raw(m, f, W, b, out):
@@ -38,23 +41,33 @@ def _noalloc_raw(m, f, W, b, out):
                                         cin, cout, 0, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
+def _noalloc_status():
+    L = ops.lib()
+    return L.vg_subm_conv3d_fwd_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 @pytest.mark.parametrize("cin,cout,dtype", [(64, 64, "f16"), (128, 64, "bf16"), (32, 32, "f32")])
 def test_noalloc_matches_fwd_on_two_calls(cin, cout, dtype):
     for seed in (1, 2):  # two calls in a row, different inputs
-        m, f, W, b = _case(seed * 31 + cin, cin, cout, dtype)
+        coords, m, f, W, b = _case(seed * 31 + cin, cin, cout, dtype)
         ref = torch.empty(f.shape[0], cout, dtype=f.dtype, device="cuda")
         ws = ops.conv_workspace(f.shape[0], cin, cout, f.dtype)
         ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, ref, ws)
         out = torch.full_like(ref, float("nan"))
         assert _noalloc_raw(m, f, W, b, out) == ops.VG_OK
-        torch.cuda.synchronize()
-        assert m.status() == ops.VG_OK
-        err = rel_fro(f64(out), f64(ref))
+        assert _noalloc_status() == ops.VG_OK
+        assert m.status() == ops.VG_OK and ops.vg_conv_status(ws) == ops.VG_OK
+        # the same kernels on the same inputs: identical bits
+        assert torch.equal(out.view(torch.uint8), ref.view(torch.uint8))
+        # and against the oracle directly, within the dtype's bound
+        nbr_ref, _ = oracle.nbrmap(coords, 2, 20, 20, 20)
+        assert np.array_equal(u32(m.nbr), nbr_ref)
+        err = rel_fro(f64(out), oracle.fwd(nbr_ref, f64(f), f64(W), f64(b)))
         assert err <= TOL[dtype], err
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    m, f, W, b = _case(5, 64, 64, "bf16", n=200)
+    _, m, f, W, b = _case(5, 64, 64, "bf16", n=200)
     W_big = torch.zeros(27, 512, 512, dtype=torch.bfloat16, device="cuda")  # 14 MiB of packed weights
     f_big = torch.zeros(f.shape[0], 512, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(f.shape[0], 512, dtype=torch.bfloat16, device="cuda")

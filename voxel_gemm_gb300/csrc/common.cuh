@@ -51,6 +51,7 @@ struct NbrLayout {
     size_t off_skeys_a = 0, off_skeys_b = 0, off_svals_b = 0, off_hist = 0, off_nbr_sorted = 0, total = 0;
     size_t off_status = 0, off_tickets = 0;
     size_t off_torder = 0, off_tkey_a = 0, off_tkey_b = 0, off_torder_b = 0;  // tile region sort
+    int sms = 0;             // SM count the sort grid is sized for
     int tile_passes = 1;     // radix passes of the tile region sort
     int64_t tile_blocks = 1; // blocks of one tile-sort pass
 };

@@ -202,9 +202,9 @@ __global__ void k_reduce_splits(const float* __restrict__ partial, int splits, i
 // db partial sums: block b sums rows [b*rows, (b+1)*rows) of dy into
 // partial_db[b][:].  Thread = (row lane, 8-column group); each thread sums its
 // rows in order, then row lanes are combined in order: a fixed summation order.
-// rows = n / (2 * 152) rounded up to a multiple of 256, within [256, 4096].
-__host__ __device__ inline int64_t dbias_rows(int64_t n) {
-    int64_t r = (n / (2 * 152) + 255) / 256 * 256;
+// rows = n / (2 * SMs) rounded up to a multiple of 256, within [256, 4096].
+inline int64_t dbias_rows(int64_t n, int sms) {
+    int64_t r = (n / (2 * (int64_t)sms) + 255) / 256 * 256;
     return r < 256 ? 256 : (r > 4096 ? 4096 : r);
 }
 
@@ -282,9 +282,9 @@ int simt_gather_pass(const GatherPass& p, cudaStream_t s) {
     return VG_ERR_INVALID_ARG;
 }
 
-int simt_wgrad_splits(int64_t n, int Cin, int Cout) {
+int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms) {
     const int64_t tiles = (int64_t)kTaps * ((Cin + BM - 1) / BM) * ((Cout + BN - 1) / BN);
-    int64_t s = (4 * 152 + tiles - 1) / tiles;
+    int64_t s = (4 * (int64_t)sms + tiles - 1) / tiles;
     s = std::min<int64_t>(s, std::max<int64_t>(1, (n + 1023) / 1024));
     return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
 }
@@ -302,7 +302,7 @@ static int launch_wgrad(const WgradPass& p, cudaStream_t s) {
                                              p.Cin, p.Cout, rpc, p.partial);
         launch_reduce_splits(p.partial, S, total, p.dW, p.dtype, p.nbr_status, s);
     }
-    if (p.db) launch_dbias(p.dy, p.n, p.Cout, S, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;
 }
 
@@ -330,23 +330,72 @@ void launch_reduce_splits(const float* partial, int splits, int64_t total, void*
     else reduce_t<__nv_bfloat16>(partial, splits, total, out, nbr_status, s);
 }
 
-int dbias_blocks(int64_t n) { return (int)std::max<int64_t>(1, (n + dbias_rows(n) - 1) / dbias_rows(n)); }
+int dbias_blocks(int64_t n, int sms) {
+    const int64_t r = dbias_rows(n, sms);
+    return (int)std::max<int64_t>(1, (n + r - 1) / r);
+}
 
 template <typename T>
-static void dbias_t(const void* dy, int64_t n, int Cout, void* db, float* partial_db,
+static void dbias_t(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                     const uint32_t* nbr_status, cudaStream_t s) {
-    const int R = dbias_blocks(n);
-    k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, dbias_rows(n), partial_db,
+    const int R = dbias_blocks(n, sms);
+    k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, dbias_rows(n, sms), partial_db,
                                          nbr_status);
     reduce_t<T>(partial_db, R, Cout, db, nbr_status, s);
 }
 
-void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s) {
-    (void)splits;
-    if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, db, partial_db, nbr_status, s);
-    else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, db, partial_db, nbr_status, s);
-    else dbias_t<__nv_bfloat16>(dy, n, Cout, db, partial_db, nbr_status, s);
+    if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
+    else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
+    else dbias_t<__nv_bfloat16>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
+}
+
+// out[i] = sum over p = 0 .. nparts-1, in that order, of parts[p][i] (fp32 adds),
+// rounded once to T: the rank-ordered gradient sum of data-parallel training.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_sum_ordered(const T* __restrict__ parts, int nparts, int64_t count, T* __restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < count; i += (int64_t)gridDim.x * 256) {
+        float s = to_f32(parts[i]);
+        for (int p = 1; p < nparts; ++p) s += to_f32(parts[(int64_t)p * count + i]);
+        out[i] = from_f32<T>(s);
+    }
+}
+
+int launch_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, void* out, int sms,
+                       cudaStream_t s) {
+    if (count == 0) return VG_OK;
+    const unsigned blocks = (unsigned)std::min<int64_t>((count + 255) / 256, 8 * (int64_t)sms);
+    if (dtype == VG_F32)
+        k_sum_ordered<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(parts), nparts, count,
+                                                    static_cast<float*>(out));
+    else if (dtype == VG_F16)
+        k_sum_ordered<__half><<<blocks, 256, 0, s>>>(static_cast<const __half*>(parts), nparts, count,
+                                                     static_cast<__half*>(out));
+    else
+        k_sum_ordered<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(parts), nparts,
+                                                             count, static_cast<__nv_bfloat16*>(out));
+    return VG_OK;
+}
+
+int plan_sms(int requested) {
+    if (requested > 0) return requested;
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev];  // 0 = not looked up yet (benign race: same value)
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return kDefaultSms;
+    }
+    if (dev < kMaxDev && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return kDefaultSms;
+    }
+    if (dev < kMaxDev) cached[dev] = n;
+    return n;
 }
 
 }  // namespace vg

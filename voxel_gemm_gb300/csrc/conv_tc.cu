@@ -1,5 +1,7 @@
-// Tensor-core (tcgen05 / TMEM) masked implicit GEMM for 16-bit features:
-// the forward pass and the input-gradient pass over Morton-sorted row tiles.
+// Tensor-core (tcgen05 / TMEM) masked implicit GEMM: the forward pass and the
+// input-gradient pass over the sorted row tiles, for fp16/bf16 features
+// (kind::f16) and for fp32 features read as TF32 (kind::tf32, when the caller
+// allows TF32).
 //
 // Method: "From CUDA to Triton: Triton JIT and autotuning", §六 6.2 — the
 // masked implicit GEMM kernel takes (input, weight, bias, neighbor,
@@ -8,7 +10,8 @@
 // neighbour cache ("Contribution Tasks — JeffreyXiang/FlexGEMM", §二 call flow).
 //
 // GB300 design (one CTA per SM, persistent over (128-row tile, N block) units):
-//   warps 0-3  gather: per tap and 64-channel K block, 128 rows x 128 B of the
+//   warps 0-3  gather: per tap and 128-byte K block (64 16-bit or 32 fp32
+//              channels), 128 rows x 128 B of the
 //              feature matrix via 16-byte cp.async with zero fill for missing
 //              neighbours, written in the 128-byte-swizzled K-major layout; each
 //              thread's copies arrive on the stage barrier by themselves
@@ -18,10 +21,11 @@
 //              the tile's 13.5 KB neighbour block.  (L2 prefetching of later taps'
 //              rows was measured to slow the gathers.)
 //   warp 4     TMEM allocation and the single MMA-issuing thread:
-//              tcgen05.mma M=128, N=BN, K=16, fp32 accumulators in TMEM,
-//              two accumulator buffers so the epilogue overlaps the next tile.
-//   warps 5-8  epilogue: tcgen05.ld, + bias, round to fp16/bf16, scatter rows
-//              back to the caller's order through sorted_idx.
+//              tcgen05.mma M=128, N=BN, K=16 (K=8 for TF32), fp32 accumulators
+//              in TMEM, several accumulator buffers so the epilogue overlaps
+//              the next tiles.
+//   warps 5-8  epilogue: tcgen05.ld, + bias, round to the output type, scatter
+//              rows back to the caller's order through sorted_idx.
 //   warp 9     weight-tile loader: one bulk copy (TMA engine) of the prepacked
 //              weight tile per stage, kept off the gather warps' issue path.
 #include "common.cuh"
@@ -36,22 +40,27 @@ using namespace ptx;
 
 constexpr int kThreads = 320;          // 10 warps
 constexpr int kBM = 128;               // rows per tile (MMA M)
-constexpr int kBK = 64;                // 16-bit elements per K block (128 bytes)
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kMaxBiasCols = 2048;     // bias staged in shared memory (16-bit) up to this many columns
+constexpr int kKBytes = 128;           // bytes of one K block of a row (64 16-bit or 32 fp32 values)
+constexpr int kABytes = kBM * kKBytes;  // 16 KB
+constexpr int kMaxBiasCols = 2048;     // 16-bit bias staged in shared memory up to this many columns
+
+// Element types of the kernel: A, B, bias and output share one.
+constexpr int kF16 = VG_F16, kBF16 = VG_BF16, kTF32 = VG_F32;
+template <int DT> struct Elt { static constexpr int size = DT == kTF32 ? 4 : 2; };
 
 int choose_bn(int ndim) {
     if (ndim % 256 == 0) return 256;
     if (ndim % 128 == 0) return 128;
-    return 64;
+    if (ndim % 64 == 0) return 64;
+    return 32;  // TF32 only (channels multiples of 32)
 }
 
 template <int BN>
 struct Cfg {
     static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);  // pipeline stages
-    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kBBytes = BN * kKBytes;
     static constexpr int NBUF = BN <= 128 ? 4 : 2;                  // TMEM accumulator buffers
-    static constexpr int kTmemCols = NBUF * BN;                      // 256 or 512 columns
+    static constexpr int kTmemCols = NBUF * BN;                      // 128, 256 or 512 columns
     static constexpr size_t kSmemA = (size_t)S * kABytes;
     static constexpr size_t kSmemB = (size_t)S * kBBytes;
     static constexpr size_t kNbrTileBytes = (size_t)kBM * kTaps * 4;  // one tile of neighbour lists
@@ -67,11 +76,11 @@ struct TcArgs {
     const uint32_t* nbr_status;
     int64_t n;
     int64_t num_tiles;
-    const uint16_t* A;    // [n][Kdim] 16-bit
+    const uint8_t* A;     // [n][Kdim] elements
     int Kdim;
     const uint8_t* Bimg;  // packed weight tiles
-    const uint16_t* bias; // [Ndim] or null
-    uint16_t* out;        // [n][Ndim]
+    const void* bias;     // [Ndim] or null
+    uint8_t* out;         // [n][Ndim]
     int Ndim;
     uint32_t* err;
 };
@@ -92,10 +101,47 @@ __device__ __forceinline__ float bits_to_f32(uint16_t b) {
     else return __half2float(__ushort_as_half(b));
 }
 
-template <int BN, bool BF16>
+// Round 32 fp32 accumulators (+ bias) to the output type and store them: 64 B
+// (16-bit) or 128 B (fp32) of one output row.  The 16-bit bias comes from its
+// shared-memory copy, the fp32 bias straight from global memory (read-only path).
+template <int DT>
+__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&acc)[32], const void* s_bias,
+                                            const void* g_bias, int col) {
+    const bool has_bias = g_bias != nullptr;
+    if constexpr (DT == kTF32) {
+        const float* sb = static_cast<const float*>(g_bias);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(acc[4 * i + e]) + (has_bias ? __ldg(sb + col + 4 * i + e) : 0.f);
+            d4[i] = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                               __float_as_uint(v[3]));
+        }
+    } else {
+        const uint16_t* sb = static_cast<const uint16_t*>(s_bias);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
+            if (has_bias) {
+                lo += bits_to_f32<DT == kBF16>(sb[col + 2 * i]);
+                hi += bits_to_f32<DT == kBF16>(sb[col + 2 * i + 1]);
+            }
+            pk[i] = pack2<DT == kBF16>(lo, hi);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+}
+
+template <int BN, int DT>
 __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     using C = Cfg<BN>;
     constexpr int S = C::S;
+    constexpr int ES = Elt<DT>::size;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -104,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_nbr + 2 * kBM * kTaps);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile uint32_t* s_abort = s_tmem + 1;
-    uint16_t* s_bias = reinterpret_cast<uint16_t*>(s_tmem + 4);  // [Ndim] when bias is given
+    uint8_t* s_bias = reinterpret_cast<uint8_t*>(s_tmem + 4);  // [Ndim] elements when bias is given
 
     if (*a.nbr_status) return;  // bad neighbour map: write nothing (uniform over the block)
 
@@ -133,15 +179,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
         tmem_relinquish();
     }
-    if (a.bias)
-        for (int c = threadIdx.x; c < a.Ndim; c += kThreads) s_bias[c] = a.bias[c];
+    if (DT != kTF32 && a.bias) {
+        const uint32_t* bsrc = static_cast<const uint32_t*>(a.bias);
+        for (int c = threadIdx.x; c < a.Ndim / 2; c += kThreads) reinterpret_cast<uint32_t*>(s_bias)[c] = bsrc[c];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
     const int NB = a.Ndim / BN;
-    const int KB = a.Kdim / kBK;
+    const int64_t a_row_bytes = (int64_t)a.Kdim * ES;
+    const int KB = (int)(a_row_bytes / kKBytes);
     const int64_t units = a.num_tiles * NB;
 
     if (warp < 4) {
@@ -183,12 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                 if (!((tm >> k) & 1u)) continue;
                 // this thread's 8 source rows for tap k, read from shared memory once per tap
                 // (all eight loads issue back to back) and reused by every K block
-                const uint16_t* src[8];
+                const uint8_t* src[8];
                 uint32_t src_bytes[8];
 #pragma unroll
                 for (int i2 = 0; i2 < 8; ++i2) {
                     const uint32_t j = nb_tile[(i2 * 16 + (p >> 3)) * kTaps + k];
-                    src[i2] = a.A + (int64_t)(j != kNone ? j : 0u) * a.Kdim + ch * 8;
+                    src[i2] = a.A + (int64_t)(j != kNone ? j : 0u) * a_row_bytes + ch * 16;
                     src_bytes[i2] = j != kNone ? 16u : 0u;
                 }
                 for (int kb = 0; kb < KB; ++kb) {
@@ -202,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
 #pragma unroll
                     for (int i2 = 0; i2 < 8; ++i2) {
                         const int row = i2 * 16 + (p >> 3);
-                        cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src[i2] + kb * kBK, src_bytes[i2]);
+                        cp_async16(a_base + row * 128 + ((ch ^ (row & 7)) << 4), src[i2] + kb * kKBytes,
+                                   src_bytes[i2]);
                     }
                     // arrives on the stage barrier when this thread's copies have landed
                     cp_async_arrive_noinc(full0 + 8 * stage);
@@ -223,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BF16, BN);
+            constexpr uint32_t idesc = DT == kTF32 ? idesc_tf32(BN) : idesc_f16(DT == kBF16, BN);
             uint32_t it = 0, ua = 0;
             bool ok = true;
             uint32_t tm_next = (int64_t)blockIdx.x < units ? a.tile_mask[blockIdx.x / NB] : 0u;
@@ -246,10 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                         tc_fence_after();
                         const uint32_t a_base = smem_u32(sA + stage * kABytes);
                         const uint32_t b_base = smem_u32(sB + stage * C::kBBytes);
+                        // four MMAs per 128-byte K block: K = 16 (16-bit) or K = 8 (TF32),
+                        // 32 bytes of each row apiece
 #pragma unroll
-                        for (int j = 0; j < kBK / 16; ++j) {
-                            mma_f16(d_tmem, sw128_kmajor_desc(a_base + 32 * j), sw128_kmajor_desc(b_base + 32 * j),
-                                    idesc, acc | (uint32_t)j);
+                        for (int j = 0; j < 4; ++j) {
+                            if constexpr (DT == kTF32)
+                                mma_tf32(d_tmem, sw128_kmajor_desc(a_base + 32 * j),
+                                         sw128_kmajor_desc(b_base + 32 * j), idesc, acc | (uint32_t)j);
+                            else
+                                mma_f16(d_tmem, sw128_kmajor_desc(a_base + 32 * j),
+                                        sw128_kmajor_desc(b_base + 32 * j), idesc, acc | (uint32_t)j);
                         }
                         acc = 1;
                         mma_commit(empty0 + 8 * stage);
@@ -297,21 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
                 uint32_t acc[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
                 tmem_ld_wait();
-                if (v != kNone) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
-                        if (a.bias) {
-                            lo += bits_to_f32<BF16>(s_bias[col0 + c0 + 2 * i]);
-                            hi += bits_to_f32<BF16>(s_bias[col0 + c0 + 2 * i + 1]);
-                        }
-                        pk[i] = pack2<BF16>(lo, hi);
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(a.out + (int64_t)v * a.Ndim + col0 + c0);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                if (v != kNone)
+                    store_row32<DT>(a.out + ((int64_t)v * a.Ndim + col0 + c0) * ES, acc, s_bias, a.bias, col0 + c0);
             }
             tc_fence_before();
             __syncwarp();
@@ -362,34 +405,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
 }
 
 // Repack W into the B-operand tiles the MMA reads: for tap k, N block nb and
-// K block kb, a [BN rows][64 K elements] tile, rows of 128 B in the 128-byte
-// swizzled layout (row n at (n/8)*1024 + (n%8)*128, 16-byte chunk c stored at
-// chunk c ^ (n%8)).  fwd: row n = output channel, K = input channel,
-// element W[k][kk][n].  dgrad: row n = input channel, K = output channel,
-// element W[26-k][n][kk] (the flipped, transposed tap).
+// K block kb, a [BN rows][128 bytes of K] tile (64 16-bit or 32 fp32 K values),
+// rows in the 128-byte swizzled layout (row n at (n/8)*1024 + (n%8)*128,
+// 16-byte chunk c stored at chunk c ^ (n%8)).  fwd: row n = output channel,
+// K = input channel, element W[k][kk][n].  dgrad: row n = input channel,
+// K = output channel, element W[26-k][n][kk] (the flipped, transposed tap).
+// One block = one tap, one K block and 32 consecutive rows n.
+template <typename T>
 __global__ void __launch_bounds__(256)
-k_pack_weights(const uint16_t* __restrict__ W, int Cin, int Cout, int dgrad, int BN, uint8_t* __restrict__ img) {
-    __shared__ uint16_t tile[64][66];
-    const int k = blockIdx.x, kb = blockIdx.y, n0 = blockIdx.z * 64;
+k_pack_weights(const T* __restrict__ W, int Cin, int Cout, int dgrad, int BN, uint8_t* __restrict__ img) {
+    constexpr int KE = 128 / sizeof(T);  // K values per block row
+    constexpr int PER_CHUNK = 16 / sizeof(T);
+    __shared__ T tile[KE][33];
+    const int k = blockIdx.x, kb = blockIdx.y, n0 = blockIdx.z * 32;
     const int Kdim = dgrad ? Cout : Cin;
-    const int KB = Kdim / 64;
+    const int KB = Kdim / KE;
     const int tid = threadIdx.x;
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
+    for (int idx = tid; idx < KE * 32; idx += 256) {
         if (!dgrad) {
-            const int kk = idx >> 6, n = idx & 63;
-            tile[kk][n] = W[((int64_t)k * Cin + kb * 64 + kk) * Cout + n0 + n];
+            const int kk = idx >> 5, n = idx & 31;
+            tile[kk][n] = W[((int64_t)k * Cin + kb * KE + kk) * Cout + n0 + n];
         } else {
-            const int n = idx >> 6, kk = idx & 63;
-            tile[kk][n] = W[((int64_t)(26 - k) * Cin + n0 + n) * Cout + kb * 64 + kk];
+            const int n = idx / KE, kk = idx % KE;
+            tile[kk][n] = W[((int64_t)(26 - k) * Cin + n0 + n) * Cout + kb * KE + kk];
         }
     }
     __syncthreads();
-    for (int chk = tid; chk < 64 * 8; chk += 256) {
+    for (int chk = tid; chk < 32 * 8; chk += 256) {
         const int n = chk >> 3, c = chk & 7;
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = (uint32_t)tile[c * 8 + 2 * e][n] | ((uint32_t)tile[c * 8 + 2 * e + 1][n] << 16);
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (sizeof(T) == 4)
+                w[e] = __float_as_uint(tile[c * PER_CHUNK + e][n]);
+            else
+                w[e] = (uint32_t)tile[c * PER_CHUNK + 2 * e][n] | ((uint32_t)tile[c * PER_CHUNK + 2 * e + 1][n] << 16);
+        }
         const int gn = n0 + n, nb = gn / BN, nl = gn - nb * BN;
         const int64_t base = (((int64_t)nb * kTaps + k) * KB + kb) * (int64_t)BN * 128;
         const int64_t off = base + (nl >> 3) * 1024 + (nl & 7) * 128 + ((c ^ (nl & 7)) << 4);
@@ -397,21 +448,14 @@ k_pack_weights(const uint16_t* __restrict__ W, int Cin, int Cout, int dgrad, int
     }
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
-
-template <int BN, bool BF16>
+template <int BN, int DT>
 int launch_tc(const TcArgs& a, cudaStream_t s) {
     using C = Cfg<BN>;
-    auto kern = k_gather_gemm_tc<BN, BF16>;
+    auto kern = k_gather_gemm_tc<BN, DT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
     const int64_t units = a.num_tiles * (a.Ndim / BN);
-    const int grid = (int)std::min<int64_t>(units, sm_count());
+    const int grid = (int)std::min<int64_t>(units, plan_sms(0));
     kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
@@ -422,25 +466,32 @@ int tc_supported(int dtype, int Cin, int Cout) {
     return (dtype == VG_F16 || dtype == VG_BF16) && Cin % 64 == 0 && Cout % 64 == 0 ? 1 : 0;
 }
 
+int tf32_supported(int dtype, int Cin, int Cout) {
+    return dtype == VG_F32 && Cin % 32 == 0 && Cout % 32 == 0 ? 1 : 0;
+}
+
 size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim) {
-    (void)dtype;
-    return (size_t)kTaps * Kdim * Ndim * 2;
+    return (size_t)kTaps * Kdim * Ndim * (dtype == VG_F32 ? 4 : 2);
 }
 
 int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void* packed,
                     const uint32_t* nbr_status, cudaStream_t s) {
-    (void)dtype;
     (void)nbr_status;
     const int Kdim = dgrad ? Cout : Cin, Ndim = dgrad ? Cin : Cout;
-    const dim3 grid(kTaps, Kdim / 64, Ndim / 64);
-    k_pack_weights<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(W), Cin, Cout, dgrad, choose_bn(Ndim),
-                                        static_cast<uint8_t*>(packed));
+    const int ke = dtype == VG_F32 ? 32 : 64;
+    const dim3 grid(kTaps, Kdim / ke, Ndim / 32);
+    if (dtype == VG_F32)
+        k_pack_weights<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), Cin, Cout, dgrad,
+                                                   choose_bn(Ndim), static_cast<uint8_t*>(packed));
+    else
+        k_pack_weights<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(W), Cin, Cout, dgrad,
+                                                      choose_bn(Ndim), static_cast<uint8_t*>(packed));
     return VG_OK;
 }
 
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     if (p.n == 0) return VG_OK;
-    if (p.bias && p.Ndim > kMaxBiasCols) return VG_ERR_UNSUPPORTED;
+    if (p.dtype != VG_F32 && p.bias && p.Ndim > kMaxBiasCols) return VG_ERR_UNSUPPORTED;
     TcArgs a;
     a.sorted_idx = p.sorted_idx;
     a.tile_mask = p.tile_mask;
@@ -448,18 +499,28 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     a.nbr_status = p.nbr_status;
     a.n = p.n;
     a.num_tiles = (p.n + kBM - 1) / kBM;
-    a.A = static_cast<const uint16_t*>(p.A);
+    a.A = static_cast<const uint8_t*>(p.A);
     a.Kdim = p.Kdim;
     a.Bimg = static_cast<const uint8_t*>(packed);
-    a.bias = static_cast<const uint16_t*>(p.bias);
-    a.out = static_cast<uint16_t*>(p.out);
+    a.bias = p.bias;
+    a.out = static_cast<uint8_t*>(p.out);
     a.Ndim = p.Ndim;
     a.err = p.err;
+    const int bn = choose_bn(p.Ndim);
+    if (p.dtype == VG_F32) {
+        switch (bn) {
+            case 256: return launch_tc<256, kTF32>(a, s);
+            case 128: return launch_tc<128, kTF32>(a, s);
+            case 64: return launch_tc<64, kTF32>(a, s);
+            default: return launch_tc<32, kTF32>(a, s);
+        }
+    }
+    if (bn < 64) return VG_ERR_UNSUPPORTED;
     const bool bf16 = p.dtype == VG_BF16;
-    switch (choose_bn(p.Ndim)) {
-        case 256: return bf16 ? launch_tc<256, true>(a, s) : launch_tc<256, false>(a, s);
-        case 128: return bf16 ? launch_tc<128, true>(a, s) : launch_tc<128, false>(a, s);
-        default: return bf16 ? launch_tc<64, true>(a, s) : launch_tc<64, false>(a, s);
+    switch (bn) {
+        case 256: return bf16 ? launch_tc<256, kBF16>(a, s) : launch_tc<256, kF16>(a, s);
+        case 128: return bf16 ? launch_tc<128, kBF16>(a, s) : launch_tc<128, kF16>(a, s);
+        default: return bf16 ? launch_tc<64, kBF16>(a, s) : launch_tc<64, kF16>(a, s);
     }
 }
 

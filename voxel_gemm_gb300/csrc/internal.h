@@ -9,7 +9,13 @@ namespace vg {
 
 struct NbrLayout;
 
-int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout* L);
+// SM count the launch plans are sized for: `requested` if > 0, else the current
+// device's (looked up once per device), else kDefaultSms when no device is
+// available (host-only size queries on a machine without a GPU).
+constexpr int kDefaultSms = 152;
+int plan_sms(int requested);
+
+int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sms, NbrLayout* L);
 int nbr_sort_passes(const NbrLayout& l);
 int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
               void* ws, size_t ws_bytes, uint32_t* nbr, uint32_t* mask, cudaStream_t s);
@@ -72,24 +78,31 @@ struct WgradPass {
     float* partial_db;  // [S][Cout]
     void* dy_sorted;    // tensor-core path: tc_wgrad_sorted_dy_bytes bytes of scratch (or null if 0)
     int splits;
+    int sms;            // SM count of the plan (grid sizes, db row blocks)
     uint32_t* err;
 };
 
-int simt_wgrad_splits(int64_t n, int Cin, int Cout);
+int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms);
 int simt_wgrad(const WgradPass& p, cudaStream_t s);
 
 // Deterministic fixed-order sum of split-K partials [splits][total] into out (dtype).
 void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
                           const uint32_t* nbr_status, cudaStream_t s);
-// db = column sums of dy over dbias_blocks(n) row blocks, reduced in a fixed order
-// (partial_db holds dbias_blocks(n) x Cout floats; `splits` is unused).
-int dbias_blocks(int64_t n);
-void launch_dbias(const void* dy, int64_t n, int Cout, int splits, void* db, float* partial_db,
+// db = column sums of dy over dbias_blocks(n, sms) row blocks, reduced in a fixed order
+// (partial_db holds dbias_blocks(n, sms) x Cout floats).
+int dbias_blocks(int64_t n, int sms);
+void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s);
+
+// out = sum of parts[0..nparts) in index order with fp32 adds, rounded once (any dtype).
+int launch_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, void* out, int sms,
+                       cudaStream_t s);
 
 // ---- tensor-core (tcgen05) path, 16-bit types ----
 int tc_supported(int dtype, int Cin, int Cout);
-int tc_wgrad_splits(int64_t n, int Cin, int Cout);
+// fp32 features on the tensor cores as TF32 (forward and input gradient): Cin, Cout % 32 == 0
+int tf32_supported(int dtype, int Cin, int Cout);
+int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms);
 size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim);
 // Repack W into the swizzled shared-memory image of the B operand
 // (dgrad = 0: B_k = W_k^T, K = Cin;  dgrad = 1: B_k = W_{26-k}, K = Cout).

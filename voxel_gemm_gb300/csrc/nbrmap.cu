@@ -370,7 +370,7 @@ static int ceil_log2(int64_t v) {
     return b;
 }
 
-int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout* L) {
+int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sms, NbrLayout* L) {
     if (N < 0 || N >= (int64_t(1) << 31) || B <= 0 || X <= 0 || Y <= 0 || Z <= 0) return VG_ERR_INVALID_ARG;
     if ((flags & VG_KEY32) && (flags & VG_KEY64)) return VG_ERR_INVALID_ARG;
     if (flags & ~(VG_KEY32 | VG_KEY64 | VG_TEST_SMALL_HASH)) return VG_ERR_INVALID_ARG;
@@ -378,6 +378,7 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     if (vol >= 18446744073709551615.0) return VG_ERR_UNSUPPORTED;
     NbrLayout l;
     l.n = N;
+    l.sms = plan_sms(sms);
     if (flags & VG_KEY64) l.key64 = 1;
     else if (flags & VG_KEY32) {
         if (vol > 4294967294.0) return VG_ERR_INVALID_ARG;  // all-ones is the empty-slot marker
@@ -411,7 +412,7 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, NbrLayout*
     l.num_tiles = (N + kTileRows - 1) / kTileRows;
     // keys per thread in the radix sort: enough blocks to fill the GPU (about
     // 2 per SM), at most 16 keys per thread
-    const int64_t per_block_target = std::max<int64_t>(1, N / (2 * 152));
+    const int64_t per_block_target = std::max<int64_t>(1, N / (2 * (int64_t)l.sms));
     l.sort_items = (int)std::min<int64_t>(16, std::max<int64_t>(1, (per_block_target + kSortThreads - 1) / kSortThreads));
     int64_t tile = (int64_t)kSortThreads * l.sort_items;
     l.sort_blocks = std::max<int64_t>(1, (N + tile - 1) / tile);
@@ -477,7 +478,7 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
     const int all = passes + l.tile_passes;
     const int64_t sblocks = std::max(l.sort_blocks, l.tile_blocks);
     cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)all - l.off_hist, s);  // counts, status, tickets
-    const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * 152);
+    const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * (int64_t)l.sms);
     k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, passes, mask, ka, hist);
     const uint32_t* vin = nullptr;
     const size_t smem = (size_t)kSortThreads * l.sort_items * (sizeof(SK) + 4);
@@ -520,7 +521,7 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
 int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
               void* ws_, size_t ws_bytes, uint32_t* nbr, uint32_t* mask, cudaStream_t s) {
     NbrLayout l;
-    int st = nbr_layout(N, B, X, Y, Z, flags, &l);
+    int st = nbr_layout(N, B, X, Y, Z, flags, 0, &l);
     if (st != VG_OK) return st;
     if (!ws_ || (reinterpret_cast<uintptr_t>(ws_) & 255)) return VG_ERR_INVALID_ARG;
     if (ws_bytes < l.total) return VG_ERR_WORKSPACE_TOO_SMALL;

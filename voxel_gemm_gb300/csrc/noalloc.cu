@@ -27,20 +27,24 @@ constexpr size_t kNoAllocScratchBytes = 256 + kNoAllocWeightBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices];  // null until a lookup on that device succeeded
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device.  Only a successful
+// lookup is kept; a failed one (for example during a stream capture, or under a
+// sticky error) returns VG_ERR_CUDA and is retried by the next call.
 int scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VG_ERR_CUDA;
-    std::call_once(g_once[dev], [dev] {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return VG_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
-    });
-    if (g_scratch_err[dev] != cudaSuccess || !g_scratch_ptr[dev]) return VG_ERR_CUDA;
+    }
     *out = g_scratch_ptr[dev];
     return VG_OK;
 }
@@ -100,4 +104,15 @@ extern "C" int vg_subm_conv3d_fwd_noalloc(const void* nbr_ws, const uint32_t* nb
     }
     if (st != VG_OK) return st;
     return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
+}
+
+extern "C" int vg_subm_conv3d_fwd_noalloc_status(void* stream) {
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != VG_OK) return VG_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t h = 0;
+    if (cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return VG_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, sizeof(h), s) != cudaSuccess) return VG_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return VG_ERR_CUDA;
+    return (h & kErrTimeout) ? VG_ERR_DEVICE_TIMEOUT : VG_OK;
 }

@@ -7,28 +7,33 @@ namespace vg {
 
 // Conv workspace layout for one (N, Cin, Cout, dtype) problem.
 struct ConvPlan {
-    int tensor_core = 0;   // 16-bit tcgen05 path
+    int sms = 0;           // SM count the plan is sized for
+    int tensor_core = 0;   // 16-bit tcgen05 path (all three passes)
+    int tf32 = 0;          // fp32 forward and input gradient on tcgen05 as TF32 (VG_ALLOW_TF32)
     int splits = 1;        // split-K chunks of the weight gradient
     size_t off_err = 0, off_wfwd = 0, off_wbwd = 0, off_partial = 0, off_partial_db = 0, off_dys = 0, total = 0;
 };
 
 static size_t dtype_size(int dt) { return dt == VG_F32 ? 4 : 2; }
 
-static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, ConvPlan* P) {
+static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int sms, ConvPlan* P) {
     if (N < 0 || N >= (int64_t(1) << 31) || Cin <= 0 || Cout <= 0) return VG_ERR_INVALID_ARG;
     if (dtype != VG_F32 && dtype != VG_F16 && dtype != VG_BF16) return VG_ERR_INVALID_ARG;
-    if (flags != 0) return VG_ERR_UNSUPPORTED;
+    if (flags & ~VG_ALLOW_TF32) return VG_ERR_UNSUPPORTED;
     if (Cin % 8 || Cout % 8) return VG_ERR_UNSUPPORTED;  // 16-byte rows for every dtype
     ConvPlan p;
+    p.sms = plan_sms(sms);
     p.tensor_core = tc_supported(dtype, Cin, Cout);
-    p.splits = p.tensor_core ? tc_wgrad_splits(N, Cin, Cout) : simt_wgrad_splits(N, Cin, Cout);
+    p.tf32 = (flags & VG_ALLOW_TF32) && tf32_supported(dtype, Cin, Cout) ? 1 : 0;
+    const int packed = p.tensor_core || p.tf32;
+    p.splits = p.tensor_core ? tc_wgrad_splits(N, Cin, Cout, p.sms) : simt_wgrad_splits(N, Cin, Cout, p.sms);
     const size_t wbytes = (size_t)kTaps * Cin * Cout * dtype_size(dtype);
     size_t o = 0;
     p.off_err = o;         o += 256;
-    p.off_wfwd = o;        o += p.tensor_core ? align_up(tc_packed_weight_bytes(dtype, Cin, Cout), 256) : 0;
-    p.off_wbwd = o;        o += p.tensor_core ? align_up(tc_packed_weight_bytes(dtype, Cout, Cin), 256) : 0;
+    p.off_wfwd = o;        o += packed ? align_up(tc_packed_weight_bytes(dtype, Cin, Cout), 256) : 0;
+    p.off_wbwd = o;        o += packed ? align_up(tc_packed_weight_bytes(dtype, Cout, Cin), 256) : 0;
     p.off_partial = o;     o += align_up((size_t)p.splits * kTaps * Cin * Cout * 4, 256);
-    p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N) * Cout * 4, 256);
+    p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N, p.sms) * Cout * 4, 256);
     p.off_dys = o;         o += p.tensor_core ? align_up(tc_wgrad_sorted_dy_bytes(N, Cout), 256) : 0;
     (void)wbytes;
     p.total = o;
@@ -72,7 +77,7 @@ int vg_version(void) { return 100; }
 
 size_t vg_nbrmap_workspace_bytes(int64_t N, int B, int X, int Y, int Z, unsigned flags) {
     NbrLayout l;
-    return nbr_layout(N, B, X, Y, Z, flags, &l) == VG_OK ? l.total : 0;
+    return nbr_layout(N, B, X, Y, Z, flags, 0, &l) == VG_OK ? l.total : 0;
 }
 
 int vg_nbrmap_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsigned flags,
@@ -97,9 +102,10 @@ const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N) {
     return ws ? reinterpret_cast<const uint32_t*>(static_cast<const char*>(ws) + tile_mask_offset(N)) : nullptr;
 }
 
-int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int info[4]) {
+int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sm_count, int info[4]) {
     NbrLayout l;
-    const int st = nbr_layout(N, B, X, Y, Z, flags, &l);
+    if (sm_count < 0) return VG_ERR_INVALID_ARG;
+    const int st = nbr_layout(N, B, X, Y, Z, flags, sm_count, &l);
     if (st != VG_OK || !info) return st != VG_OK ? st : VG_ERR_INVALID_ARG;
     const int passes = nbr_sort_passes(l);
     info[0] = l.key64;
@@ -110,20 +116,21 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     return VG_OK;
 }
 
-int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int info[4]) {
+int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int sm_count, int info[4]) {
     ConvPlan p;
-    const int st = conv_plan(N, Cin, Cout, dtype, flags, &p);
+    if (sm_count < 0) return VG_ERR_INVALID_ARG;
+    const int st = conv_plan(N, Cin, Cout, dtype, flags, sm_count, &p);
     if (st != VG_OK || !info) return st != VG_OK ? st : VG_ERR_INVALID_ARG;
-    info[0] = p.tensor_core;
+    info[0] = p.tensor_core ? 1 : (p.tf32 ? 2 : 0);
     info[1] = p.splits;
-    info[2] = N > 0 ? (p.tensor_core ? tc_fwd_launches() : 1) : 0;
-    info[3] = N > 0 ? (p.tensor_core ? tc_bwd_launches(Cout) : 1 + 2 + 2) : 0;
+    info[2] = N > 0 ? (p.tensor_core || p.tf32 ? tc_fwd_launches() : 1) : 0;
+    info[3] = N > 0 ? (p.tensor_core ? tc_bwd_launches(Cout) : (p.tf32 ? 2 : 1) + 2 + 2) : 0;
     return VG_OK;
 }
 
 size_t vg_conv_workspace_bytes(int64_t N, int Cin, int Cout, int dtype, unsigned flags) {
     ConvPlan p;
-    return conv_plan(N, Cin, Cout, dtype, flags, &p) == VG_OK ? p.total : 0;
+    return conv_plan(N, Cin, Cout, dtype, flags, 0, &p) == VG_OK ? p.total : 0;
 }
 
 int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask, int64_t N,
@@ -131,7 +138,7 @@ int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
                        void* out, int Cin, int Cout, unsigned flags,
                        void* conv_ws, size_t conv_ws_bytes, void* stream) {
     ConvPlan p;
-    int st = conv_plan(N, Cin, Cout, dtype, flags, &p);
+    int st = conv_plan(N, Cin, Cout, dtype, flags, 0, &p);
     if (st != VG_OK) return st;
     st = check_common(nbr_ws, nbr, mask, N, conv_ws, conv_ws_bytes, p);
     if (st != VG_OK) return st;
@@ -160,7 +167,7 @@ int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
     g.Ndim = Cout;
     g.dtype = dtype;
     g.err = reinterpret_cast<uint32_t*>(ws + p.off_err);
-    if (p.tensor_core) {
+    if (p.tensor_core || p.tf32) {
         st = tc_pack_weights(weight, dtype, Cin, Cout, 0, ws + p.off_wfwd, g.nbr_status, s);
         if (st == VG_OK) st = tc_gather_pass(g, ws + p.off_wfwd, s);
     } else {
@@ -176,7 +183,7 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
                        int Cin, int Cout, unsigned flags,
                        void* conv_ws, size_t conv_ws_bytes, void* stream) {
     ConvPlan p;
-    int st = conv_plan(N, Cin, Cout, dtype, flags, &p);
+    int st = conv_plan(N, Cin, Cout, dtype, flags, 0, &p);
     if (st != VG_OK) return st;
     st = check_common(nbr_ws, nbr, mask, N, conv_ws, conv_ws_bytes, p);
     if (st != VG_OK) return st;
@@ -219,7 +226,7 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         g.Ndim = Cin;
         g.dtype = dtype;
         g.err = err;
-        if (p.tensor_core) {
+        if (p.tensor_core || p.tf32) {
             st = tc_pack_weights(weight, dtype, Cin, Cout, 1, ws + p.off_wbwd, nbr_status, s);
             if (st == VG_OK) st = tc_gather_pass(g, ws + p.off_wbwd, s);
         } else {
@@ -248,10 +255,24 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         w.partial_db = reinterpret_cast<float*>(ws + p.off_partial_db);
         w.dy_sorted = ws + p.off_dys;
         w.splits = p.splits;
+        w.sms = p.sms;
         w.err = err;
         st = p.tensor_core ? tc_wgrad(w, s) : simt_wgrad(w, s);
         if (st != VG_OK) return st;
     }
+    return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
+}
+
+int vg_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, void* out, void* stream) {
+    if (nparts <= 0 || count < 0) return VG_ERR_INVALID_ARG;
+    if (dtype != VG_F32 && dtype != VG_F16 && dtype != VG_BF16) return VG_ERR_INVALID_ARG;
+    if (count > 0 && (!parts || !out)) return VG_ERR_INVALID_ARG;
+    const size_t es = dtype_size(dtype);
+    if (misaligned(parts, es) || misaligned(out, es)) return VG_ERR_INVALID_ARG;
+    cudaGetLastError();
+    const int st = launch_sum_ordered(parts, nparts, count, dtype, out, plan_sms(0),
+                                      static_cast<cudaStream_t>(stream));
+    if (st != VG_OK) return st;
     return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
 }
 

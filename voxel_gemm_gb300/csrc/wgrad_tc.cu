@@ -454,13 +454,6 @@ int wg_bn(int cout) {
     return 64;
 }
 
-int sm_count_w() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
-}
-
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -479,7 +472,7 @@ EncodeTiled encode_tiled() {
 }
 
 template <int BN, bool BF16>
-int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, cudaStream_t s) {
+int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream_t s) {
     using C = WCfg<BN>;
     auto kern = k_wgrad_tc<BN, BF16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
@@ -501,7 +494,7 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, cudaStream_t s) {
     }
     const int MG = (num_munits(a.Cin) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
-    const int grid = (int)std::min<int64_t>(units, sm_count_w());
+    const int grid = (int)std::min<int64_t>(units, sms);
     kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
     return VG_OK;
 }
@@ -512,13 +505,13 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, cudaStream_t s) {
 // tiles (the units running side by side then stream the same rows through L2;
 // measured at 602k voxels, C = 1024: 2 chunks 17.6 ms, 8 chunks 16.1 ms), at
 // least 4 tiles per chunk (every chunk non-empty), partial sums capped at 1 GiB.
-int tc_wgrad_splits(int64_t n, int Cin, int Cout) {
+int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms) {
     const int bn = wg_bn(Cout);
     const int mu = bn == 64 ? WCfg<64>::MU : (bn == 128 ? WCfg<128>::MU : WCfg<256>::MU);
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
     const int64_t MG = (num_munits(Cin) + mu - 1) / mu;
     const int64_t per_split = MG * (Cout / bn);
-    int64_t S = std::max<int64_t>(1, (4 * 152 + per_split - 1) / per_split);
+    int64_t S = std::max<int64_t>(1, (4 * (int64_t)sms + per_split - 1) / per_split);
     S = std::max<int64_t>(S, (T + 255) / 256);
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
@@ -559,19 +552,19 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
             if (!dys) return VG_ERR_INVALID_ARG;
             const int64_t rows_pad = a.num_tiles * kTileRows;
             const int64_t chunks = rows_pad * (p.Cout / 8);
-            const unsigned blocks = (unsigned)std::min<int64_t>((chunks + 255) / 256, 16 * 152);
+            const unsigned blocks = (unsigned)std::min<int64_t>((chunks + 255) / 256, 16 * (int64_t)p.sms);
             k_sort_rows<<<blocks, 256, 0, s>>>(a.dy, p.sorted_idx, p.n, rows_pad, p.Cout, p.nbr_status, dys);
         }
         int st;
         switch (bn) {
-            case 256: st = bf16 ? launch_wgrad<256, true>(a, dys, s) : launch_wgrad<256, false>(a, dys, s); break;
-            case 128: st = bf16 ? launch_wgrad<128, true>(a, dys, s) : launch_wgrad<128, false>(a, dys, s); break;
-            default: st = bf16 ? launch_wgrad<64, true>(a, dys, s) : launch_wgrad<64, false>(a, dys, s); break;
+            case 256: st = bf16 ? launch_wgrad<256, true>(a, dys, p.sms, s) : launch_wgrad<256, false>(a, dys, p.sms, s); break;
+            case 128: st = bf16 ? launch_wgrad<128, true>(a, dys, p.sms, s) : launch_wgrad<128, false>(a, dys, p.sms, s); break;
+            default: st = bf16 ? launch_wgrad<64, true>(a, dys, p.sms, s) : launch_wgrad<64, false>(a, dys, p.sms, s); break;
         }
         if (st != VG_OK) return st;
         launch_reduce_splits(p.partial, p.splits, (int64_t)kTaps * p.Cin * p.Cout, p.dW, p.dtype, p.nbr_status, s);
     }
-    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.splits, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;
 }
 

@@ -23,6 +23,7 @@ VG_ERR_HASH_FULL, VG_ERR_UNSUPPORTED, VG_ERR_WORKSPACE_TOO_SMALL, VG_ERR_CUDA = 
 VG_ERR_DEVICE_TIMEOUT = 8
 VG_F32, VG_F16, VG_BF16 = 0, 1, 2
 VG_KEY32, VG_KEY64, VG_TEST_SMALL_HASH = 0x1, 0x2, 0x100
+VG_ALLOW_TF32 = 0x10
 VG_NONE = 0xFFFFFFFF
 VG_TILE_ROWS = 128
 
@@ -62,9 +63,11 @@ def lib():
             "vg_subm_conv3d_fwd": ([P, P, P, I64, I, P, P, P, P, I, I, U, P, SZ, P], I),
             "vg_subm_conv3d_bwd": ([P, P, P, I64, I, P, P, P, P, P, P, I, I, U, P, SZ, P], I),
             "vg_conv_status": ([P, P], I),
-            "vg_nbrmap_describe": ([I64, I, I, I, I, U, ctypes.POINTER(ctypes.c_int)], I),
-            "vg_conv_describe": ([I64, I, I, I, U, ctypes.POINTER(ctypes.c_int)], I),
+            "vg_nbrmap_describe": ([I64, I, I, I, I, U, I, ctypes.POINTER(ctypes.c_int)], I),
+            "vg_conv_describe": ([I64, I, I, I, U, I, ctypes.POINTER(ctypes.c_int)], I),
             "vg_subm_conv3d_fwd_noalloc": ([P, P, P, I64, I, P, P, P, P, I, I, U, P], I),
+            "vg_subm_conv3d_fwd_noalloc_status": ([P], I),
+            "vg_sum_ordered": ([P, I, I64, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -160,6 +163,11 @@ def vg_subm_conv3d_fwd_noalloc(nbr_ws, nbr, mask, feats, weight, bias, out, flag
            "vg_subm_conv3d_fwd_noalloc")
 
 
+def vg_subm_conv3d_fwd_noalloc_status(stream=None) -> int:
+    """Device-side status of the last no-allocation forward on the current device (syncs `stream`)."""
+    return lib().vg_subm_conv3d_fwd_noalloc_status(_s(stream))
+
+
 def vg_subm_conv3d_bwd(nbr_ws, nbr, mask, grad_out, feats, weight, grad_feats, grad_weight, grad_bias,
                        conv_ws, flags=0, stream=None) -> None:
     N, Cout = grad_out.shape
@@ -171,17 +179,26 @@ def vg_subm_conv3d_bwd(nbr_ws, nbr, mask, grad_out, feats, weight, grad_feats, g
            "vg_subm_conv3d_bwd")
 
 
-def vg_nbrmap_describe(N, B, X, Y, Z, flags=0) -> dict:
+def vg_nbrmap_describe(N, B, X, Y, Z, flags=0, sm_count=0) -> dict:
     info = (ctypes.c_int * 4)()
-    _check(lib().vg_nbrmap_describe(N, B, X, Y, Z, flags, info), "vg_nbrmap_describe")
+    _check(lib().vg_nbrmap_describe(N, B, X, Y, Z, flags, sm_count, info), "vg_nbrmap_describe")
     return {"key64": info[0], "sort_bits": info[1], "sort_passes": info[2], "launches": info[3]}
 
 
-def vg_conv_describe(N, Cin, Cout, dtype, flags=0) -> dict:
+def vg_conv_describe(N, Cin, Cout, dtype, flags=0, sm_count=0) -> dict:
     code = dtype if isinstance(dtype, int) else _DT[dtype]
     info = (ctypes.c_int * 4)()
-    _check(lib().vg_conv_describe(N, Cin, Cout, code, flags, info), "vg_conv_describe")
+    _check(lib().vg_conv_describe(N, Cin, Cout, code, flags, sm_count, info), "vg_conv_describe")
     return {"tensor_core": info[0], "splits": info[1], "launches_fwd": info[2], "launches_bwd": info[3]}
+
+
+def vg_sum_ordered(parts, out, stream=None) -> None:
+    """out = parts[0] + parts[1] + ... (fp32 adds in index order, one rounding); parts [n, *out.shape]."""
+    if parts.dtype != out.dtype or parts.shape[1:] != out.shape or not parts.is_contiguous() \
+            or not out.is_contiguous():
+        raise ValueError("vg_sum_ordered: parts must be [n, *out.shape], contiguous, of out's dtype")
+    _check(lib().vg_sum_ordered(_p(parts), parts.shape[0], out.numel(), _dtype_code(out), _p(out), _s(stream)),
+           "vg_sum_ordered")
 
 
 def vg_conv_status(conv_ws, stream=None) -> int:

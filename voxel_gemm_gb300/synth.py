@@ -157,6 +157,17 @@ def shell_voxels(kind: str, centre, radii, res: int) -> np.ndarray:
     return np.stack([cx_[ok], cy_[ok], zs[ok]], axis=1).astype(np.int64)
 
 
+def _sorted_unique(a: np.ndarray) -> np.ndarray:
+    """Sorted distinct values of a 1-D array (np.unique's result, by sort + compare)."""
+    a = np.sort(a)
+    if a.size == 0:
+        return a
+    keep = np.empty(a.size, dtype=bool)
+    keep[0] = True
+    np.not_equal(a[1:], a[:-1], out=keep[1:])
+    return a[keep]
+
+
 def make_coords(wl: Workload) -> np.ndarray:
     """int32 [N,4] (b,x,y,z), deduplicated, rows in a seeded random permutation."""
     rng = np.random.default_rng(wl.seed)
@@ -165,16 +176,17 @@ def make_coords(wl: Workload) -> np.ndarray:
     for b, kind, centre, radii in _shape_params(wl, rng):
         v = shell_voxels(kind, centre, radii, res)
         keys.append(((b * res + v[:, 0]) * res + v[:, 1]) * res + v[:, 2])
-    allk = np.unique(np.concatenate(keys)) if keys else np.zeros(0, np.int64)
+    allk = _sorted_unique(np.concatenate(keys)) if keys else np.zeros(0, np.int64)
     perm = rng.permutation(allk.size)
     allk = allk[perm]
-    z = allk % res
+    out = np.empty((allk.size, 4), dtype=np.int32)
+    out[:, 3] = allk % res
     t = allk // res
-    y = t % res
+    out[:, 2] = t % res
     t //= res
-    x = t % res
-    b = t // res
-    return np.stack([b, x, y, z], axis=1).astype(np.int32)
+    out[:, 1] = t % res
+    out[:, 0] = t // res
+    return out
 
 
 TORCH_DTYPES = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
