@@ -38,6 +38,8 @@ METRIC = "submanifold conv3d fwd+bwd voxels/s & TFLOP/s (valid pairs), % of GB30
 DEFAULT_WORKLOAD = "b1_r512_shapes_c1024_bf16"
 SWEEP = ["b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16",
          "b1_r512_shapes_c512_bf16", "b1_r1024_shapes_c64_f16"]
+INFER_WORKLOAD = "b1_r64_spheres_c256_bf16_infer"
+ORDER_WORKLOADS = ["b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16", "b1_r1024_shapes_c64_f16"]
 STEP = "nbrmap build + fwd + dgrad + wgrad + dbias"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 << 20
@@ -494,6 +496,112 @@ def run_workload(args, wl, rank, world, dev, flush, full):
     return rec
 
 
+def run_inference(args, wl, dev, flush):
+    """The small-N inference forward (few voxels, forward only): CUDA-event time of the
+    forward call with the default plan (taps cut into groups when the (tile, channel
+    block) units do not fill the SMs) and with VG_NO_SMALL_N_SPLIT, same inputs."""
+    import torch
+    from voxel_gemm_gb300 import ops, synth
+    stream = torch.cuda.Stream(device=dev)
+    coords_np = synth.make_coords(wl)
+    N = coords_np.shape[0]
+    dt = synth.torch_dtype(wl.dtype)
+    s = 4 if wl.dtype == "f32" else 2
+    with torch.cuda.stream(stream):
+        coords = torch.from_numpy(coords_np).to(dev)
+        f, W, b, _ = synth.make_tensors(wl, N, device=dev)
+        m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag, device=dev)
+        out = torch.empty(N, wl.cout, dtype=dt, device=dev)
+    m.build(coords, stream)
+    assert m.status(stream) == ops.VG_OK
+    P = count_pairs(m.mask.cpu().numpy().view("uint32"))
+    rec = {"workload": wl.name, "N": N, "P": P, "pass": "fwd"}
+    peaks = load_peaks()
+    for tag, flags in (("split", 0), ("unsplit", ops.VG_NO_SMALL_N_SPLIT)):
+        with torch.cuda.stream(stream):
+            ws = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev, flags=flags)
+        call = lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, flags=flags,  # noqa: E731
+                                              stream=stream)
+        for _ in range(3):
+            call()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        ts = []
+        for _ in range(max(5, min(args.steps, 50))):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            ts.append((e0, e1))
+        stream.synchronize()
+        assert ops.vg_conv_status(ws, stream) == ops.VG_OK
+        ms = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+        plan = ops.vg_conv_describe(N, wl.cin, wl.cout, dt, flags)
+        fl, by = pass_work(N, P, wl.cin, wl.cout, s, 1)["fwd"]
+        rec[tag] = {"ms": ms, "launches": plan["launches_fwd"], "tflops": fl / (ms * 1e-3) / 1e12,
+                    "frac_of_roofline": max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+                    / (ms * 1e-3)}
+    rec["speedup_split"] = rec["unsplit"]["ms"] / rec["split"]["ms"]
+    return rec
+
+
+def run_row_orders(args, wl, dev, flush):
+    """The two row orders of the neighbour map on one workload: Morton (the default)
+    and Hilbert (VG_ORDER_HILBERT).  Per order: the useful fraction of the MMA rows
+    (valid pairs / (rows x taps the tile masks make the GEMM process)), and the
+    CUDA-event time of the map build, the forward and the weight-gradient call."""
+    import numpy as np
+    import torch
+    from voxel_gemm_gb300 import ops, synth
+    stream = torch.cuda.Stream(device=dev)
+    coords_np = synth.make_coords(wl)
+    N = coords_np.shape[0]
+    dt = synth.torch_dtype(wl.dtype)
+    with torch.cuda.stream(stream):
+        coords = torch.from_numpy(coords_np).to(dev)
+        f, W, b, dY = synth.make_tensors(wl, N, device=dev)
+        out = torch.empty(N, wl.cout, dtype=dt, device=dev)
+        dW = torch.empty(27, wl.cin, wl.cout, dtype=dt, device=dev)
+        db = torch.empty(wl.cout, dtype=dt, device=dev)
+        ws = ops.conv_workspace(N, wl.cin, wl.cout, dt, device=dev)
+    rec = {"workload": wl.name, "N": N}
+    for tag, flag in (("morton", 0), ("hilbert", ops.VG_ORDER_HILBERT)):
+        m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag | flag, device=dev)
+        m.build(coords, stream)
+        assert m.status(stream) == ops.VG_OK
+        tm = m.tile_mask().cpu().numpy().view(np.uint32)
+        pop_tiles = int(sum(int(((tm >> k) & 1).sum()) for k in range(27)))
+        P = count_pairs(m.mask.cpu().numpy().view("uint32"))
+        calls = {
+            "nbrmap": lambda: m.build(coords, stream),
+            "fwd": lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=stream),
+            "wgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws, stream=stream),
+        }
+        r = {"useful_mma_row_fraction": P / (128.0 * pop_tiles)}
+        for name, fn in calls.items():
+            fn()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            ts = []
+            for _ in range(max(3, min(args.steps, 10))):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                ts.append((e0, e1))
+            stream.synchronize()
+            r[name + "_ms"] = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+        assert ops.vg_conv_status(ws, stream) == ops.VG_OK
+        rec[tag] = r
+    return rec
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from voxel_gemm_gb300 import synth
@@ -514,6 +622,21 @@ def run_ours(args, rank, world, local_rank):
             except Exception as e:  # noqa: BLE001 - a failed sub-record must not hide the headline
                 sweep.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
             torch.cuda.empty_cache()
+        try:
+            infer = run_inference(args, synth.WORKLOADS[INFER_WORKLOAD], dev, flush)
+        except Exception as e:  # noqa: BLE001
+            infer = {"workload": INFER_WORKLOAD, "error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+        orders = []
+        for name in ORDER_WORKLOADS:
+            try:
+                orders.append(run_row_orders(args, synth.WORKLOADS[name], dev, flush))
+            except Exception as e:  # noqa: BLE001
+                orders.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
+            torch.cuda.empty_cache()
+    else:
+        infer = None
+        orders = None
 
     res = {
         "metric": METRIC, "value": head["value"], "unit": "voxels/s", "n_gpus": world,
@@ -528,6 +651,8 @@ def run_ours(args, rank, world, local_rank):
         "path": head["path"], "launch": head["launch"], "clocks": head["clocks"],
         "wall_s_timed_region": head["wall_s_timed_region"],
         "sweep": sweep,
+        "inference_small_n": infer,
+        "row_order_morton_vs_hilbert": orders,
     }
     return res
 

@@ -70,6 +70,7 @@ extern "C" {
 /* ---- flags -------------------------------------------------------------------------- */
 #define VG_KEY32            0x1u   /* force 32-bit hash keys (needs B*X*Y*Z < 2^32)    */
 #define VG_KEY64            0x2u   /* force 64-bit hash keys                            */
+#define VG_ORDER_HILBERT    0x4u   /* row order from the Hilbert code instead of Morton  */
 /* Testing aid: size the hash table below N so that the overflow path
  * (VG_ERR_HASH_FULL) can be exercised from the host. */
 #define VG_TEST_SMALL_HASH  0x100u
@@ -80,6 +81,14 @@ extern "C" {
  * Applies to fp32 with Cin and Cout multiples of 32; otherwise, and without the
  * flag, fp32 runs on the exact FFMA path. */
 #define VG_ALLOW_TF32       0x10u
+/* Convolution flag: on the tensor-core paths, keep one work unit per (128-row
+ * tile, output-channel block) even when there are fewer such units than SMs.
+ * By default a small problem (the pages' inference benchmark case: few voxels)
+ * cuts each unit's taps into up to 6 groups that run on separate SMs and writes
+ * fp32 partial sums, which a second kernel adds in group order (deterministic)
+ * before the bias and the rounding; this flag turns that off, for comparisons.
+ * Results agree within rounding either way. */
+#define VG_NO_SMALL_N_SPLIT 0x20u
 
 #define VG_NONE 0xFFFFFFFFu        /* missing neighbour in nbr                          */
 #define VG_TILE_ROWS 128           /* rows per tile of the sorted order (tile masks)    */
@@ -128,7 +137,9 @@ VG_API int vg_nbrmap_status(const void* ws, void* stream);
  *   sorted_idx [N] uint32 — row r of the processing order is voxel sorted_idx[r]
  *                (the page's sorted_idx).  Stable sort by the key
  *                ((m >> F) << (27 + G)) | (mask << G) | ((m & (2^F - 1)) >> (F - G)),
- *                where m = (b << 3L) | bit-interleave(x, y, z) is the Morton code,
+ *                where m = (b << 3L) | bit-interleave(x, y, z) is the Morton code
+ *                (with VG_ORDER_HILBERT: m = (b << 3L) | Hilbert code of (x, y, z) with
+ *                L bits, as vg_encode_seq computes it),
  *                L = ceil(log2(max(X,Y,Z))), F = min(3L, 30) and G = min(F, 6),
  *                lowered to 32 - 27 - (bits of m above F) when that makes the
  *                whole key fit 32 bits (4 radix passes instead of 5):
@@ -166,7 +177,8 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
  *          TF32), VG_F16 or VG_BF16 (tensor-core path when Cin and Cout are
  *          multiples of 64, CUDA-core path otherwise).
  *   Cin and Cout must be multiples of 8 (VG_ERR_UNSUPPORTED otherwise); flags
- *   is 0 or VG_ALLOW_TF32 (other bits: VG_ERR_UNSUPPORTED).
+ *   is 0 or a combination of VG_ALLOW_TF32 and VG_NO_SMALL_N_SPLIT (other bits:
+ *   VG_ERR_UNSUPPORTED); the conv workspace size depends on the flags.
  *   feats [N][Cin], weight [27][Cin][Cout], bias [Cout] (or NULL), out [N][Cout],
  *   all of `dtype`, 16-byte aligned.
  *   nbr_ws/nbr/mask: a map built by vg_nbrmap_build for the same N.
@@ -215,6 +227,31 @@ VG_API int vg_conv_status(void* conv_ws, void* stream);
 
 
 /* ======================================================================================
+ * Serialisation: space-filling-curve codes of voxel coordinates
+ * "Contribution Tasks — JeffreyXiang/FlexGEMM", §二 module table (kernels.cuda.serialize:
+ * z_order_encode/decode, hilbert_encode/decode) and the ops layer's
+ * encode_seq/decode_seq(coords, shape, mode).  The pages give the names only; the
+ * reading taken: code = (b << 3*bits) | curve(x, y, z) for x, y, z in [0, 2^bits).
+ *   VG_CURVE_ZORDER:  bit j of x, y, z at bit 3j+2, 3j+1, 3j of the curve part.
+ *   VG_CURVE_HILBERT: J. Skilling's Hilbert curve ("Programming the Hilbert curve",
+ *                     AIP Conf. Proc. 707, 2004): consecutive codes are face
+ *                     neighbours; its transposed index is interleaved like a z-order
+ *                     code, x before y before z at each level.
+ * The neighbour-map build can use either curve for its row order (VG_ORDER_HILBERT).
+ * ====================================================================================== */
+#define VG_CURVE_ZORDER  0
+#define VG_CURVE_HILBERT 1
+
+/* codes[i] (uint64, device) of coords[i] = (b,x,y,z) (int32 [N][4], device, 16-byte
+ * aligned), bits in [0, 20].  A row whose x, y or z lies outside [0, 2^bits), or whose
+ * b is negative or does not fit above the curve bits (b >= 2^(63 - 3*bits)), gets
+ * the code 0xFFFFFFFFFFFFFFFF.  Asynchronous; VG_ERR_INVALID_ARG for bad sizes,
+ * modes or pointers. */
+VG_API int vg_encode_seq(const int32_t* coords, int64_t N, int bits, int mode, uint64_t* codes, void* stream);
+/* The inverse: coords[i] = (b,x,y,z) of codes[i] (the bits above 3*bits are b). */
+VG_API int vg_decode_seq(const uint64_t* codes, int64_t N, int bits, int mode, int32_t* coords, void* stream);
+
+/* ======================================================================================
  * Data-parallel gradient exchange
  * The pages describe a single-GPU operator library and have no multi-GPU step.
  * When several processes each run the convolution on their own batch elements
@@ -242,8 +279,9 @@ VG_API int vg_sum_ordered(const void* parts, int nparts, int64_t count, int dtyp
  * Arguments and output are those of vg_subm_conv3d_fwd without conv_ws: the scratch
  * (repacked weight tiles and the error word) is a fixed __device__ array of
  * 8 MiB + 256 B inside the library, which every GPU that loads the library holds
- * until the process exits.  The call runs the same kernels as vg_subm_conv3d_fwd,
- * so the output is bit-identical to it.  A kernel that gives up a bounded wait
+ * until the process exits.  The call runs the same kernels as vg_subm_conv3d_fwd
+ * with VG_NO_SMALL_N_SPLIT (it has no room for split partial sums), so the
+ * output is bit-identical to that call's.  A kernel that gives up a bounded wait
  * is reported by vg_subm_conv3d_fwd_noalloc_status(), not by this call's
  * return value (which covers argument and launch errors only).
  *  - Returns VG_ERR_WORKSPACE_TOO_SMALL when the repacked weights (27*Cin*Cout*2

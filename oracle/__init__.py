@@ -20,7 +20,11 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                 all-ones closed form, permutation equivariance
   dgrad_scatter dense conv3d autograd, adjoint identity
   dgrad_rows    equal to dgrad_scatter (it is a regrouping of the same sum)
-  wgrad         dense conv3d autograd, central finite differences
+  wgrad         dense conv3d autograd (dW and db), central finite differences
+  curve_encode / curve_decode (z-order, Hilbert)
+                bijection onto [0, 8^bits) by exhaustion on small cubes, decode is
+                the inverse of encode, z-order's parent/child nesting, Hilbert's
+                unit steps between consecutive codes
 No function is left unpinned.
 """
 from __future__ import annotations
@@ -74,6 +78,10 @@ def _load():
         lib.oracle_dgrad_rows.restype = None
         lib.oracle_wgrad.argtypes = [P, I64, P, I64, P, I, I, P, P]
         lib.oracle_wgrad.restype = None
+        lib.oracle_curve_encode.argtypes = [P, I64, I, I, P]
+        lib.oracle_curve_encode.restype = I
+        lib.oracle_curve_decode.argtypes = [P, I64, I, I, P]
+        lib.oracle_curve_decode.restype = I
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = I
         lib.oracle_set_num_threads.argtypes = [I]
@@ -166,3 +174,27 @@ def wgrad(nbr, f, dY, with_bias: bool = True):
     _load().oracle_wgrad(_ptr(nbr), nbr.shape[0], _ptr(f), f.shape[0], _ptr(dY), cin, cout,
                          _ptr(dW), None if db is None else _ptr(db))
     return dW, db
+
+
+ZORDER, HILBERT = 0, 1
+
+
+def curve_encode(coords, bits: int, curve: int):
+    """uint64 codes (b << 3*bits) | curve(x, y, z) of int32 (b,x,y,z) rows; curve ZORDER or HILBERT."""
+    c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
+    out = np.empty(c.shape[0], dtype=np.uint64)
+    rc = _load().oracle_curve_encode(_ptr(c), c.shape[0], bits, curve, _ptr(out))
+    if rc != OK:
+        raise OracleError(rc)
+    return out
+
+
+def curve_decode(codes, bits: int, curve: int):
+    """int32 (b,x,y,z) rows of uint64 curve codes (the inverse of curve_encode)."""
+    k = np.ascontiguousarray(np.asarray(codes, dtype=np.uint64).reshape(-1))
+    out = np.empty((k.shape[0], 4), dtype=np.int32)
+    rc = _load().oracle_curve_decode(_ptr(k), k.shape[0], bits, curve, _ptr(out))
+    if rc != OK:
+        raise OracleError(rc)
+    return out
+

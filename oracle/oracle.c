@@ -261,3 +261,144 @@ void oracle_wgrad(const uint32_t* nbr, int64_t N, const double* f, int64_t Nf,
             for (int co = 0; co < Cout; ++co) db[co] += dY[i * Cout + co];
     }
 }
+
+/*
+ * Space-filling-curve codes of voxel coordinates ("Contribution Tasks —
+ * JeffreyXiang/FlexGEMM", §二 module table, kernels.cuda.serialize:
+ * z_order_encode/decode and hilbert_encode/decode, with a CPU and a CUDA path;
+ * ops.serialize encode_seq/decode_seq with mode 'z_order' or 'hilbert').  The
+ * pages give the names only.  Readings taken: a code packs the batch index above
+ * 3*bits curve bits, code = (b << 3*bits) | c(x, y, z), for coordinates in
+ * [0, 2^bits).
+ *  - z-order: bit j of x, y, z goes to bit 3j+2, 3j+1, 3j of c.
+ *  - Hilbert: the curve of J. Skilling, "Programming the Hilbert curve" (AIP
+ *    Conf. Proc. 707, 2004).  The coordinates are turned into the curve's
+ *    "transposed" index -- from the top level down, each level's excess
+ *    rotation/reflection is undone, then the words are Gray-coded -- and the
+ *    transposed words are read out most significant level first, x before y
+ *    before z, three bits per level.  Decoding runs those steps backwards.
+ */
+static uint64_t zorder_code(uint32_t x, uint32_t y, uint32_t z, int bits)
+{
+    uint64_t c = 0;
+    for (int j = 0; j < bits; ++j) {
+        c |= (uint64_t)((x >> j) & 1u) << (3 * j + 2);
+        c |= (uint64_t)((y >> j) & 1u) << (3 * j + 1);
+        c |= (uint64_t)((z >> j) & 1u) << (3 * j);
+    }
+    return c;
+}
+
+static void zorder_cell(uint64_t c, int bits, uint32_t* x, uint32_t* y, uint32_t* z)
+{
+    *x = *y = *z = 0;
+    for (int j = 0; j < bits; ++j) {
+        *x |= (uint32_t)((c >> (3 * j + 2)) & 1u) << j;
+        *y |= (uint32_t)((c >> (3 * j + 1)) & 1u) << j;
+        *z |= (uint32_t)((c >> (3 * j)) & 1u) << j;
+    }
+}
+
+/* Skilling's AxesToTranspose for three axes. */
+static void hilbert_to_transpose(uint32_t w[3], int bits)
+{
+    const uint32_t top = 1u << (bits - 1);
+    for (uint32_t q = top; q > 1; q >>= 1) {          /* undo excess work, top level first */
+        const uint32_t p = q - 1;
+        for (int i = 0; i < 3; ++i) {
+            if (w[i] & q) {
+                w[0] ^= p;                             /* invert the low bits of axis 0 */
+            } else {
+                const uint32_t t = (w[0] ^ w[i]) & p;  /* exchange low bits of axes 0 and i */
+                w[0] ^= t;
+                w[i] ^= t;
+            }
+        }
+    }
+    for (int i = 1; i < 3; ++i) w[i] ^= w[i - 1];      /* Gray encode */
+    uint32_t t = 0;
+    for (uint32_t q = top; q > 1; q >>= 1)
+        if (w[2] & q) t ^= q - 1;
+    for (int i = 0; i < 3; ++i) w[i] ^= t;
+}
+
+/* Skilling's TransposeToAxes for three axes (the inverse of the above). */
+static void hilbert_from_transpose(uint32_t w[3], int bits)
+{
+    const uint32_t end = 2u << (bits - 1);
+    uint32_t t = w[2] >> 1;                            /* Gray decode */
+    for (int i = 2; i > 0; --i) w[i] ^= w[i - 1];
+    w[0] ^= t;
+    for (uint32_t q = 2; q != end; q <<= 1) {          /* redo the work, bottom level first */
+        const uint32_t p = q - 1;
+        for (int i = 2; i >= 0; --i) {
+            if (w[i] & q) {
+                w[0] ^= p;
+            } else {
+                t = (w[0] ^ w[i]) & p;
+                w[0] ^= t;
+                w[i] ^= t;
+            }
+        }
+    }
+}
+
+static uint64_t hilbert_code(uint32_t x, uint32_t y, uint32_t z, int bits)
+{
+    if (bits == 0) return 0;
+    uint32_t w[3] = {x, y, z};
+    hilbert_to_transpose(w, bits);
+    uint64_t c = 0;
+    for (int j = bits - 1; j >= 0; --j)
+        for (int i = 0; i < 3; ++i) c = (c << 1) | ((w[i] >> j) & 1u);
+    return c;
+}
+
+static void hilbert_cell(uint64_t c, int bits, uint32_t* x, uint32_t* y, uint32_t* z)
+{
+    uint32_t w[3] = {0, 0, 0};
+    if (bits > 0) {
+        int pos = 3 * bits - 1;                        /* bit of c being read, most significant first */
+        for (int j = bits - 1; j >= 0; --j)
+            for (int i = 0; i < 3; ++i, --pos) w[i] |= (uint32_t)((c >> pos) & 1u) << j;
+        hilbert_from_transpose(w, bits);
+    }
+    *x = w[0];
+    *y = w[1];
+    *z = w[2];
+}
+
+/* codes[i] = (b << 3*bits) | curve(x, y, z) of coords[i] = (b, x, y, z); curve 0 =
+ * z-order, 1 = Hilbert.  Returns ORACLE_BAD_ARG for bits outside [0, 20] or a
+ * coordinate outside [0, 2^bits) (negative b included). */
+int oracle_curve_encode(const int32_t* coords, int64_t N, int bits, int curve, uint64_t* codes)
+{
+    if (bits < 0 || bits > 20 || N < 0) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        if (c[0] < 0) return ORACLE_BAD_ARG;
+        for (int a = 1; a < 4; ++a)
+            if (c[a] < 0 || (int64_t)c[a] >= ((int64_t)1 << bits)) return ORACLE_BAD_ARG;
+        const uint64_t h = curve ? hilbert_code((uint32_t)c[1], (uint32_t)c[2], (uint32_t)c[3], bits)
+                                 : zorder_code((uint32_t)c[1], (uint32_t)c[2], (uint32_t)c[3], bits);
+        codes[i] = ((uint64_t)c[0] << (3 * bits)) | h;
+    }
+    return ORACLE_OK;
+}
+
+/* The inverse: coords[i] = (b, x, y, z) of codes[i]. */
+int oracle_curve_decode(const uint64_t* codes, int64_t N, int bits, int curve, int32_t* coords)
+{
+    if (bits < 0 || bits > 20 || N < 0) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < N; ++i) {
+        const uint64_t low = bits ? codes[i] & ((((uint64_t)1) << (3 * bits)) - 1) : 0;
+        uint32_t x, y, z;
+        if (curve) hilbert_cell(low, bits, &x, &y, &z);
+        else zorder_cell(low, bits, &x, &y, &z);
+        coords[4 * i + 0] = (int32_t)(codes[i] >> (3 * bits));
+        coords[4 * i + 1] = (int32_t)x;
+        coords[4 * i + 2] = (int32_t)y;
+        coords[4 * i + 3] = (int32_t)z;
+    }
+    return ORACLE_OK;
+}

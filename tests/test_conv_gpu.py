@@ -290,3 +290,50 @@ def test_tf32_flag_falls_back_to_ffma_for_other_channels():
     assert ops.vg_conv_describe(coords.shape[0], 24, 40, torch.float32, ops.VG_ALLOW_TF32)["tensor_core"] == 0
     full_check(coords, (1, 12, 12, 12), f, W, b, dY, TOL["f32"], flags=ops.VG_ALLOW_TF32)
 
+
+# ---------------------------------------------------------------- small-N forward (tap groups)
+@pytest.mark.parametrize("dtype,c,n", [("bf16", 256, 2000), ("f16", 64, 900), ("f32", 128, 1500)])
+def test_small_n_split_matches_oracle_and_unsplit(dtype, c, n):
+    # few voxels: fewer (tile, channel block) units than SMs, so the forward and the
+    # input gradient cut each unit's taps into groups summed by a second kernel
+    coords = synth.random_coords(c + n, n, 1, 20, 20, 20)
+    N = coords.shape[0]
+    flags = ops.VG_ALLOW_TF32 if dtype == "f32" else 0
+    d_split = ops.vg_conv_describe(N, c, c, synth.torch_dtype(dtype), flags)
+    d_plain = ops.vg_conv_describe(N, c, c, synth.torch_dtype(dtype), flags | ops.VG_NO_SMALL_N_SPLIT)
+    assert d_split["launches_fwd"] == 3 and d_plain["launches_fwd"] == 2
+    wl = synth.Workload("t", 1, 20, 0, ("sphere",), c, c, dtype, 15, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, N)
+    tol = TF32_TOL if dtype == "f32" else TOL[dtype]
+    errs = full_check(coords, (1, 20, 20, 20), f, W, b, dY, tol, flags=flags)
+    r_plain = run_gpu(coords, (1, 20, 20, 20), f, W, b, dY, flags=flags | ops.VG_NO_SMALL_N_SPLIT)
+    r_split = run_gpu(coords, (1, 20, 20, 20), f, W, b, dY, flags=flags)
+    for k in ("out", "dX"):
+        assert rel_fro(f64(r_split[k]), f64(r_plain[k])) <= tol, (k, errs)
+    # the split pass is deterministic: the same bits twice
+    r_again = run_gpu(coords, (1, 20, 20, 20), f, W, b, dY, flags=flags)
+    for k in ("out", "dX"):
+        assert torch.equal(r_again[k], r_split[k]), k
+
+
+
+def test_hilbert_row_order_gives_the_same_convolution():
+    # the row order only changes the schedule: results stay within the dtype bound of
+    # the oracle (sampled rows and dW entries at full size)
+    name = "b2_r256_shapes_c128_bf16"
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    N = coords.shape[0]
+    nbr_ref, _ = oracle_map(name)
+    f, W, b, dY = synth.make_tensors(wl, N)
+    r = run_gpu(coords, wl.grid, f, W, b, dY, wl.key_flag | ops.VG_ORDER_HILBERT)
+    rng = np.random.default_rng(99)
+    rows = np.sort(rng.choice(N, size=2048, replace=False))
+    cols = np.sort(rng.choice(wl.cout, size=32, replace=False))
+    e_out = rel_fro(f64(r["out"][rows][:, cols]), oracle_fwd_rows(nbr_ref, rows, cols, f, W, b))
+    e_dx = rel_fro(f64(r["dX"][rows][:, cols]), oracle_dgrad_rows(nbr_ref, rows, cols, dY, W))
+    ci = np.sort(rng.choice(wl.cin, size=8, replace=False))
+    co = np.sort(rng.choice(wl.cout, size=8, replace=False))
+    dW_ref, _ = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
+    e_dw = rel_fro(f64(r["dW"][:, ci][:, :, co]), dW_ref)
+    assert max(e_out, e_dx, e_dw) <= TOL[wl.dtype], (e_out, e_dx, e_dw)

@@ -138,3 +138,70 @@ def test_bad_map_blocks_the_convolution():
     ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, None, out, ws)
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)
+
+
+# ---------------------------------------------------------------- serialisation (z-order / Hilbert)
+@pytest.mark.parametrize("mode", [ops.VG_CURVE_ZORDER, ops.VG_CURVE_HILBERT])
+@pytest.mark.parametrize("bits", [0, 1, 5, 10, 20])
+def test_encode_decode_seq_bit_exact(mode, bits):
+    rng = np.random.default_rng(bits * 3 + mode)
+    n = 20000
+    b = rng.integers(0, 5, (n, 1))
+    xyz = rng.integers(0, 1 << bits, (n, 3))
+    c = np.concatenate([b, xyz], 1).astype(np.int32)
+    codes = torch.empty(n, dtype=torch.int64, device="cuda")
+    ops.vg_encode_seq(torch.from_numpy(c).cuda(), bits, mode, codes)
+    ref = oracle.curve_encode(c, bits, mode)
+    assert np.array_equal(codes.cpu().numpy().view(np.uint64), ref)
+    back = torch.empty(n, 4, dtype=torch.int32, device="cuda")
+    ops.vg_decode_seq(codes, bits, mode, back)
+    assert np.array_equal(back.cpu().numpy(), c)
+
+
+def test_encode_seq_marks_out_of_range_rows():
+    c = np.array([[0, 8, 0, 0], [0, 1, 2, 3], [-1, 0, 0, 0]], np.int32)
+    codes = torch.empty(3, dtype=torch.int64, device="cuda")
+    ops.vg_encode_seq(torch.from_numpy(c).cuda(), 3, ops.VG_CURVE_HILBERT, codes)
+    got = codes.cpu().numpy().view(np.uint64)
+    assert got[0] == np.uint64(0xFFFFFFFFFFFFFFFF) and got[2] == np.uint64(0xFFFFFFFFFFFFFFFF)
+    assert got[1] == oracle.curve_encode(c[1:2], 3, oracle.HILBERT)[0]
+
+
+def hilbert_order_keys(coords, mask, grid):
+    """The documented sort key with the Hilbert code (from the oracle) in place of Morton."""
+    B, X, Y, Z = grid
+    L = int(np.ceil(np.log2(max(X, Y, Z)))) if max(X, Y, Z) > 1 else 0
+    m = oracle.curve_encode(coords, L, oracle.HILBERT)
+    lb = int(np.ceil(np.log2(B))) if B > 1 else 0
+    F = min(3 * L, 30)
+    G = min(F, 6)
+    coarse = lb + 3 * L - F
+    if coarse + 27 + G > 32 and coarse + 27 <= 32:
+        G = 32 - 27 - coarse
+    F, G = np.uint64(F), np.uint64(G)
+    fine = (m & ((np.uint64(1) << F) - np.uint64(1))) >> (F - G)
+    return ((m >> F) << (np.uint64(27) + G)) | (mask.astype(np.uint64) << G) | fine
+
+
+@pytest.mark.parametrize("name", ["b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16"])
+def test_hilbert_row_order(name):
+    # VG_ORDER_HILBERT leaves the map unchanged and sorts the rows by the Hilbert key
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    nbr_ref, mask_ref = oracle_map(name)
+    m, st = gpu_map(coords, wl.grid, wl.key_flag | ops.VG_ORDER_HILBERT)
+    assert st == ops.VG_OK
+    assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
+    order = u32(m.sorted_idx()).astype(np.int64)
+    n = coords.shape[0]
+    assert np.array_equal(np.sort(order), np.arange(n))
+    keys = hilbert_order_keys(coords, mask_ref, wl.grid)[order]
+    assert np.all(keys[1:] >= keys[:-1])
+    ties = keys[1:] == keys[:-1]
+    assert np.all(order[1:][ties] > order[:-1][ties])
+    T = (n + 127) // 128
+    pad = np.zeros(T * 128, dtype=np.uint32)
+    pad[:n] = mask_ref[order]
+    assert np.array_equal(u32(m.tile_mask()), np.bitwise_or.reduce(pad.reshape(T, 128), axis=1))
+    sn = u32(m.sorted_nbr())
+    assert np.array_equal(sn[:n], nbr_ref[order]) and np.all(sn[n:] == 0xFFFFFFFF)

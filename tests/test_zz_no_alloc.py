@@ -51,8 +51,11 @@ def test_noalloc_matches_fwd_on_two_calls(cin, cout, dtype):
     for seed in (1, 2):  # two calls in a row, different inputs
         coords, m, f, W, b = _case(seed * 31 + cin, cin, cout, dtype)
         ref = torch.empty(f.shape[0], cout, dtype=f.dtype, device="cuda")
-        ws = ops.conv_workspace(f.shape[0], cin, cout, f.dtype)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, ref, ws)
+        # the workspace forward in the same schedule (one unit per tile and channel
+        # block; the no-allocation forward has no room for split partial sums)
+        fl = ops.VG_NO_SMALL_N_SPLIT
+        ws = ops.conv_workspace(f.shape[0], cin, cout, f.dtype, flags=fl)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, ref, ws, flags=fl)
         out = torch.full_like(ref, float("nan"))
         assert _noalloc_raw(m, f, W, b, out) == ops.VG_OK
         assert _noalloc_status() == ops.VG_OK

@@ -52,6 +52,7 @@ struct NbrLayout {
     size_t off_status = 0, off_tickets = 0;
     size_t off_torder = 0, off_tkey_a = 0, off_tkey_b = 0, off_torder_b = 0;  // tile region sort
     int sms = 0;             // SM count the sort grid is sized for
+    int curve = 0;           // curve of the row order: 0 z-order (Morton), 1 Hilbert
     int tile_passes = 1;     // radix passes of the tile region sort
     int64_t tile_blocks = 1; // blocks of one tile-sort pass
 };

@@ -43,6 +43,7 @@ constexpr int kBM = 128;               // rows per tile (MMA M)
 constexpr int kKBytes = 128;           // bytes of one K block of a row (64 16-bit or 32 fp32 values)
 constexpr int kABytes = kBM * kKBytes;  // 16 KB
 constexpr int kMaxBiasCols = 2048;     // 16-bit bias staged in shared memory up to this many columns
+constexpr int kMaxTapGroups = 6;      // most tap groups per (tile, N block) at small N
 
 // Element types of the kernel: A, B, bias and output share one.
 constexpr int kF16 = VG_F16, kBF16 = VG_BF16, kTF32 = VG_F32;
@@ -82,8 +83,23 @@ struct TcArgs {
     const void* bias;     // [Ndim] or null
     uint8_t* out;         // [n][Ndim]
     int Ndim;
+    int ksplit;           // tap groups per (tile, N block); > 1: fp32 partials, reduced by a second kernel
+    float* partial;       // [ksplit][num_tiles*128][Ndim] when ksplit > 1
     uint32_t* err;
 };
+
+// Taps of group ks (of ks_count) of a tile's tap mask: its set bits, in order,
+// cut into ks_count runs of near-equal length (run g holds the j-th set bit when
+// floor(j * ks_count / popcount) = g).  ks_count = 1: the whole mask.
+__device__ __forceinline__ uint32_t tap_group(uint32_t tm, int ks, int ks_count) {
+    if (ks_count == 1) return tm;
+    const int c = __popc(tm);
+    uint32_t out = 0;
+    int j = 0;
+    for (uint32_t m = tm; m != 0u; m &= m - 1u, ++j)
+        if (j * ks_count / c == ks) out |= m & (0u - m);
+    return out;
+}
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -189,9 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
     const uint32_t tmem = *s_tmem;
 
     const int NB = a.Ndim / BN;
+    const int KS = a.ksplit;
     const int64_t a_row_bytes = (int64_t)a.Kdim * ES;
     const int KB = (int)(a_row_bytes / kKBytes);
-    const int64_t units = a.num_tiles * NB;
+    // unit u = (tile t, N block nb, tap group ks), u = (t * NB + nb) * KS + ks
+    const int64_t per_tile = (int64_t)NB * KS;
+    const int64_t units = a.num_tiles * per_tile;
+    auto unit_taps = [&](int64_t uu) {
+        const int64_t t = uu / per_tile;
+        return tap_group(a.tile_mask[t], (int)(uu % KS), KS);
+    };
 
     if (warp < 4) {
         // ------------------------------------------------------------ gather producer
@@ -206,18 +229,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         int64_t u = blockIdx.x;
         if (p == 0 && u < units) {
             mbar_arrive_expect_tx(nbar0, tile_bytes);
-            bulk_g2s(smem_u32(s_nbr), a.sorted_nbr + (u / NB) * kBM * kTaps, tile_bytes, nbar0);
+            bulk_g2s(smem_u32(s_nbr), a.sorted_nbr + (u / per_tile) * kBM * kTaps, tile_bytes, nbar0);
         }
-        uint32_t tm_next = u < units ? a.tile_mask[u / NB] : 0u;
+        uint32_t tm_next = u < units ? unit_taps(u) : 0u;
         for (; u < units; u += gridDim.x, ++idx) {
             const uint32_t buf = idx & 1u;
             const uint32_t tm = tm_next;
             const int64_t un = u + gridDim.x;
             if (un < units) {
-                tm_next = a.tile_mask[un / NB];
+                tm_next = unit_taps(un);
                 if (p == 0) {  // buffer buf^1 was released by the named barrier that ended the previous unit
                     mbar_arrive_expect_tx(nbar0 + 8 * (buf ^ 1u), tile_bytes);
-                    bulk_g2s(smem_u32(s_nbr + (buf ^ 1u) * kBM * kTaps), a.sorted_nbr + (un / NB) * kBM * kTaps,
+                    bulk_g2s(smem_u32(s_nbr + (buf ^ 1u) * kBM * kTaps), a.sorted_nbr + (un / per_tile) * kBM * kTaps,
                              tile_bytes, nbar0 + 8 * (buf ^ 1u));
                 }
             }
@@ -276,12 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             constexpr uint32_t idesc = DT == kTF32 ? idesc_tf32(BN) : idesc_f16(DT == kBF16, BN);
             uint32_t it = 0, ua = 0;
             bool ok = true;
-            uint32_t tm_next = (int64_t)blockIdx.x < units ? a.tile_mask[blockIdx.x / NB] : 0u;
-            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
-                const uint32_t buf = ua % NBUF;
+            uint32_t tm_next = (int64_t)blockIdx.x < units ? unit_taps(blockIdx.x) : 0u;
+            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const uint32_t tm = tm_next;
-                if (u + gridDim.x < units) tm_next = a.tile_mask[(u + gridDim.x) / NB];
-                if (!mbar_wait(tempty0 + 8 * buf, ((ua / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
+                if (u + gridDim.x < units) tm_next = unit_taps(u + gridDim.x);
+                if (tm == 0u) continue;  // an empty tap group (split units only): no accumulator used
+                const uint32_t uc = ua++;
+                const uint32_t buf = uc % NBUF;
+                if (!mbar_wait(tempty0 + 8 * buf, ((uc / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * BN;
                 uint32_t acc = 0;
@@ -331,30 +356,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
         int64_t u = blockIdx.x;
         // output row of this thread for the next unit, loaded one unit ahead
         uint32_t v_next = kNone;
-        if (u < units) {
-            const int64_t r = (u / NB) * kBM + q * 32 + lane;
+        if (u < units && KS == 1) {
+            const int64_t r = (u / per_tile) * kBM + q * 32 + lane;
             v_next = r < a.n ? a.sorted_idx[r] : kNone;
         }
-        for (; u < units; u += gridDim.x, ++ua) {
-            const int64_t t = u / NB;
-            const int nb = (int)(u - t * NB);
-            const uint32_t buf = ua % NBUF;
+        const int64_t rows_pad = a.num_tiles * kBM;
+        for (; u < units; u += gridDim.x) {
+            const int64_t t = u / per_tile;
+            const int nb = (int)((u % per_tile) / KS);
+            const int ks = (int)(u % KS);
             const uint32_t v = v_next;
-            if (u + gridDim.x < units) {
-                const int64_t r = ((u + gridDim.x) / NB) * kBM + q * 32 + lane;
+            if (u + gridDim.x < units && KS == 1) {
+                const int64_t r = ((u + gridDim.x) / per_tile) * kBM + q * 32 + lane;
                 v_next = r < a.n ? a.sorted_idx[r] : kNone;
             }
+            const int col0 = nb * BN;
+            // split units write fp32 partials for every row of the tile, in sorted order
+            float* prow = KS > 1 ? a.partial + ((int64_t)ks * rows_pad + t * kBM + q * 32 + lane) * a.Ndim + col0
+                                 : nullptr;
+            if (KS > 1 && unit_taps(u) == 0u) {  // empty tap group: its partial is zero
+                for (int c = 0; c < BN; c += 4)
+                    *reinterpret_cast<float4*>(prow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                continue;
+            }
+            const uint32_t buf = ua % NBUF;
             ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua / NBUF) & 1u, s_abort));
+            ++ua;
             if (!ok) break;  // warp-uniform
             tc_fence_after();
-            const int col0 = nb * BN;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
                 tmem_ld_wait();
-                if (v != kNone)
+                if (KS > 1) {
+                    float4* d4 = reinterpret_cast<float4*>(prow + c0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
+                                            __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
+                } else if (v != kNone) {
                     store_row32<DT>(a.out + ((int64_t)v * a.Ndim + col0 + c0) * ES, acc, s_bias, a.bias, col0 + c0);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -372,9 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
             uint32_t it = 0;
             bool ok = true;
             for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const int64_t t = u / NB;
-                const int nb = (int)(u - t * NB);
-                const uint32_t tm = a.tile_mask[t];
+                const int nb = (int)((u % per_tile) / KS);
+                const uint32_t tm = unit_taps(u);
                 for (int k = 0; k < kTaps && ok; ++k) {
                     if (!((tm >> k) & 1u)) continue;
                     const uint8_t* bsrc = a.Bimg + ((int64_t)nb * kTaps + k) * KB * C::kBBytes;
@@ -454,13 +496,64 @@ int launch_tc(const TcArgs& a, cudaStream_t s) {
     auto kern = k_gather_gemm_tc<BN, DT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
-    const int64_t units = a.num_tiles * (a.Ndim / BN);
+    const int64_t units = a.num_tiles * (a.Ndim / BN) * a.ksplit;
     const int grid = (int)std::min<int64_t>(units, plan_sms(0));
     kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
 
+// Forward / input-gradient with tap-group units: the fixed-order sum of the
+// groups' fp32 partials (group 0 first), + bias, rounded once, written to the
+// caller's row order through sorted_idx.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_split_reduce(const float* __restrict__ partial, int ks_count, int64_t rows_pad, int64_t n, int Ndim,
+               const uint32_t* __restrict__ sorted_idx, const T* __restrict__ bias, T* __restrict__ out,
+               const uint32_t* __restrict__ nbr_status) {
+    if (*nbr_status) return;
+    const int c4n = Ndim / 4;
+    const int64_t total = n * c4n;
+    for (int64_t e = (int64_t)blockIdx.x * 256 + threadIdx.x; e < total; e += (int64_t)gridDim.x * 256) {
+        const int64_t r = e / c4n;
+        const int c = (int)(e - r * c4n) * 4;
+        float4 acc = *reinterpret_cast<const float4*>(partial + r * Ndim + c);
+        for (int g = 1; g < ks_count; ++g) {
+            const float4 v = *reinterpret_cast<const float4*>(partial + ((int64_t)g * rows_pad + r) * Ndim + c);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (bias) {
+            acc.x += to_f32(bias[c]);
+            acc.y += to_f32(bias[c + 1]);
+            acc.z += to_f32(bias[c + 2]);
+            acc.w += to_f32(bias[c + 3]);
+        }
+        T* dst = out + (int64_t)sorted_idx[r] * Ndim + c;
+        dst[0] = from_f32<T>(acc.x);
+        dst[1] = from_f32<T>(acc.y);
+        dst[2] = from_f32<T>(acc.z);
+        dst[3] = from_f32<T>(acc.w);
+    }
+}
+
+template <typename T>
+void launch_split_reduce(const TcArgs& a, int sms, cudaStream_t s) {
+    const int64_t total = a.n * (a.Ndim / 4);
+    const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 8 * (int64_t)sms));
+    k_split_reduce<T><<<blocks, 256, 0, s>>>(a.partial, a.ksplit, a.num_tiles * kBM, a.n, a.Ndim, a.sorted_idx,
+                                             static_cast<const T*>(a.bias), reinterpret_cast<T*>(a.out),
+                                             a.nbr_status);
+}
+
 }  // namespace
+
+int tc_gather_splits(int64_t n, int Ndim, int sms) {
+    const int64_t units = (n + kBM - 1) / kBM * (Ndim / choose_bn(Ndim));
+    if (units == 0 || units >= sms) return 1;
+    return (int)std::min<int64_t>(kMaxTapGroups, (sms + units - 1) / units);
+}
 
 int tc_supported(int dtype, int Cin, int Cout) {
     return (dtype == VG_F16 || dtype == VG_BF16) && Cin % 64 == 0 && Cout % 64 == 0 ? 1 : 0;
@@ -505,25 +598,37 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     a.bias = p.bias;
     a.out = static_cast<uint8_t*>(p.out);
     a.Ndim = p.Ndim;
+    a.ksplit = p.ksplit > 1 ? p.ksplit : 1;
+    a.partial = p.partial;
     a.err = p.err;
+    if (a.ksplit > 1 && !a.partial) return VG_ERR_INVALID_ARG;
     const int bn = choose_bn(p.Ndim);
+    int st;
     if (p.dtype == VG_F32) {
         switch (bn) {
-            case 256: return launch_tc<256, kTF32>(a, s);
-            case 128: return launch_tc<128, kTF32>(a, s);
-            case 64: return launch_tc<64, kTF32>(a, s);
-            default: return launch_tc<32, kTF32>(a, s);
+            case 256: st = launch_tc<256, kTF32>(a, s); break;
+            case 128: st = launch_tc<128, kTF32>(a, s); break;
+            case 64: st = launch_tc<64, kTF32>(a, s); break;
+            default: st = launch_tc<32, kTF32>(a, s); break;
+        }
+    } else {
+        if (bn < 64) return VG_ERR_UNSUPPORTED;
+        const bool bf16 = p.dtype == VG_BF16;
+        switch (bn) {
+            case 256: st = bf16 ? launch_tc<256, kBF16>(a, s) : launch_tc<256, kF16>(a, s); break;
+            case 128: st = bf16 ? launch_tc<128, kBF16>(a, s) : launch_tc<128, kF16>(a, s); break;
+            default: st = bf16 ? launch_tc<64, kBF16>(a, s) : launch_tc<64, kF16>(a, s); break;
         }
     }
-    if (bn < 64) return VG_ERR_UNSUPPORTED;
-    const bool bf16 = p.dtype == VG_BF16;
-    switch (bn) {
-        case 256: return bf16 ? launch_tc<256, kBF16>(a, s) : launch_tc<256, kF16>(a, s);
-        case 128: return bf16 ? launch_tc<128, kBF16>(a, s) : launch_tc<128, kF16>(a, s);
-        default: return bf16 ? launch_tc<64, kBF16>(a, s) : launch_tc<64, kF16>(a, s);
-    }
+    if (st != VG_OK || a.ksplit == 1) return st;
+    const int sms = plan_sms(0);
+    if (p.dtype == VG_F32) launch_split_reduce<float>(a, sms, s);
+    else if (p.dtype == VG_BF16) launch_split_reduce<__nv_bfloat16>(a, sms, s);
+    else launch_split_reduce<__half>(a, sms, s);
+    return VG_OK;
 }
 
-int tc_fwd_launches() { return 2; }  // weight repack, gather GEMM
+// weight repack, gather GEMM (+ the split reduce when the pass is cut into tap groups)
+int tc_fwd_launches(int ksplit) { return ksplit > 1 ? 3 : 2; }
 
 }  // namespace vg

@@ -56,6 +56,10 @@ struct GatherPass {
     int Ndim;
     int dtype;
     uint32_t* err;               // conv workspace error word
+    // tensor-core path: tap groups per (tile, N block) (tc_gather_splits); > 1 needs
+    // `partial`, [ksplit][ceil(n/128)*128][Ndim] fp32 of scratch
+    int ksplit = 1;
+    float* partial = nullptr;
 };
 
 int simt_gather_pass(const GatherPass& p, cudaStream_t s);
@@ -94,6 +98,10 @@ int dbias_blocks(int64_t n, int sms);
 void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s);
 
+// Space-filling-curve codes (curve 0 = z-order, 1 = Hilbert) of (b,x,y,z) rows and back.
+int curve_encode(const int32_t* coords, int64_t n, int bits, int curve, uint64_t* codes, cudaStream_t s);
+int curve_decode(const uint64_t* codes, int64_t n, int bits, int curve, int32_t* coords, cudaStream_t s);
+
 // out = sum of parts[0..nparts) in index order with fp32 adds, rounded once (any dtype).
 int launch_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, void* out, int sms,
                        cudaStream_t s);
@@ -113,7 +121,11 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s);
 // Scratch of the weight gradient: dY rows copied into processing order (zero rows
 // pad the last tile) when Cout takes the wide-N kernel, else 0 bytes.
 size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout);
-int tc_fwd_launches();            // kernels per forward call on the tensor-core path
+// Tap groups per (tile, N block) of a forward or input-gradient pass: 1 when the
+// (tile, N block) units already fill the SMs, else enough to about fill them
+// (at most 6); each group adds n_pad * Ndim * 4 bytes of fp32 partials.
+int tc_gather_splits(int64_t n, int Ndim, int sms);
+int tc_fwd_launches(int ksplit);  // kernels per forward call on the tensor-core path
 int tc_bwd_launches(int Cout);    // kernels per full backward call on the tensor-core path
 
 }  // namespace vg

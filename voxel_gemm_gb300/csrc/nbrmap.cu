@@ -9,6 +9,7 @@
 // kernels.cuda.serialize (z_order_encode) plus ops.utils.init_hashmap (32- or
 // 64-bit keys chosen by grid volume).
 #include "common.cuh"
+#include "curves.cuh"
 #include "internal.h"
 
 namespace vg {
@@ -76,19 +77,17 @@ __global__ void k_insert(const int4* __restrict__ coords, int64_t n, int B, int 
 // the top G fine Morton bits (a 4x4x4 split of the block).  Below that the stable sort keeps
 // the input order; dropping the low Morton bits saves radix passes, and rows with
 // equal masks in one sub-block are gathered alike whatever their order.
-// Morton (z-order) code (b << 3L) | interleave(x, y, z) of a voxel.
-__device__ __forceinline__ uint64_t morton(int4 c, int L) {
-    uint64_t m = (uint64_t)(uint32_t)c.x << (3 * L);
-    for (int b = 0; b < L; ++b) {
-        m |= (uint64_t)(((uint32_t)c.y >> b) & 1u) << (3 * b + 2);
-        m |= (uint64_t)(((uint32_t)c.z >> b) & 1u) << (3 * b + 1);
-        m |= (uint64_t)(((uint32_t)c.w >> b) & 1u) << (3 * b);
-    }
-    return m;
+// Curve code (b << 3L) | curve(x, y, z) of a voxel: the Morton (z-order) code,
+// or the Hilbert code when the build asks for the Hilbert row order (L <= 20
+// whenever the layout is valid).
+__device__ __forceinline__ uint64_t curve_code(int4 c, int L, int curve) {
+    const uint64_t h = curve == kCurveHilbert ? hilbert3((uint32_t)c.y, (uint32_t)c.z, (uint32_t)c.w, L)
+                                              : zorder3((uint32_t)c.y, (uint32_t)c.z, (uint32_t)c.w);
+    return ((uint64_t)(uint32_t)c.x << (3 * L)) | h;
 }
 
-__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L, int G) {
-    const uint64_t m = morton(c, L);
+__device__ __forceinline__ uint64_t order_key(int4 c, uint32_t mask, int L, int G, int curve) {
+    const uint64_t m = curve_code(c, L, curve);
     const int F = min(3 * L, kFineOrderBits);
     const uint64_t fine = (m & ((uint64_t(1) << F) - 1)) >> (F - G);
     return ((m >> F) << (kTaps + G)) | ((uint64_t)mask << G) | fine;
@@ -157,7 +156,8 @@ __device__ __forceinline__ uint32_t row_mask(const uint32_t* __restrict__ row) {
 template <typename SK>
 __global__ void __launch_bounds__(kSortThreads)
 k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ nbr, int64_t n, int L, int G,
-                 int passes, uint32_t* __restrict__ mask, SK* __restrict__ keys, uint32_t* __restrict__ ghist) {
+                 int curve, int passes, uint32_t* __restrict__ mask, SK* __restrict__ keys,
+                 uint32_t* __restrict__ ghist) {
     __shared__ uint32_t h[kMaxSortPasses][kRadix];
     const int t = threadIdx.x;
     for (int p = 0; p < passes; ++p) h[p][t] = 0;
@@ -165,7 +165,7 @@ k_key_globalhist(const int4* __restrict__ coords, const uint32_t* __restrict__ n
     for (int64_t i = (int64_t)blockIdx.x * kSortThreads + t; i < n; i += (int64_t)gridDim.x * kSortThreads) {
         const uint32_t m = row_mask(nbr + i * kTaps);
         mask[i] = m;
-        const SK key = (SK)order_key(coords[i], m, L, G);
+        const SK key = (SK)order_key(coords[i], m, L, G, curve);
         keys[i] = key;
         for (int p = 0; p < passes; ++p) atomicAdd(&h[p][(uint32_t)(key >> (p * kRadixBits)) & (kRadix - 1)], 1u);
     }
@@ -329,7 +329,7 @@ k_onesweep(const SK* __restrict__ kin, const uint32_t* __restrict__ vin, SK* __r
 __global__ void __launch_bounds__(kTileRows)
 k_tile_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
             const uint32_t* __restrict__ mask, int64_t n, uint32_t* __restrict__ tmask,
-            uint32_t* __restrict__ sorted_nbr, const int4* __restrict__ coords, int L, int G,
+            uint32_t* __restrict__ sorted_nbr, const int4* __restrict__ coords, int L, int G, int curve,
             int tile_passes, uint32_t* __restrict__ tkey, uint32_t* __restrict__ thist,
             uint32_t* __restrict__ torder) {
     __shared__ uint32_t rows[kTileRows];
@@ -349,7 +349,7 @@ k_tile_rows(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict_
             torder[blockIdx.x] = blockIdx.x;
         } else {
             const int F = min(3 * L, kFineOrderBits);
-            const uint32_t key = (uint32_t)(morton(coords[rows[0]], L) >> (F - G));  // rows[0] < n always
+            const uint32_t key = (uint32_t)(curve_code(coords[rows[0]], L, curve) >> (F - G));  // rows[0] < n always
             tkey[blockIdx.x] = key;
             for (int p = 0; p < tile_passes; ++p)
                 atomicAdd(&thist[p * kRadix + ((key >> (p * kRadixBits)) & (kRadix - 1))], 1u);
@@ -373,12 +373,13 @@ static int ceil_log2(int64_t v) {
 int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sms, NbrLayout* L) {
     if (N < 0 || N >= (int64_t(1) << 31) || B <= 0 || X <= 0 || Y <= 0 || Z <= 0) return VG_ERR_INVALID_ARG;
     if ((flags & VG_KEY32) && (flags & VG_KEY64)) return VG_ERR_INVALID_ARG;
-    if (flags & ~(VG_KEY32 | VG_KEY64 | VG_TEST_SMALL_HASH)) return VG_ERR_INVALID_ARG;
+    if (flags & ~(VG_KEY32 | VG_KEY64 | VG_ORDER_HILBERT | VG_TEST_SMALL_HASH)) return VG_ERR_INVALID_ARG;
     const double vol = (double)B * X * Y * Z;
     if (vol >= 18446744073709551615.0) return VG_ERR_UNSUPPORTED;
     NbrLayout l;
     l.n = N;
     l.sms = plan_sms(sms);
+    l.curve = (flags & VG_ORDER_HILBERT) ? kCurveHilbert : kCurveZOrder;
     if (flags & VG_KEY64) l.key64 = 1;
     else if (flags & VG_KEY32) {
         if (vol > 4294967294.0) return VG_ERR_INVALID_ARG;  // all-ones is the empty-slot marker
@@ -479,7 +480,8 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
     const int64_t sblocks = std::max(l.sort_blocks, l.tile_blocks);
     cudaMemsetAsync(hist, 0, l.off_tickets + 4 * (size_t)all - l.off_hist, s);  // counts, status, tickets
     const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * (int64_t)l.sms);
-    k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, passes, mask, ka, hist);
+    k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, l.curve, passes, mask,
+                                                            ka, hist);
     const uint32_t* vin = nullptr;
     const size_t smem = (size_t)kSortThreads * l.sort_items * (sizeof(SK) + 4);
     cudaFuncSetAttribute(k_onesweep<SK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -499,7 +501,7 @@ static void launch_build(const int4* coords, const NbrLayout& l, int B, int X, i
     uint32_t* to1 = reinterpret_cast<uint32_t*>(ws + l.off_torder_b);
     k_tile_rows<<<(unsigned)l.num_tiles, kTileRows, 0, s>>>(
         v0, nbr, mask, n, reinterpret_cast<uint32_t*>(ws + l.off_tmask),
-        reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted), coords, L, l.fine_keep, l.tile_passes, tka,
+        reinterpret_cast<uint32_t*>(ws + l.off_nbr_sorted), coords, L, l.fine_keep, l.curve, l.tile_passes, tka,
         hist + passes * kRadix, to0);
     // stable sort of the tiles by region key: the weight gradient's visiting order
     const size_t tsmem = (size_t)kSortThreads * l.sort_items * (sizeof(uint32_t) + 4);

@@ -10,8 +10,10 @@ struct ConvPlan {
     int sms = 0;           // SM count the plan is sized for
     int tensor_core = 0;   // 16-bit tcgen05 path (all three passes)
     int tf32 = 0;          // fp32 forward and input gradient on tcgen05 as TF32 (VG_ALLOW_TF32)
+    int ks_fwd = 1, ks_dgrad = 1;  // tap groups of the tensor-core forward / input gradient (small N)
     int splits = 1;        // split-K chunks of the weight gradient
-    size_t off_err = 0, off_wfwd = 0, off_wbwd = 0, off_partial = 0, off_partial_db = 0, off_dys = 0, total = 0;
+    size_t off_err = 0, off_wfwd = 0, off_wbwd = 0, off_partial = 0, off_partial_db = 0, off_dys = 0;
+    size_t off_gpart = 0, total = 0;
 };
 
 static size_t dtype_size(int dt) { return dt == VG_F32 ? 4 : 2; }
@@ -19,13 +21,20 @@ static size_t dtype_size(int dt) { return dt == VG_F32 ? 4 : 2; }
 static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, int sms, ConvPlan* P) {
     if (N < 0 || N >= (int64_t(1) << 31) || Cin <= 0 || Cout <= 0) return VG_ERR_INVALID_ARG;
     if (dtype != VG_F32 && dtype != VG_F16 && dtype != VG_BF16) return VG_ERR_INVALID_ARG;
-    if (flags & ~VG_ALLOW_TF32) return VG_ERR_UNSUPPORTED;
+    if (flags & ~(VG_ALLOW_TF32 | VG_NO_SMALL_N_SPLIT)) return VG_ERR_UNSUPPORTED;
     if (Cin % 8 || Cout % 8) return VG_ERR_UNSUPPORTED;  // 16-byte rows for every dtype
     ConvPlan p;
     p.sms = plan_sms(sms);
     p.tensor_core = tc_supported(dtype, Cin, Cout);
     p.tf32 = (flags & VG_ALLOW_TF32) && tf32_supported(dtype, Cin, Cout) ? 1 : 0;
     const int packed = p.tensor_core || p.tf32;
+    if (packed && !(flags & VG_NO_SMALL_N_SPLIT)) {
+        p.ks_fwd = tc_gather_splits(N, Cout, p.sms);
+        p.ks_dgrad = tc_gather_splits(N, Cin, p.sms);
+    }
+    const size_t rows_pad = (size_t)((N + 127) / 128) * 128;
+    const size_t gpart = std::max(p.ks_fwd > 1 ? (size_t)p.ks_fwd * rows_pad * Cout * 4 : 0,
+                                  p.ks_dgrad > 1 ? (size_t)p.ks_dgrad * rows_pad * Cin * 4 : 0);
     p.splits = p.tensor_core ? tc_wgrad_splits(N, Cin, Cout, p.sms) : simt_wgrad_splits(N, Cin, Cout, p.sms);
     const size_t wbytes = (size_t)kTaps * Cin * Cout * dtype_size(dtype);
     size_t o = 0;
@@ -35,6 +44,7 @@ static int conv_plan(int64_t N, int Cin, int Cout, int dtype, unsigned flags, in
     p.off_partial = o;     o += align_up((size_t)p.splits * kTaps * Cin * Cout * 4, 256);
     p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N, p.sms) * Cout * 4, 256);
     p.off_dys = o;         o += p.tensor_core ? align_up(tc_wgrad_sorted_dy_bytes(N, Cout), 256) : 0;
+    p.off_gpart = o;       o += align_up(gpart, 256);
     (void)wbytes;
     p.total = o;
     *P = p;
@@ -123,8 +133,9 @@ int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, in
     if (st != VG_OK || !info) return st != VG_OK ? st : VG_ERR_INVALID_ARG;
     info[0] = p.tensor_core ? 1 : (p.tf32 ? 2 : 0);
     info[1] = p.splits;
-    info[2] = N > 0 ? (p.tensor_core || p.tf32 ? tc_fwd_launches() : 1) : 0;
-    info[3] = N > 0 ? (p.tensor_core ? tc_bwd_launches(Cout) : (p.tf32 ? 2 : 1) + 2 + 2) : 0;
+    const int dgrad_launches = p.tensor_core || p.tf32 ? tc_fwd_launches(p.ks_dgrad) : 1;
+    info[2] = N > 0 ? (p.tensor_core || p.tf32 ? tc_fwd_launches(p.ks_fwd) : 1) : 0;
+    info[3] = N > 0 ? (p.tensor_core ? dgrad_launches - 2 + tc_bwd_launches(Cout) : dgrad_launches + 2 + 2) : 0;
     return VG_OK;
 }
 
@@ -167,6 +178,8 @@ int vg_subm_conv3d_fwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
     g.Ndim = Cout;
     g.dtype = dtype;
     g.err = reinterpret_cast<uint32_t*>(ws + p.off_err);
+    g.ksplit = p.ks_fwd;
+    g.partial = reinterpret_cast<float*>(ws + p.off_gpart);
     if (p.tensor_core || p.tf32) {
         st = tc_pack_weights(weight, dtype, Cin, Cout, 0, ws + p.off_wfwd, g.nbr_status, s);
         if (st == VG_OK) st = tc_gather_pass(g, ws + p.off_wfwd, s);
@@ -226,6 +239,8 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         g.Ndim = Cin;
         g.dtype = dtype;
         g.err = err;
+        g.ksplit = p.ks_dgrad;
+        g.partial = reinterpret_cast<float*>(ws + p.off_gpart);
         if (p.tensor_core || p.tf32) {
             st = tc_pack_weights(weight, dtype, Cin, Cout, 1, ws + p.off_wbwd, nbr_status, s);
             if (st == VG_OK) st = tc_gather_pass(g, ws + p.off_wbwd, s);
@@ -260,6 +275,24 @@ int vg_subm_conv3d_bwd(const void* nbr_ws, const uint32_t* nbr, const uint32_t* 
         st = p.tensor_core ? tc_wgrad(w, s) : simt_wgrad(w, s);
         if (st != VG_OK) return st;
     }
+    return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
+}
+
+int vg_encode_seq(const int32_t* coords, int64_t N, int bits, int mode, uint64_t* codes, void* stream) {
+    if (N < 0 || bits < 0 || bits > 20 || (mode != VG_CURVE_ZORDER && mode != VG_CURVE_HILBERT))
+        return VG_ERR_INVALID_ARG;
+    if (N > 0 && (!coords || !codes || misaligned(coords, 16) || misaligned(codes, 8))) return VG_ERR_INVALID_ARG;
+    cudaGetLastError();
+    curve_encode(coords, N, bits, mode, codes, static_cast<cudaStream_t>(stream));
+    return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
+}
+
+int vg_decode_seq(const uint64_t* codes, int64_t N, int bits, int mode, int32_t* coords, void* stream) {
+    if (N < 0 || bits < 0 || bits > 20 || (mode != VG_CURVE_ZORDER && mode != VG_CURVE_HILBERT))
+        return VG_ERR_INVALID_ARG;
+    if (N > 0 && (!coords || !codes || misaligned(coords, 16) || misaligned(codes, 8))) return VG_ERR_INVALID_ARG;
+    cudaGetLastError();
+    curve_decode(codes, N, bits, mode, coords, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? VG_OK : VG_ERR_CUDA;
 }
 

@@ -22,8 +22,9 @@ VG_OK, VG_ERR_INVALID_ARG, VG_ERR_COORD_OUT_OF_RANGE, VG_ERR_DUPLICATE_COORD = 0
 VG_ERR_HASH_FULL, VG_ERR_UNSUPPORTED, VG_ERR_WORKSPACE_TOO_SMALL, VG_ERR_CUDA = 4, 5, 6, 7
 VG_ERR_DEVICE_TIMEOUT = 8
 VG_F32, VG_F16, VG_BF16 = 0, 1, 2
-VG_KEY32, VG_KEY64, VG_TEST_SMALL_HASH = 0x1, 0x2, 0x100
-VG_ALLOW_TF32 = 0x10
+VG_KEY32, VG_KEY64, VG_ORDER_HILBERT, VG_TEST_SMALL_HASH = 0x1, 0x2, 0x4, 0x100
+VG_CURVE_ZORDER, VG_CURVE_HILBERT = 0, 1
+VG_ALLOW_TF32, VG_NO_SMALL_N_SPLIT = 0x10, 0x20
 VG_NONE = 0xFFFFFFFF
 VG_TILE_ROWS = 128
 
@@ -68,6 +69,8 @@ def lib():
             "vg_subm_conv3d_fwd_noalloc": ([P, P, P, I64, I, P, P, P, P, I, I, U, P], I),
             "vg_subm_conv3d_fwd_noalloc_status": ([P], I),
             "vg_sum_ordered": ([P, I, I64, I, P, P], I),
+            "vg_encode_seq": ([P, I64, I, I, P, P], I),
+            "vg_decode_seq": ([P, I64, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -199,6 +202,16 @@ def vg_sum_ordered(parts, out, stream=None) -> None:
         raise ValueError("vg_sum_ordered: parts must be [n, *out.shape], contiguous, of out's dtype")
     _check(lib().vg_sum_ordered(_p(parts), parts.shape[0], out.numel(), _dtype_code(out), _p(out), _s(stream)),
            "vg_sum_ordered")
+
+
+def vg_encode_seq(coords, bits: int, mode: int, codes, stream=None) -> None:
+    """codes[i] (int64 storage of uint64) = (b << 3*bits) | curve(x, y, z) of coords[i]."""
+    _check(lib().vg_encode_seq(_p(coords), coords.shape[0], bits, mode, _p(codes), _s(stream)), "vg_encode_seq")
+
+
+def vg_decode_seq(codes, bits: int, mode: int, coords, stream=None) -> None:
+    """coords[i] = (b, x, y, z) of codes[i] (the inverse of vg_encode_seq)."""
+    _check(lib().vg_decode_seq(_p(codes), codes.shape[0], bits, mode, _p(coords), _s(stream)), "vg_decode_seq")
 
 
 def vg_conv_status(conv_ws, stream=None) -> int:
