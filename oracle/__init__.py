@@ -21,6 +21,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
   dgrad_scatter dense conv3d autograd, adjoint identity
   dgrad_rows    equal to dgrad_scatter (it is a regrouping of the same sum)
   wgrad         dense conv3d autograd (dW and db), central finite differences
+  sparse_map    (regular strided / transposed convolution) dense torch conv3d and
+                conv_transpose3d on the densified grid (outputs, output set,
+                autograd), adjoint identity
+  dgrad_scatter_to  dense conv3d autograd (the strided convolution's input gradient)
   curve_encode / curve_decode (z-order, Hilbert)
                 bijection onto [0, 8^bits) by exhaustion on small cubes, decode is
                 the inverse of encode, z-order's parent/child nesting, Hilbert's
@@ -78,6 +82,10 @@ def _load():
         lib.oracle_dgrad_rows.restype = None
         lib.oracle_wgrad.argtypes = [P, I64, P, I64, P, I, I, P, P]
         lib.oracle_wgrad.restype = None
+        lib.oracle_dgrad_scatter_to.argtypes = [P, I64, P, P, I, I, I64, P]
+        lib.oracle_dgrad_scatter_to.restype = None
+        lib.oracle_sparse_map.argtypes = [P, I64, I, I, I, I, I, I, P, P, P, P]
+        lib.oracle_sparse_map.restype = I
         lib.oracle_curve_encode.argtypes = [P, I64, I, I, P]
         lib.oracle_curve_encode.restype = I
         lib.oracle_curve_decode.argtypes = [P, I64, I, I, P]
@@ -197,4 +205,35 @@ def curve_decode(codes, bits: int, curve: int):
     if rc != OK:
         raise OracleError(rc)
     return out
+
+
+def dgrad_scatter_to(nbr, dY, W, n_x: int):
+    """dX [n_x, Cin] (fp64): every valid pair (i, k) of nbr [R,27] adds W_k dY[i] to dX[nbr[i][k]]."""
+    nbr = np.ascontiguousarray(nbr, dtype=np.uint32)
+    dY = _f64(dY)
+    W = _f64(W)
+    _, cin, cout = W.shape
+    dX = np.empty((n_x, cin), dtype=np.float64)
+    _load().oracle_dgrad_scatter_to(_ptr(nbr), nbr.shape[0], _ptr(dY), _ptr(W), cin, cout, n_x, _ptr(dX))
+    return dX
+
+
+def sparse_map(coords, B: int, X: int, Y: int, Z: int, kernel: int, stride: int):
+    """Regular sparse convolution map: (coords_out int32 [No,4] in ascending linear key,
+    down uint32 [No,27] -> input rows, up uint32 [N,27] -> output rows).  Kernel 2 or 3
+    (padding 0 or 1), stride 1 or 2; taps k >= kernel^3 are absent."""
+    c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 4))
+    n = c.shape[0]
+    T = kernel ** 3
+    cap = max(1, n * T)
+    out = np.empty((cap, 4), dtype=np.int32)
+    down = np.empty((cap, 27), dtype=np.uint32)
+    up = np.empty((max(1, n), 27), dtype=np.uint32)
+    no = ctypes.c_int64(0)
+    rc = _load().oracle_sparse_map(_ptr(c), n, B, X, Y, Z, kernel, stride, ctypes.byref(no), _ptr(out),
+                                   _ptr(down), _ptr(up))
+    if rc != OK:
+        raise OracleError(rc)
+    k = no.value
+    return out[:k].copy(), down[:k].copy(), up[:n].copy()
 

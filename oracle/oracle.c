@@ -402,3 +402,182 @@ int oracle_curve_decode(const uint64_t* codes, int64_t N, int bits, int curve, i
     }
     return ORACLE_OK;
 }
+
+/*
+ * Input gradient by its definition with separate row counts: the R rows of
+ * dY (lists nbr [R][27]) scatter W_k dY[i] into the Nx rows of dX.  The regular
+ * (strided / transposed) convolution below uses it, where the rows of dY and
+ * the rows of dX are different voxel sets.
+ */
+void oracle_dgrad_scatter_to(const uint32_t* nbr, int64_t R, const double* dY, const double* W,
+                             int Cin, int Cout, int64_t Nx, double* dX)
+{
+    memset(dX, 0, (size_t)Nx * Cin * sizeof(double));
+    for (int64_t i = 0; i < R; ++i) {
+        const double* g = dY + i * Cout;
+        for (int k = 0; k < 27; ++k) {
+            uint32_t j = nbr[i * 27 + k];
+            if (j == ORACLE_NONE) continue;
+            double* d = dX + (int64_t)j * Cin;
+            for (int ci = 0; ci < Cin; ++ci) {
+                const double* w = W + ((int64_t)k * Cin + ci) * Cout;
+                double s = 0.0;
+                for (int co = 0; co < Cout; ++co) s += w[co] * g[co];
+                d[ci] += s;
+            }
+        }
+    }
+}
+
+/*
+ * Regular (non-submanifold) sparse convolution map: "Contribution Tasks —
+ * JeffreyXiang/FlexGEMM", §二 module table and key functions (sparse_conv3d,
+ * kernels.cuda.spconv sparse_neighbor_map): the output sites differ from the
+ * input sites (strided down-sampling, and its transposed up-sampling).  The
+ * pages give no formula; the reading taken is the convolution that
+ * torch.nn.functional.conv3d computes on the densified grid, with kernel K per
+ * axis (K = 3: padding 1, taps t - 1 for t in {0,1,2}; K = 2: padding 0, taps
+ * t in {0,1}) and stride s, evaluated only at the output sites whose window
+ * holds at least one active input:
+ *   output grid: Xo = (X + 2p - K) / s + 1 (floor), likewise Yo, Zo, same batch
+ *   tap k = (tx*K + ty)*K + tz  <->  offset d = (tx - p, ty - p, tz - p)
+ *   o is active  iff  some input sits at s*o + d_k
+ *   down[o][k] = input row at s*o + d_k (or NONE); columns k >= K^3 are NONE
+ *   up[j][k]   = output row o with s*o + d_k = coord_j (or NONE)
+ * Output rows are numbered in ascending linear key ((b*Xo + x)*Yo + y)*Zo + z.
+ * The strided convolution is then out[o] = bias + sum_k W_k^T f[down[o][k]];
+ * its input gradient scatters along down (oracle_dgrad_scatter_to) and its
+ * weight gradient is oracle_wgrad over down.  The transposed convolution maps
+ * the output sites back to the input sites: out[j] = bias + sum_k W_k^T
+ * g[up[j][k]] (torch conv_transpose3d with the same K, s, p).
+ * coords_out must hold N * K^3 rows, down N * K^3 rows of 27, up N rows of 27.
+ * Returns ORACLE_BAD_ARG for K not in {2,3}, s not in {1,2} or a grid with no
+ * output cell, ORACLE_OUT_OF_RANGE / ORACLE_DUPLICATE as oracle_nbrmap.
+ */
+typedef struct { uint64_t key; int32_t b, x, y, z; } cand_entry;
+
+static int cmp_cand(const void* a, const void* b)
+{
+    const uint64_t ka = ((const cand_entry*)a)->key, kb = ((const cand_entry*)b)->key;
+    return ka < kb ? -1 : (ka > kb ? 1 : 0);
+}
+
+int oracle_sparse_map(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, int K, int s,
+                      int64_t* N_out, int32_t* coords_out, uint32_t* down, uint32_t* up)
+{
+    if (N < 0 || B <= 0 || X <= 0 || Y <= 0 || Z <= 0) return ORACLE_BAD_ARG;
+    if ((K != 2 && K != 3) || (s != 1 && s != 2)) return ORACLE_BAD_ARG;
+    const int p = K == 3 ? 1 : 0;
+    const int64_t Xo = (X + 2 * p - K) / s + 1, Yo = (Y + 2 * p - K) / s + 1, Zo = (Z + 2 * p - K) / s + 1;
+    if (X + 2 * p < K || Y + 2 * p < K || Z + 2 * p < K) return ORACLE_BAD_ARG;
+    const int T = K * K * K;
+    *N_out = 0;
+    if (N == 0) return ORACLE_OK;
+    /* the input sites, as a dictionary (also rejects bad or repeated coordinates) */
+    uint32_t* nbr_sub = (uint32_t*)malloc((size_t)N * 27 * sizeof(uint32_t));
+    uint32_t* mask_sub = (uint32_t*)malloc((size_t)N * sizeof(uint32_t));
+    dict_entry* din = (dict_entry*)malloc((size_t)N * sizeof(dict_entry));
+    cand_entry* cand = (cand_entry*)malloc((size_t)N * T * sizeof(cand_entry));
+    if (!nbr_sub || !mask_sub || !din || !cand) {
+        free(nbr_sub); free(mask_sub); free(din); free(cand);
+        return ORACLE_NO_MEMORY;
+    }
+    int rc = oracle_nbrmap(coords, N, B, X, Y, Z, nbr_sub, mask_sub);
+    free(nbr_sub);
+    free(mask_sub);
+    if (rc != ORACLE_OK) {
+        free(din); free(cand);
+        return rc;
+    }
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        din[i].key = linear_key(c[0], c[1], c[2], c[3], X, Y, Z);
+        din[i].row = i;
+    }
+    qsort(din, (size_t)N, sizeof(dict_entry), cmp_entry);
+    /* every output whose window holds an input: o = (c - d_k) / s where divisible */
+    int64_t nc = 0;
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        for (int k = 0; k < T; ++k) {
+            const int d[3] = {k / (K * K) - p, (k / K) % K - p, k % K - p};
+            int64_t o[3];
+            int ok = 1;
+            for (int a = 0; a < 3; ++a) {
+                const int64_t v = (int64_t)c[1 + a] - d[a];
+                const int64_t lim = a == 0 ? Xo : (a == 1 ? Yo : Zo);
+                if (v < 0 || v % s != 0 || v / s >= lim) ok = 0;
+                o[a] = ok ? v / s : 0;
+            }
+            if (!ok) continue;
+            cand[nc].key = linear_key(c[0], o[0], o[1], o[2], Xo, Yo, Zo);
+            cand[nc].b = c[0];
+            cand[nc].x = (int32_t)o[0];
+            cand[nc].y = (int32_t)o[1];
+            cand[nc].z = (int32_t)o[2];
+            ++nc;
+        }
+    }
+    qsort(cand, (size_t)nc, sizeof(cand_entry), cmp_cand);
+    int64_t no = 0;
+    for (int64_t i = 0; i < nc; ++i) {
+        if (no > 0 && cand[i].key == cand[no - 1].key) continue;
+        cand[no++] = cand[i];
+    }
+    for (int64_t o = 0; o < no; ++o) {
+        coords_out[4 * o + 0] = cand[o].b;
+        coords_out[4 * o + 1] = cand[o].x;
+        coords_out[4 * o + 2] = cand[o].y;
+        coords_out[4 * o + 3] = cand[o].z;
+    }
+    /* down: the input row at s*o + d_k */
+    for (int64_t o = 0; o < no; ++o) {
+        for (int k = 0; k < 27; ++k) {
+            uint32_t j = ORACLE_NONE;
+            if (k < T) {
+                const int64_t x = (int64_t)s * cand[o].x + k / (K * K) - p;
+                const int64_t y = (int64_t)s * cand[o].y + (k / K) % K - p;
+                const int64_t z = (int64_t)s * cand[o].z + k % K - p;
+                if (x >= 0 && x < X && y >= 0 && y < Y && z >= 0 && z < Z) {
+                    dict_entry probe;
+                    probe.key = linear_key(cand[o].b, x, y, z, X, Y, Z);
+                    probe.row = 0;
+                    const dict_entry* hit = (const dict_entry*)bsearch(&probe, din, (size_t)N,
+                                                                       sizeof(dict_entry), cmp_entry);
+                    if (hit) j = (uint32_t)hit->row;
+                }
+            }
+            down[o * 27 + k] = j;
+        }
+    }
+    /* up: the output row o with s*o + d_k = coord_j (the outputs are sorted by key) */
+    for (int64_t i = 0; i < N; ++i) {
+        const int32_t* c = coords + 4 * i;
+        for (int k = 0; k < 27; ++k) {
+            uint32_t oi = ORACLE_NONE;
+            if (k < T) {
+                const int d[3] = {k / (K * K) - p, (k / K) % K - p, k % K - p};
+                int64_t o[3];
+                int ok = 1;
+                for (int a = 0; a < 3; ++a) {
+                    const int64_t v = (int64_t)c[1 + a] - d[a];
+                    const int64_t lim = a == 0 ? Xo : (a == 1 ? Yo : Zo);
+                    if (v < 0 || v % s != 0 || v / s >= lim) ok = 0;
+                    o[a] = ok ? v / s : 0;
+                }
+                if (ok) {
+                    cand_entry probe;
+                    probe.key = linear_key(c[0], o[0], o[1], o[2], Xo, Yo, Zo);
+                    const cand_entry* hit = (const cand_entry*)bsearch(&probe, cand, (size_t)no,
+                                                                       sizeof(cand_entry), cmp_cand);
+                    if (hit) oi = (uint32_t)(hit - cand);
+                }
+            }
+            up[i * 27 + k] = oi;
+        }
+    }
+    *N_out = no;
+    free(din);
+    free(cand);
+    return ORACLE_OK;
+}
