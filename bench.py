@@ -39,6 +39,7 @@ DEFAULT_WORKLOAD = "b1_r512_shapes_c1024_bf16"
 SWEEP = ["b4_r64_spheres_c64_f16", "b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16",
          "b1_r512_shapes_c512_bf16", "b1_r1024_shapes_c64_f16"]
 INFER_WORKLOAD = "b1_r64_spheres_c256_bf16_infer"
+REGULAR_WORKLOAD = "b1_r512_shapes_c256_bf16"
 ORDER_WORKLOADS = ["b2_r256_shapes_c128_bf16", "b1_r512_shapes_c256_bf16", "b1_r1024_shapes_c64_f16"]
 STEP = "nbrmap build + fwd + dgrad + wgrad + dbias"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -602,6 +603,74 @@ def run_row_orders(args, wl, dev, flush):
     return rec
 
 
+def run_regular_conv(args, wl, dev, flush):
+    """Strided (down-sampling) and transposed (up-sampling) sparse convolution on the
+    workload's voxels: the map build, the strided forward, its backward (input,
+    weight and bias gradient) and the transposed forward, each timed alone with CUDA
+    events; FLOPs count valid (output, tap) pairs only."""
+    import torch
+    from voxel_gemm_gb300 import ops, synth
+    stream = torch.cuda.Stream(device=dev)
+    coords = torch.from_numpy(synth.make_coords(wl)).to(dev)
+    dt = synth.torch_dtype(wl.dtype)
+    peaks = load_peaks()
+    recs = []
+    for K, s_ in ((2, 2), (3, 2)):
+        ev = []
+        with torch.cuda.stream(stream):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+        m = ops.SparseMap(coords, wl.grid, K, s_, stream=stream)
+        with torch.cuda.stream(stream):
+            t1.record(stream)
+        stream.synchronize()
+        build_ms = t0.elapsed_time(t1)
+        T = K ** 3
+        g = torch.Generator(device=dev)
+        g.manual_seed(17 + K)
+        f = torch.randn(m.n_in, wl.cin, generator=g, device=dev).to(dt)
+        W = (torch.randn(T, wl.cin, wl.cout, generator=g, device=dev) * (2.0 / (T * wl.cin)) ** 0.5).to(dt)
+        b = torch.zeros(wl.cout, dtype=dt, device=dev)
+        dY = torch.randn(m.n_out, wl.cout, generator=g, device=dev).to(dt)
+        out = torch.empty(m.n_out, wl.cout, dtype=dt, device=dev)
+        dX = torch.empty(m.n_in, wl.cin, dtype=dt, device=dev)
+        dW = torch.empty_like(W)
+        db = torch.empty_like(b)
+        gc = torch.randn(m.n_out, wl.cin, generator=g, device=dev).to(dt)
+        up_out = torch.empty(m.n_in, wl.cout, dtype=dt, device=dev)
+        ws0 = m.workspace(0, wl.cin, wl.cout, dt)
+        ws1 = m.workspace(1, wl.cin, wl.cout, dt)
+        P = int((m.down().cpu().numpy().view("uint32") != 0xFFFFFFFF).sum())
+        calls = {"strided_fwd": lambda: m.fwd(0, f, W, b, out, ws0, stream=stream),
+                 "strided_bwd": lambda: m.bwd(0, dY, f, W, dX, dW, db, ws0, stream=stream),
+                 "transposed_fwd": lambda: m.fwd(1, gc, W, b, up_out, ws1, stream=stream)}
+        r = {"kernel": K, "stride": s_, "n_in": m.n_in, "n_out": m.n_out, "pairs": P, "map_build_ms": build_ms}
+        for name, fn in calls.items():
+            fn()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+            ts = []
+            for _ in range(max(3, min(args.steps, 10))):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    gr.replay()
+                    e1.record(stream)
+                ts.append((e0, e1))
+            stream.synchronize()
+            ms = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+            fl = (2.0 if name != "strided_bwd" else 4.0) * P * wl.cin * wl.cout
+            r[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                       "frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+        assert ops.vg_conv_status(ws0, stream) == ops.VG_OK and ops.vg_conv_status(ws1, stream) == ops.VG_OK
+        recs.append(r)
+        del m, ws0, ws1
+        torch.cuda.empty_cache()
+    return {"workload": wl.name, "cases": recs}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from voxel_gemm_gb300 import synth
@@ -634,9 +703,15 @@ def run_ours(args, rank, world, local_rank):
             except Exception as e:  # noqa: BLE001
                 orders.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
             torch.cuda.empty_cache()
+        try:
+            regular = run_regular_conv(args, synth.WORKLOADS[REGULAR_WORKLOAD], dev, flush)
+        except Exception as e:  # noqa: BLE001
+            regular = {"workload": REGULAR_WORKLOAD, "error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
     else:
         infer = None
         orders = None
+        regular = None
 
     res = {
         "metric": METRIC, "value": head["value"], "unit": "voxels/s", "n_gpus": world,
@@ -653,6 +728,7 @@ def run_ours(args, rank, world, local_rank):
         "sweep": sweep,
         "inference_small_n": infer,
         "row_order_morton_vs_hilbert": orders,
+        "regular_conv": regular,
     }
     return res
 

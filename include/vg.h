@@ -227,6 +227,72 @@ VG_API int vg_conv_status(void* conv_ws, void* stream);
 
 
 /* ======================================================================================
+ * Regular sparse convolution: strided (down-sampling) and transposed (up-sampling)
+ * "Contribution Tasks — JeffreyXiang/FlexGEMM", §二 module table and key functions:
+ * sparse_conv3d and kernels.cuda.spconv sparse_neighbor_map -- a convolution whose
+ * output sites differ from its input sites.  The pages give no formula; the reading
+ * taken is the convolution torch's dense conv3d computes on the densified grid, kept
+ * at the output sites whose window holds an active input:
+ *   kernel K in {2, 3} per axis (padding 0 for K = 2, 1 for K = 3), stride s in {1, 2};
+ *   output grid Xo = (X + 2p - K) / s + 1 (floor), likewise Yo, Zo, same batch count;
+ *   tap k = (tx*K + ty)*K + tz <-> offset d_k = (tx - p, ty - p, tz - p), taps = K^3;
+ *   output site o is active iff an input sits at s*o + d_k for some k;
+ *   output rows are numbered in ascending linear key ((b*Xo + x)*Yo + y)*Zo + z.
+ * Strided forward:    out[o] = bias + sum_k W_k^T f[down[o][k]]         (f: input sites)
+ * Transposed forward: out[j] = bias + sum_k W_k^T g[up[j][k]]           (g: output sites)
+ *   (the dense equivalent is conv_transpose3d with the same K, s, p, output at the input sites)
+ * W is [taps][Cin][Cout].  The backward passes run the same kernels as the
+ * submanifold convolution (input gradient through the other map with W_k
+ * transposed, weight gradient split-K with a fixed-order reduce).
+ * ====================================================================================== */
+
+/* A built regular-convolution map: host struct filled by vg_sparse_map_build.  Every
+ * pointer points into the map workspace (device memory) and stays valid while it does. */
+typedef struct {
+    int64_t n_in;               /* input sites (rows of coords)                          */
+    int64_t n_out;              /* output sites                                          */
+    int kernel, stride, taps;   /* taps = kernel^3                                        */
+    int out_grid[4];            /* B, Xo, Yo, Zo                                          */
+    const void* side_in;        /* row order and tiles of the input sites (device)        */
+    const void* side_out;       /* row order and tiles of the output sites (device)       */
+    const uint32_t* down;       /* [n_out][27]: input row at stride*o + d_k, else VG_NONE */
+    const uint32_t* down_mask;  /* [n_out]: bit k set iff down[o][k] is valid             */
+    const uint32_t* up;         /* [n_in][27]: output row o with stride*o + d_k = coord   */
+    const uint32_t* up_mask;    /* [n_in]                                                 */
+    const int32_t* coords_out;  /* [n_out][4] (b, x, y, z) in the output grid             */
+} vg_sparse_map;
+
+/* Bytes of map workspace for N input sites (0 if the arguments are invalid); flags:
+ * 0 or VG_ORDER_HILBERT.  Sized for the largest possible number of output sites. */
+VG_API size_t vg_sparse_map_workspace_bytes(int64_t N, int B, int X, int Y, int Z, int kernel, int stride,
+                                            unsigned flags);
+/* Build the map of N input sites coords [N][4] (device, int32, 16-byte aligned) into
+ * ws (device, 256-byte aligned).  SYNCHRONISES `stream`: the number of output sites
+ * is data-dependent and returned in map->n_out.  Returns VG_OK, an argument error,
+ * VG_ERR_COORD_OUT_OF_RANGE / VG_ERR_DUPLICATE_COORD for bad input sites (map->n_out
+ * is then 0 and convolutions on the map write nothing), VG_ERR_HASH_FULL or
+ * VG_ERR_DEVICE_TIMEOUT. */
+VG_API int vg_sparse_map_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, int kernel,
+                               int stride, unsigned flags, void* ws, size_t ws_bytes, vg_sparse_map* map,
+                               void* stream);
+/* Conv workspace for a pass on `map` (transposed = 0: strided, input sites -> output
+ * sites; 1: transposed, output sites -> input sites), as vg_conv_workspace_bytes. */
+VG_API size_t vg_sparse_conv_workspace_bytes(const vg_sparse_map* map, int transposed, int Cin, int Cout,
+                                             int dtype, unsigned flags);
+/* Forward.  transposed = 0: feats [n_in][Cin] -> out [n_out][Cout];  transposed = 1:
+ * feats [n_out][Cin] -> out [n_in][Cout].  Conventions, dtypes, flags and errors as
+ * vg_subm_conv3d_fwd; asynchronous. */
+VG_API int vg_sparse_conv3d_fwd(const vg_sparse_map* map, int transposed, int dtype, const void* feats,
+                                const void* weight, const void* bias, void* out, int Cin, int Cout,
+                                unsigned flags, void* conv_ws, size_t conv_ws_bytes, void* stream);
+/* Backward: grad_out has the forward output's rows, grad_feats the forward input's;
+ * grad_weight [taps][Cin][Cout], grad_bias [Cout]; each output may be NULL. */
+VG_API int vg_sparse_conv3d_bwd(const vg_sparse_map* map, int transposed, int dtype, const void* grad_out,
+                                const void* feats, const void* weight, void* grad_feats, void* grad_weight,
+                                void* grad_bias, int Cin, int Cout, unsigned flags, void* conv_ws,
+                                size_t conv_ws_bytes, void* stream);
+
+/* ======================================================================================
  * Serialisation: space-filling-curve codes of voxel coordinates
  * "Contribution Tasks — JeffreyXiang/FlexGEMM", §二 module table (kernels.cuda.serialize:
  * z_order_encode/decode, hilbert_encode/decode) and the ops layer's

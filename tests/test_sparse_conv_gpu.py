@@ -1,0 +1,145 @@
+"""Regular (strided and transposed) sparse convolution on the GPU vs the oracle.
+
+The map (output sites in linear-key order, down and up tables) must equal the
+oracle's bit for bit; the forward, input gradient, weight and bias gradient of
+both directions must be within the dtype's relative Frobenius bound, on all four
+(kernel, stride) cases and on ragged sizes, through the tensor-core, TF32 and
+FFMA paths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL, f64, rel_fro, u32
+from voxel_gemm_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+TF32_TOL = 5e-3
+
+
+def _pad27(W):
+    out = np.zeros((27,) + tuple(W.shape[1:]))
+    out[: W.shape[0]] = f64(W)
+    return out
+
+
+def _problem(K, s, n, grid, cin, cout, dtype, seed):
+    coords = synth.random_coords(seed, n, *grid)
+    rng = torch.Generator().manual_seed(seed)
+    dt = synth.torch_dtype(dtype)
+    T = K ** 3
+    f_in = torch.randn(coords.shape[0], cin, generator=rng).to(dt)
+    W = (torch.randn(T, cin, cout, generator=rng) * (2.0 / (T * cin)) ** 0.5).to(dt)
+    b = (torch.randn(cout, generator=rng) * 0.1).to(dt)
+    return coords, f_in, W, b
+
+
+@pytest.mark.parametrize("K,s", [(2, 2), (3, 2), (3, 1), (2, 1)])
+def test_sparse_map_bit_exact(K, s):
+    grid = (2, 18, 11, 14)
+    coords = synth.random_coords(K * 10 + s, 1500, *grid)
+    co_ref, down_ref, up_ref = oracle.sparse_map(coords, *grid, K, s)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, K, s)
+    assert m.n_out == co_ref.shape[0] and m.taps == K ** 3
+    assert np.array_equal(m.coords_out().cpu().numpy(), co_ref)
+    assert np.array_equal(u32(m.down()), down_ref)
+    assert np.array_equal(u32(m.up()), up_ref)
+
+
+CASES = [(K, s, dt, c) for (K, s) in [(2, 2), (3, 2), (3, 1), (2, 1)] for dt, c in
+         [("bf16", (64, 128)), ("f16", (128, 64)), ("f32", (24, 40))]]
+
+
+@pytest.mark.parametrize("K,s,dtype,chan", CASES)
+def test_strided_and_transposed_conv_match_oracle(K, s, dtype, chan):
+    cin, cout = chan
+    grid = (2, 16, 14, 12)
+    coords, f_in, W, b = _problem(K, s, 1700, grid, cin, cout, dtype, K * 100 + s * 10 + cin)
+    co, down, up = oracle.sparse_map(coords, *grid, K, s)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, K, s)
+    assert m.n_out == co.shape[0]
+    tol = TOL[dtype]
+    W27 = _pad27(W)
+    dt = f_in.dtype
+    Wd, bd = W.cuda(), b.cuda()
+    # ---- strided: input sites -> output sites
+    fi = f_in.cuda()
+    dY = torch.randn(m.n_out, cout, generator=torch.Generator().manual_seed(1)).to(dt)
+    ws = m.workspace(0, cin, cout, dt)
+    out = torch.empty(m.n_out, cout, dtype=dt, device="cuda")
+    m.fwd(0, fi, Wd, bd, out, ws)
+    dX = torch.empty(m.n_in, cin, dtype=dt, device="cuda")
+    dW = torch.empty_like(Wd)
+    db = torch.empty_like(bd)
+    m.bwd(0, dY.cuda(), fi, Wd, dX, dW, db, ws)
+    torch.cuda.synchronize()
+    assert ops.vg_conv_status(ws) == ops.VG_OK
+    out_ref = oracle.fwd(down, f64(f_in), W27, f64(b))
+    dX_ref = oracle.dgrad_scatter_to(down, f64(dY), W27, m.n_in)
+    dW_ref, db_ref = oracle.wgrad(down, f64(f_in), f64(dY))
+    errs = {"out": rel_fro(f64(out), out_ref), "dX": rel_fro(f64(dX), dX_ref),
+            "dW": rel_fro(f64(dW), dW_ref[: K ** 3]), "db": rel_fro(f64(db), db_ref)}
+    assert all(e <= tol for e in errs.values()), errs
+    # ---- transposed: output sites -> input sites (the same map, the other way)
+    g = torch.randn(m.n_out, cin, generator=torch.Generator().manual_seed(2)).to(dt)
+    dYt = torch.randn(m.n_in, cout, generator=torch.Generator().manual_seed(3)).to(dt)
+    wst = m.workspace(1, cin, cout, dt)
+    outt = torch.empty(m.n_in, cout, dtype=dt, device="cuda")
+    m.fwd(1, g.cuda(), Wd, bd, outt, wst)
+    dG = torch.empty(m.n_out, cin, dtype=dt, device="cuda")
+    m.bwd(1, dYt.cuda(), g.cuda(), Wd, dG, dW, db, wst)
+    torch.cuda.synchronize()
+    assert ops.vg_conv_status(wst) == ops.VG_OK
+    out_ref = oracle.fwd(up, f64(g), W27, f64(b))
+    dG_ref = oracle.dgrad_scatter_to(up, f64(dYt), W27, m.n_out)
+    dW_ref, db_ref = oracle.wgrad(up, f64(g), f64(dYt))
+    errs = {"out": rel_fro(f64(outt), out_ref), "dG": rel_fro(f64(dG), dG_ref),
+            "dW": rel_fro(f64(dW), dW_ref[: K ** 3]), "db": rel_fro(f64(db), db_ref)}
+    assert all(e <= tol for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("K,s", [(2, 2), (3, 2)])
+def test_sparse_conv_tf32(K, s):
+    grid = (1, 20, 20, 20)
+    coords, f_in, W, b = _problem(K, s, 2500, grid, 64, 32, "f32", 77 + K)
+    co, down, up = oracle.sparse_map(coords, *grid, K, s)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, K, s)
+    fl = ops.VG_ALLOW_TF32
+    ws = m.workspace(0, 64, 32, torch.float32, fl)
+    out = torch.empty(m.n_out, 32, device="cuda")
+    m.fwd(0, f_in.cuda(), W.cuda(), b.cuda(), out, ws, flags=fl)
+    dY = torch.randn(m.n_out, 32)
+    dX = torch.empty(m.n_in, 64, device="cuda")
+    m.bwd(0, dY.cuda(), f_in.cuda(), W.cuda(), dX, None, None, ws, flags=fl)
+    torch.cuda.synchronize()
+    W27 = _pad27(W)
+    assert rel_fro(f64(out), oracle.fwd(down, f64(f_in), W27, f64(b))) <= TF32_TOL
+    assert rel_fro(f64(dX), oracle.dgrad_scatter_to(down, f64(dY), W27, m.n_in)) <= TF32_TOL
+
+
+def test_sparse_map_rejects_bad_sites_and_arguments():
+    grid = (1, 8, 8, 8)
+    c = torch.tensor([[0, 1, 1, 1], [0, 1, 1, 1]], dtype=torch.int32, device="cuda")
+    with pytest.raises(ops.VGError) as e:
+        ops.SparseMap(c, grid, 3, 2)
+    assert e.value.status == ops.VG_ERR_DUPLICATE_COORD
+    c = torch.tensor([[0, 8, 1, 1]], dtype=torch.int32, device="cuda")
+    with pytest.raises(ops.VGError) as e:
+        ops.SparseMap(c, grid, 2, 2)
+    assert e.value.status == ops.VG_ERR_COORD_OUT_OF_RANGE
+    assert ops.lib().vg_sparse_map_workspace_bytes(10, 1, 8, 8, 8, 4, 2, 0) == 0
+    assert ops.lib().vg_sparse_map_workspace_bytes(10, 1, 8, 8, 8, 3, 3, 0) == 0
+
+
+def test_sparse_map_empty_input():
+    m = ops.SparseMap(torch.zeros(0, 4, dtype=torch.int32, device="cuda"), (1, 8, 8, 8), 3, 2)
+    assert m.n_out == 0
+    W = torch.randn(27, 64, 64, device="cuda").bfloat16()
+    ws = m.workspace(0, 64, 64, torch.bfloat16)
+    dW = torch.full_like(W, 3.0)
+    db = torch.full((64,), 3.0, dtype=torch.bfloat16, device="cuda")
+    m.bwd(0, torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"), torch.zeros(0, 64, dtype=torch.bfloat16,
+          device="cuda"), W, None, dW, db, ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dW) == 0 and torch.count_nonzero(db) == 0

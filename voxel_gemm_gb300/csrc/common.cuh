@@ -57,6 +57,27 @@ struct NbrLayout {
     int64_t tile_blocks = 1; // blocks of one tile-sort pass
 };
 
+// Workspace layout of a regular (strided / transposed) convolution map: a header
+// (status word, number of output sites), one submanifold-layout block per side
+// (input sites, output sites: row order, tile masks, lists in processing order,
+// tile order, hash table, sort scratch), the down/up neighbour tables and masks,
+// the output coordinates, and the output-site candidate sort.
+struct SparseLayout {
+    int64_t n_in = 0, n_out = -1, cap_out = 0;
+    int K = 3, stride = 2, pad = 1, T = 27;
+    int B = 1, X = 1, Y = 1, Z = 1;
+    int64_t Xo = 1, Yo = 1, Zo = 1;
+    unsigned flags = 0;
+    NbrLayout li, lo_cap, lo;  // input side; output side sized for cap_out; output side for n_out
+    size_t side_o_bytes = 0;
+    int cand64 = 0, cand_passes = 1, cand_items = 16;
+    int64_t cand_n = 0, cand_blocks = 1, scan_blocks = 1;
+    uint64_t sentinel = 0;     // key meaning "no output cell": the output grid's volume
+    size_t off_hdr = 0, off_side_i = 0, off_side_o = 0, off_nbr_down = 0, off_mask_down = 0, off_nbr_up = 0,
+           off_mask_up = 0, off_coords_out = 0, off_cand_a = 0, off_cand_b = 0, off_cand_va = 0, off_cand_vb = 0,
+           off_cand_hist = 0, off_cand_status = 0, off_cand_tickets = 0, off_scan = 0, total = 0;
+};
+
 constexpr int kSortThreads = 256;
 constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digits
 constexpr int kRadixBits = 8;

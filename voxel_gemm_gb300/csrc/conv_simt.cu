@@ -119,7 +119,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 k_wgrad_simt(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict__ nbr,
              const uint32_t* __restrict__ nbr_status, int64_t n, const T* __restrict__ f,
-             const T* __restrict__ dy, int Cin, int Cout, int64_t rows_per_chunk,
+             const T* __restrict__ dy, int Cin, int Cout, int taps, int64_t rows_per_chunk,
              float* __restrict__ partial) {
     __shared__ float Fs[WR][BM + 4];
     __shared__ float Gs[WR][BN + 4];
@@ -127,8 +127,8 @@ k_wgrad_simt(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict
     if (*nbr_status) return;
     const int tid = threadIdx.x;
     const int co0 = blockIdx.x * BN, ci0 = blockIdx.y * BM;
-    const int k = blockIdx.z % kTaps;
-    const int s = blockIdx.z / kTaps;
+    const int k = blockIdx.z % taps;
+    const int s = blockIdx.z / taps;
     const int64_t rb = (int64_t)s * rows_per_chunk;
     const int64_t re = min(n, rb + rows_per_chunk);
     const int ty = tid >> 4, tx = tid & 15;
@@ -189,13 +189,13 @@ k_wgrad_simt(const uint32_t* __restrict__ sorted_idx, const uint32_t* __restrict
 
 // Fixed-order sum of split-K partials (deterministic), then round to T.
 template <typename T>
-__global__ void k_reduce_splits(const float* __restrict__ partial, int splits, int64_t total,
+__global__ void k_reduce_splits(const float* __restrict__ partial, int splits, int64_t total, int64_t stride,
                                 T* __restrict__ out, const uint32_t* __restrict__ nbr_status) {
     if (*nbr_status) return;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
     float s = 0.f;
-    for (int p = 0; p < splits; ++p) s += partial[(int64_t)p * total + i];
+    for (int p = 0; p < splits; ++p) s += partial[(int64_t)p * stride + i];
     out[i] = from_f32<T>(s);
 }
 
@@ -261,12 +261,12 @@ template <typename T>
 static int launch_gather(const GatherPass& p, cudaStream_t s) {
     const dim3 grid((unsigned)((p.n + BM - 1) / BM), (unsigned)((p.Ndim + BN - 1) / BN));
     // W offsets: fwd  W[k][kk][n]  -> sK = Cout, sN = 1
-    //            dgrad W[26-k][n][kk] -> sK = 1,    sN = Cout
+    //            dgrad W[26-k][n][kk] (mode 1) or W[k][n][kk] (mode 2) -> sK = 1, sN = Cout
     const int64_t sK = p.dgrad ? 1 : p.Cout;
     const int64_t sN = p.dgrad ? p.Cout : 1;
     k_gather_gemm_simt<T><<<grid, 256, 0, s>>>(p.sorted_idx, p.nbr, p.nbr_status, p.n,
                                                static_cast<const T*>(p.A), p.Kdim,
-                                               static_cast<const T*>(p.W), p.dgrad, sK, sN,
+                                               static_cast<const T*>(p.W), p.dgrad == 1, sK, sN,
                                                static_cast<const T*>(p.bias), static_cast<T*>(p.out),
                                                p.Ndim);
     return VG_OK;
@@ -282,8 +282,8 @@ int simt_gather_pass(const GatherPass& p, cudaStream_t s) {
     return VG_ERR_INVALID_ARG;
 }
 
-int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms) {
-    const int64_t tiles = (int64_t)kTaps * ((Cin + BM - 1) / BM) * ((Cout + BN - 1) / BN);
+int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
+    const int64_t tiles = (int64_t)taps * ((Cin + BM - 1) / BM) * ((Cout + BN - 1) / BN);
     int64_t s = (4 * (int64_t)sms + tiles - 1) / tiles;
     s = std::min<int64_t>(s, std::max<int64_t>(1, (n + 1023) / 1024));
     return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
@@ -293,14 +293,14 @@ template <typename T>
 static int launch_wgrad(const WgradPass& p, cudaStream_t s) {
     const int S = p.splits;
     const int64_t rpc = ((p.n + S - 1) / S + WR - 1) / WR * WR;
-    const int64_t total = (int64_t)kTaps * p.Cin * p.Cout;
+    const int64_t total = (int64_t)p.taps * p.Cin * p.Cout;
     if (p.dW) {
         const dim3 grid((unsigned)((p.Cout + BN - 1) / BN), (unsigned)((p.Cin + BM - 1) / BM),
-                        (unsigned)(kTaps * S));
+                        (unsigned)(p.taps * S));
         k_wgrad_simt<T><<<grid, 256, 0, s>>>(p.sorted_idx, p.nbr, p.nbr_status, p.n,
                                              static_cast<const T*>(p.f), static_cast<const T*>(p.dy),
-                                             p.Cin, p.Cout, rpc, p.partial);
-        launch_reduce_splits(p.partial, S, total, p.dW, p.dtype, p.nbr_status, s);
+                                             p.Cin, p.Cout, p.taps, rpc, p.partial);
+        launch_reduce_splits(p.partial, S, total, (int64_t)kTaps * p.Cin * p.Cout, p.dW, p.dtype, p.nbr_status, s);
     }
     if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;
@@ -317,17 +317,17 @@ int simt_wgrad(const WgradPass& p, cudaStream_t s) {
 }
 
 template <typename T>
-static void reduce_t(const float* partial, int splits, int64_t total, void* out,
+static void reduce_t(const float* partial, int splits, int64_t total, int64_t stride, void* out,
                      const uint32_t* nbr_status, cudaStream_t s) {
     k_reduce_splits<T><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-        partial, splits, total, static_cast<T*>(out), nbr_status);
+        partial, splits, total, stride, static_cast<T*>(out), nbr_status);
 }
 
-void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
+void launch_reduce_splits(const float* partial, int splits, int64_t total, int64_t stride, void* out, int dtype,
                           const uint32_t* nbr_status, cudaStream_t s) {
-    if (dtype == VG_F32) reduce_t<float>(partial, splits, total, out, nbr_status, s);
-    else if (dtype == VG_F16) reduce_t<__half>(partial, splits, total, out, nbr_status, s);
-    else reduce_t<__nv_bfloat16>(partial, splits, total, out, nbr_status, s);
+    if (dtype == VG_F32) reduce_t<float>(partial, splits, total, stride, out, nbr_status, s);
+    else if (dtype == VG_F16) reduce_t<__half>(partial, splits, total, stride, out, nbr_status, s);
+    else reduce_t<__nv_bfloat16>(partial, splits, total, stride, out, nbr_status, s);
 }
 
 int dbias_blocks(int64_t n, int sms) {
@@ -341,7 +341,7 @@ static void dbias_t(const void* dy, int64_t n, int Cout, int sms, void* db, floa
     const int R = dbias_blocks(n, sms);
     k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, dbias_rows(n, sms), partial_db,
                                          nbr_status);
-    reduce_t<T>(partial_db, R, Cout, db, nbr_status, s);
+    reduce_t<T>(partial_db, R, Cout, Cout, db, nbr_status, s);
 }
 
 void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,

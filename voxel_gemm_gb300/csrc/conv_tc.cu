@@ -451,25 +451,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
 // rows in the 128-byte swizzled layout (row n at (n/8)*1024 + (n%8)*128,
 // 16-byte chunk c stored at chunk c ^ (n%8)).  fwd: row n = output channel,
 // K = input channel, element W[k][kk][n].  dgrad: row n = input channel,
-// K = output channel, element W[26-k][n][kk] (the flipped, transposed tap).
+// K = output channel, element W[26-k][n][kk] (the flipped, transposed tap);
+// mode 2 (input gradient of a strided / transposed map): element W[k][n][kk].
 // One block = one tap, one K block and 32 consecutive rows n.
 template <typename T>
 __global__ void __launch_bounds__(256)
-k_pack_weights(const T* __restrict__ W, int Cin, int Cout, int dgrad, int BN, uint8_t* __restrict__ img) {
+k_pack_weights(const T* __restrict__ W, int Cin, int Cout, int mode, int BN, uint8_t* __restrict__ img) {
     constexpr int KE = 128 / sizeof(T);  // K values per block row
     constexpr int PER_CHUNK = 16 / sizeof(T);
     __shared__ T tile[KE][33];
     const int k = blockIdx.x, kb = blockIdx.y, n0 = blockIdx.z * 32;
-    const int Kdim = dgrad ? Cout : Cin;
+    const int Kdim = mode ? Cout : Cin;
+    const int src_tap = mode == 1 ? 26 - k : k;
     const int KB = Kdim / KE;
     const int tid = threadIdx.x;
     for (int idx = tid; idx < KE * 32; idx += 256) {
-        if (!dgrad) {
+        if (!mode) {
             const int kk = idx >> 5, n = idx & 31;
             tile[kk][n] = W[((int64_t)k * Cin + kb * KE + kk) * Cout + n0 + n];
         } else {
             const int n = idx / KE, kk = idx % KE;
-            tile[kk][n] = W[((int64_t)(26 - k) * Cin + n0 + n) * Cout + kb * KE + kk];
+            tile[kk][n] = W[((int64_t)src_tap * Cin + n0 + n) * Cout + kb * KE + kk];
         }
     }
     __syncthreads();
@@ -567,17 +569,18 @@ size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim) {
     return (size_t)kTaps * Kdim * Ndim * (dtype == VG_F32 ? 4 : 2);
 }
 
-int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void* packed,
+int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int mode, int taps, void* packed,
                     const uint32_t* nbr_status, cudaStream_t s) {
     (void)nbr_status;
-    const int Kdim = dgrad ? Cout : Cin, Ndim = dgrad ? Cin : Cout;
+    const int Kdim = mode ? Cout : Cin, Ndim = mode ? Cin : Cout;
     const int ke = dtype == VG_F32 ? 32 : 64;
-    const dim3 grid(kTaps, Kdim / ke, Ndim / 32);
+    // mode 1 reads tap 26 - k for image tap k: all 27 taps; otherwise the kernel's taps
+    const dim3 grid(mode == 1 ? kTaps : taps, Kdim / ke, Ndim / 32);
     if (dtype == VG_F32)
-        k_pack_weights<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), Cin, Cout, dgrad,
+        k_pack_weights<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), Cin, Cout, mode,
                                                    choose_bn(Ndim), static_cast<uint8_t*>(packed));
     else
-        k_pack_weights<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(W), Cin, Cout, dgrad,
+        k_pack_weights<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(W), Cin, Cout, mode,
                                                       choose_bn(Ndim), static_cast<uint8_t*>(packed));
     return VG_OK;
 }

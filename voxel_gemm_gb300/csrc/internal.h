@@ -21,6 +21,14 @@ int nbr_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, unsi
               void* ws, size_t ws_bytes, uint32_t* nbr, uint32_t* mask, cudaStream_t s);
 int nbr_status(const void* ws, cudaStream_t s);
 
+// Regular (strided / transposed) convolution map.  n_out < 0: the layout before
+// the number of output sites is known (sizes for the largest possible count).
+struct SparseLayout;
+int sparse_layout(int64_t N, int B, int X, int Y, int Z, int K, int stride, unsigned flags, int sms,
+                  int64_t n_out, SparseLayout* S);
+int sparse_build(const int32_t* coords, int64_t N, int B, int X, int Y, int Z, int K, int stride, unsigned flags,
+                 void* ws, size_t ws_bytes, int64_t* n_out_host, cudaStream_t s);
+
 // Byte offset of sorted_idx / tile masks inside a neighbour-map workspace.
 constexpr size_t kSortedIdxOffset = 256;
 inline size_t tile_mask_offset(int64_t N) { return 256 + ((4 * (size_t)N + 255) / 256) * 256; }
@@ -48,9 +56,12 @@ struct GatherPass {
     int64_t n;
     const void* A;
     int Kdim;
-    const void* W;               // user weight [27][Cin][Cout]
+    const void* W;               // user weight [taps][Cin][Cout]
     int Cin, Cout;
-    int dgrad;                   // 0 = forward, 1 = input gradient
+    // 0 = forward (B_k = W_k^T), 1 = submanifold input gradient (B_k = W_{26-k}),
+    // 2 = input gradient of a strided / transposed map (B_k = W_k, no flip)
+    int dgrad;
+    int taps = 27;               // taps of the kernel (27, or 8 for a 2x2x2 kernel)
     const void* bias;            // may be null
     void* out;
     int Ndim;
@@ -83,14 +94,16 @@ struct WgradPass {
     void* dy_sorted;    // tensor-core path: tc_wgrad_sorted_dy_bytes bytes of scratch (or null if 0)
     int splits;
     int sms;            // SM count of the plan (grid sizes, db row blocks)
+    int taps = 27;      // dW has taps x Cin x Cout entries (partials keep a 27-tap stride)
     uint32_t* err;
 };
 
-int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms);
+int simt_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps = 27);
 int simt_wgrad(const WgradPass& p, cudaStream_t s);
 
-// Deterministic fixed-order sum of split-K partials [splits][total] into out (dtype).
-void launch_reduce_splits(const float* partial, int splits, int64_t total, void* out, int dtype,
+// Deterministic fixed-order sum of split-K partials (split p at partial + p * stride)
+// over the first `total` entries into out (dtype).
+void launch_reduce_splits(const float* partial, int splits, int64_t total, int64_t stride, void* out, int dtype,
                           const uint32_t* nbr_status, cudaStream_t s);
 // db = column sums of dy over dbias_blocks(n, sms) row blocks, reduced in a fixed order
 // (partial_db holds dbias_blocks(n, sms) x Cout floats).
@@ -110,11 +123,11 @@ int launch_sum_ordered(const void* parts, int nparts, int64_t count, int dtype, 
 int tc_supported(int dtype, int Cin, int Cout);
 // fp32 features on the tensor cores as TF32 (forward and input gradient): Cin, Cout % 32 == 0
 int tf32_supported(int dtype, int Cin, int Cout);
-int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms);
+int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps = 27);
 size_t tc_packed_weight_bytes(int dtype, int Kdim, int Ndim);
-// Repack W into the swizzled shared-memory image of the B operand
-// (dgrad = 0: B_k = W_k^T, K = Cin;  dgrad = 1: B_k = W_{26-k}, K = Cout).
-int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int dgrad, void* packed,
+// Repack W ([taps][Cin][Cout]) into the swizzled shared-memory image of the B operand
+// (mode 0: B_k = W_k^T, K = Cin;  1: B_k = W_{26-k}, K = Cout;  2: B_k = W_k, K = Cout).
+int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int mode, int taps, void* packed,
                     const uint32_t* nbr_status, cudaStream_t s);
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
 int tc_wgrad(const WgradPass& p, cudaStream_t s);

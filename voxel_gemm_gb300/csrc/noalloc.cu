@@ -97,7 +97,7 @@ extern "C" int vg_subm_conv3d_fwd_noalloc(const void* nbr_ws, const uint32_t* nb
     g.dtype = dtype;
     g.err = err;
     if (tc) {
-        st = tc_pack_weights(weight, dtype, Cin, Cout, 0, base + 256, g.nbr_status, s);
+        st = tc_pack_weights(weight, dtype, Cin, Cout, 0, kTaps, base + 256, g.nbr_status, s);
         if (st == VG_OK) st = tc_gather_pass(g, base + 256, s);
     } else {
         st = simt_gather_pass(g, s);

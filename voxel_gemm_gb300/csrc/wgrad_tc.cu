@@ -78,6 +78,7 @@ struct WgArgs {
     const uint16_t* f;
     const uint16_t* dy;
     int Cin, Cout;
+    int taps;        // taps of the kernel (27, or 8): (tap, channel block) slots of the M blocks
     float* partial;  // [splits][27][Cin][Cout]
     uint32_t* err;
 };
@@ -90,19 +91,19 @@ struct MUnit {
     int tap0, tap1;  // tap1 = -1: the second 64-channel block is unused (zero)
     int c0, c1;
 };
-__host__ __device__ __forceinline__ int num_munits(int Cin) { return (kTaps * (Cin / 64) + 1) / 2; }
-__device__ __forceinline__ MUnit munit(int m, int Cin) {
+__host__ __device__ __forceinline__ int num_munits(int Cin, int taps) { return (taps * (Cin / 64) + 1) / 2; }
+__device__ __forceinline__ MUnit munit(int m, int Cin, int taps) {
     const int CB = Cin / 64;
     const int s0 = 2 * m, s1 = 2 * m + 1;
     MUnit r;
-    if (s0 >= kTaps * CB) {  // past the last slot (a partial group of M blocks): all zero
+    if (s0 >= taps * CB) {  // past the last slot (a partial group of M blocks): all zero
         r.tap0 = r.tap1 = -1;
         r.c0 = r.c1 = 0;
         return r;
     }
     r.tap0 = s0 / CB;
     r.c0 = (s0 % CB) * 64;
-    if (s1 < kTaps * CB) {
+    if (s1 < taps * CB) {
         r.tap1 = s1 / CB;
         r.c1 = (s1 % CB) * 64;
     } else {
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a, const __grid
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    const int M = num_munits(a.Cin);
+    const int M = num_munits(a.Cin, a.taps);
     const int MG = (M + MU - 1) / MU;  // groups of MU M blocks
     const int NB = a.Cout / BN;
     const int64_t units = (int64_t)MG * NB * a.splits;
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a, const __grid
             uint32_t umask = 0;
 #pragma unroll
             for (int v = 0; v < MU; ++v) {
-                mu[v] = munit(mg * MU + v, a.Cin);
+                mu[v] = munit(mg * MU + v, a.Cin, a.taps);
                 if (mu[v].tap0 >= 0) umask |= 1u << mu[v].tap0;
                 if (mu[v].tap1 >= 0) umask |= 1u << mu[v].tap1;
             }
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a, const __grid
             const int blk = mrow >> 6;
 #pragma unroll 1
             for (int v = 0; v < MU; ++v) {
-                const MUnit muv = munit(mg * MU + v, a.Cin);
+                const MUnit muv = munit(mg * MU + v, a.Cin, a.taps);
                 const int tap = blk ? muv.tap1 : muv.tap0;
                 const int ci = (blk ? muv.c1 : muv.c0) + (mrow & 63);
                 float* dst = tap >= 0 ? a.partial + ((s * kTaps + tap) * a.Cin + ci) * (int64_t)a.Cout + nb * BN
@@ -492,7 +493,7 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return VG_ERR_CUDA;
     }
-    const int MG = (num_munits(a.Cin) + C::MU - 1) / C::MU;
+    const int MG = (num_munits(a.Cin, a.taps) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, sms);
     kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
@@ -505,11 +506,11 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream
 // tiles (the units running side by side then stream the same rows through L2;
 // measured at 602k voxels, C = 1024: 2 chunks 17.6 ms, 8 chunks 16.1 ms), at
 // least 4 tiles per chunk (every chunk non-empty), partial sums capped at 1 GiB.
-int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms) {
+int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
     const int bn = wg_bn(Cout);
     const int mu = bn == 64 ? WCfg<64>::MU : (bn == 128 ? WCfg<128>::MU : WCfg<256>::MU);
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
-    const int64_t MG = (num_munits(Cin) + mu - 1) / mu;
+    const int64_t MG = (num_munits(Cin, taps) + mu - 1) / mu;
     const int64_t per_split = MG * (Cout / bn);
     int64_t S = std::max<int64_t>(1, (4 * (int64_t)sms + per_split - 1) / per_split);
     S = std::max<int64_t>(S, (T + 255) / 256);
@@ -543,6 +544,7 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.dy = static_cast<const uint16_t*>(p.dy);
         a.Cin = p.Cin;
         a.Cout = p.Cout;
+        a.taps = p.taps;
         a.partial = p.partial;
         a.err = p.err;
         const bool bf16 = p.dtype == VG_BF16;
@@ -562,7 +564,8 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
             default: st = bf16 ? launch_wgrad<64, true>(a, dys, p.sms, s) : launch_wgrad<64, false>(a, dys, p.sms, s); break;
         }
         if (st != VG_OK) return st;
-        launch_reduce_splits(p.partial, p.splits, (int64_t)kTaps * p.Cin * p.Cout, p.dW, p.dtype, p.nbr_status, s);
+        launch_reduce_splits(p.partial, p.splits, (int64_t)p.taps * p.Cin * p.Cout, (int64_t)kTaps * p.Cin * p.Cout,
+                             p.dW, p.dtype, p.nbr_status, s);
     }
     if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;

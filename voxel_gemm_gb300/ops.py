@@ -35,6 +35,15 @@ _lib = None
 _DT = {torch.float32: VG_F32, torch.float16: VG_F16, torch.bfloat16: VG_BF16}
 
 
+class SparseMapStruct(ctypes.Structure):
+    """Mirror of vg_sparse_map (include/vg.h)."""
+    _fields_ = [("n_in", ctypes.c_int64), ("n_out", ctypes.c_int64), ("kernel", ctypes.c_int),
+                ("stride", ctypes.c_int), ("taps", ctypes.c_int), ("out_grid", ctypes.c_int * 4),
+                ("side_in", ctypes.c_void_p), ("side_out", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("down_mask", ctypes.c_void_p), ("up", ctypes.c_void_p), ("up_mask", ctypes.c_void_p),
+                ("coords_out", ctypes.c_void_p)]
+
+
 class VGError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {vg_strerror(status)} (status {status})")
@@ -70,6 +79,12 @@ def lib():
             "vg_subm_conv3d_fwd_noalloc_status": ([P], I),
             "vg_sum_ordered": ([P, I, I64, I, P, P], I),
             "vg_encode_seq": ([P, I64, I, I, P, P], I),
+            "vg_sparse_map_workspace_bytes": ([I64, I, I, I, I, I, I, U], SZ),
+            "vg_sparse_map_build": ([P, I64, I, I, I, I, I, I, U, P, SZ, ctypes.POINTER(SparseMapStruct), P], I),
+            "vg_sparse_conv_workspace_bytes": ([ctypes.POINTER(SparseMapStruct), I, I, I, I, U], SZ),
+            "vg_sparse_conv3d_fwd": ([ctypes.POINTER(SparseMapStruct), I, I, P, P, P, P, I, I, U, P, SZ, P], I),
+            "vg_sparse_conv3d_bwd": ([ctypes.POINTER(SparseMapStruct), I, I, P, P, P, P, P, P, I, I, U, P, SZ, P],
+                                     I),
             "vg_decode_seq": ([P, I64, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
@@ -262,3 +277,67 @@ def conv_workspace(N, Cin, Cout, dtype, device="cuda", flags=0) -> torch.Tensor:
     if nb == 0:
         raise VGError(VG_ERR_UNSUPPORTED, "vg_conv_workspace_bytes")
     return torch.zeros(nb, dtype=torch.uint8, device=device)  # zero error record before any call
+
+
+# ---------------------------------------------------------------- regular (strided / transposed) conv
+class SparseMap:
+    """A regular-convolution map (input sites -> strided output sites) in a torch-owned workspace."""
+
+    def __init__(self, coords, grid, kernel: int, stride: int, flags: int = 0, stream=None):
+        B, X, Y, Z = grid
+        N = coords.shape[0]
+        nb = int(lib().vg_sparse_map_workspace_bytes(N, B, X, Y, Z, kernel, stride, flags))
+        if nb == 0:
+            raise VGError(VG_ERR_INVALID_ARG, "vg_sparse_map_workspace_bytes")
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=coords.device)
+        self.coords = coords
+        self.m = SparseMapStruct()
+        _check(lib().vg_sparse_map_build(_p(coords), N, B, X, Y, Z, kernel, stride, flags, _p(self.ws), nb,
+                                         ctypes.byref(self.m), _s(stream)), "vg_sparse_map_build")
+
+    @property
+    def n_in(self) -> int:
+        return self.m.n_in
+
+    @property
+    def n_out(self) -> int:
+        return self.m.n_out
+
+    @property
+    def taps(self) -> int:
+        return self.m.taps
+
+    def _view(self, ptr, nbytes, dtype, shape):
+        off = ptr - self.ws.data_ptr()
+        return self.ws.view(torch.uint8)[off: off + nbytes].view(dtype).view(*shape)
+
+    def coords_out(self) -> torch.Tensor:
+        return self._view(self.m.coords_out, 16 * self.n_out, torch.int32, (self.n_out, 4))
+
+    def down(self) -> torch.Tensor:
+        return self._view(self.m.down, 4 * 27 * self.n_out, torch.int32, (self.n_out, 27))
+
+    def up(self) -> torch.Tensor:
+        return self._view(self.m.up, 4 * 27 * self.n_in, torch.int32, (self.n_in, 27))
+
+    def workspace(self, transposed, Cin, Cout, dtype, flags=0) -> torch.Tensor:
+        code = dtype if isinstance(dtype, int) else _DT[dtype]
+        nb = int(lib().vg_sparse_conv_workspace_bytes(ctypes.byref(self.m), int(transposed), Cin, Cout, code, flags))
+        if nb == 0:
+            raise VGError(VG_ERR_UNSUPPORTED, "vg_sparse_conv_workspace_bytes")
+        return torch.zeros(nb, dtype=torch.uint8, device=self.ws.device)
+
+    def fwd(self, transposed, feats, weight, bias, out, conv_ws, flags=0, stream=None) -> None:
+        Cin, Cout = weight.shape[1], weight.shape[2]
+        _check(lib().vg_sparse_conv3d_fwd(ctypes.byref(self.m), int(transposed), _dtype_code(weight), _p(feats),
+                                          _p(weight), _p(bias), _p(out), Cin, Cout, flags, _p(conv_ws),
+                                          conv_ws.numel(), _s(stream)), "vg_sparse_conv3d_fwd")
+
+    def bwd(self, transposed, grad_out, feats, weight, grad_feats, grad_weight, grad_bias, conv_ws, flags=0,
+            stream=None) -> None:
+        Cin, Cout = weight.shape[1], weight.shape[2]
+        _check(lib().vg_sparse_conv3d_bwd(ctypes.byref(self.m), int(transposed), _dtype_code(weight), _p(grad_out),
+                                          _p(feats), _p(weight), _p(grad_feats), _p(grad_weight), _p(grad_bias),
+                                          Cin, Cout, flags, _p(conv_ws), conv_ws.numel(), _s(stream)),
+               "vg_sparse_conv3d_bwd")
+

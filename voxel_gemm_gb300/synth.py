@@ -69,6 +69,10 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     # batch 1, 1024^3, 8 random spheres/tori, 64-bit hash keys; fp16
     _mk("b1_r1024_shapes_c64_f16", 1, 1024, 8, ("sphere", "torus"), 64, "f16", 4,
         key_flag=KEY64),
+    # a smaller case of the 512^3 C = 1024 kernels (256^3 grid, same generator), for
+    # counter captures that must stay a few GB on the device; its DRAM bytes per valid
+    # pair scale to the large case
+    _mk("b1_r256_shapes_c1024_bf16", 1, 256, 6, ("sphere", "torus"), 1024, "bf16", 3),
     # small inference case (forward only, few voxels): batch 1, 64^3, 2 random spheres,
     # C = 256 bf16 -- fewer (tile, channel block) units than SMs
     _mk("b1_r64_spheres_c256_bf16_infer", 1, 64, 2, ("sphere",), 256, "bf16", 5),
