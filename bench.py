@@ -809,6 +809,34 @@ def rows_budget(wl):
     return int(max(256, min(65536, 2e9 / per_row)))
 
 
+def run_ncu_step(args):
+    """The command a profiler attaches to: --warmup eager steps, then one more, of the
+    workload's map build + forward + input gradient + weight/bias gradient on one
+    stream with one conv workspace (per step the kernels launch in that order)."""
+    import torch
+    from voxel_gemm_gb300 import ops, synth
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    coords = torch.from_numpy(synth.make_coords(wl)).to(dev)
+    N = coords.shape[0]
+    f, W, b, dY = synth.make_tensors(wl, N, device=dev)
+    dt = f.dtype
+    m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag)
+    ws = ops.conv_workspace(N, wl.cin, wl.cout, dt)
+    out = torch.empty(N, wl.cout, dtype=dt, device=dev)
+    dX = torch.empty(N, wl.cin, dtype=dt, device=dev)
+    dW = torch.empty_like(W)
+    db = torch.empty_like(b)
+    for _ in range(args.warmup + 1):
+        m.build(coords, s)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=s)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=s)
+    s.synchronize()
+    assert m.status(s) == ops.VG_OK and ops.vg_conv_status(ws, s) == ops.VG_OK
+    print(json.dumps({"ncu_step": wl.name, "N": N}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -821,7 +849,12 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each call eagerly instead of replaying a CUDA graph")
     ap.add_argument("--one-stream", action="store_true",
                     help="issue the step's conv passes one after the other on one stream")
+    ap.add_argument("--ncu-step", action="store_true",
+                    help="run --warmup + 1 eager steps on one stream and exit (for profilers)")
     args = ap.parse_args()
+    if args.ncu_step:
+        run_ncu_step(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

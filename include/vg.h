@@ -78,8 +78,9 @@ extern "C" {
  * read with a 10-bit mantissa, products accumulated in fp32), as the pages'
  * allow_tf32 switch does ("From CUDA to Triton: Triton JIT and autotuning",
  * §六 6.2: allow_tf32 is part of the autotune key and of the kernel arguments).
- * Applies to fp32 with Cin and Cout multiples of 32; otherwise, and without the
- * flag, fp32 runs on the exact FFMA path. */
+ * Applies to fp32 with Cin and Cout multiples of 32 (forward, input gradient and
+ * weight gradient); otherwise, and without the flag, fp32 runs on the exact FFMA
+ * path. */
 #define VG_ALLOW_TF32       0x10u
 /* Convolution flag: on the tensor-core paths, keep one work unit per (128-row
  * tile, output-channel block) even when there are fewer such units than SMs.
@@ -173,8 +174,8 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
  * §二 call flow: the backward reuses the neighbour cache and returns feats.grad
  * and weight.grad).
  *   dtype: VG_F32 (fp32 FFMA path; with VG_ALLOW_TF32 and Cin, Cout multiples
- *          of 32 the forward and the input gradient run on the tensor cores as
- *          TF32), VG_F16 or VG_BF16 (tensor-core path when Cin and Cout are
+ *          of 32 all three passes run on the tensor cores as TF32), VG_F16 or
+ *          VG_BF16 (tensor-core path when Cin and Cout are
  *          multiples of 64, CUDA-core path otherwise).
  *   Cin and Cout must be multiples of 8 (VG_ERR_UNSUPPORTED otherwise); flags
  *   is 0 or a combination of VG_ALLOW_TF32 and VG_NO_SMALL_N_SPLIT (other bits:
@@ -193,8 +194,8 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
 VG_API size_t vg_conv_workspace_bytes(int64_t N, int Cin, int Cout, int dtype, unsigned flags);
 
 /* Host-only description of the convolution plan (no device work):
- *   info[0] = 1 on the 16-bit tensor-core path, 2 when the fp32 forward and input
- *   gradient run on the tensor cores as TF32, else 0, info[1] = split-K chunks of the weight
+ *   info[0] = 1 on the 16-bit tensor-core path, 2 when the fp32 passes run on the
+ *   tensor cores as TF32, else 0, info[1] = split-K chunks of the weight
  *   gradient, info[2] = kernels launched by a forward call, info[3] = kernels
  *   launched by a backward call producing all three gradients (memsets not
  *   counted).  sm_count as in vg_nbrmap_describe (the split-K chunk count and

@@ -266,7 +266,8 @@ def test_tf32_sphere_workload():
     assert errs["out"] > 1e-5  # the TF32 path really ran (the FFMA path is ~3e-7 on this case)
 
 
-@pytest.mark.parametrize("cin,cout", [(32, 32), (64, 64), (64, 128), (128, 64), (192, 64), (32, 96), (256, 256)])
+@pytest.mark.parametrize("cin,cout", [(32, 32), (64, 64), (64, 128), (128, 64), (192, 64), (32, 96), (256, 256),
+                                      (160, 512)])
 def test_tf32_ragged_and_shapes(cin, cout):
     coords = synth.random_coords(cin * 5 + cout, 1111, 2, 14, 14, 14)
     wl = synth.Workload("t", 2, 14, 0, ("sphere",), cin, cout, "f32", 13, 2.0)
@@ -337,3 +338,29 @@ def test_hilbert_row_order_gives_the_same_convolution():
     dW_ref, _ = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
     e_dw = rel_fro(f64(r["dW"][:, ci][:, :, co]), dW_ref)
     assert max(e_out, e_dx, e_dw) <= TOL[wl.dtype], (e_out, e_dx, e_dw)
+
+
+def test_tf32_weight_gradient_sampled_at_full_size():
+    # the 512^3 voxels with fp32 features under VG_ALLOW_TF32 (Cin = Cout = 256): the
+    # tensor-core TF32 weight gradient on 6912 full-sum dW entries and all of db
+    name = "b1_r512_shapes_c256_bf16"
+    base = synth.WORKLOADS[name]
+    wl = synth.Workload("tf32_512", base.B, base.res, base.shapes_per_sample, base.kinds, 256, 256, "f32",
+                        base.seed, 2.0)
+    coords = coords_of(name)
+    N = coords.shape[0]
+    nbr_ref, _ = oracle_map(name)
+    f, W, b, dY = synth.make_tensors(wl, N)
+    r = run_gpu(coords, wl.grid, f, W, b, dY, flags=ops.VG_ALLOW_TF32)
+    rng = np.random.default_rng(5)
+    ci = np.sort(rng.choice(256, size=16, replace=False))
+    co = np.sort(rng.choice(256, size=16, replace=False))
+    dW_ref, _ = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
+    _, db_ref = oracle_wgrad_cols(nbr_ref, f[:, :1], dY, np.arange(1), np.arange(256))
+    e_dw = rel_fro(f64(r["dW"][:, ci][:, :, co]), dW_ref)
+    e_db = rel_fro(f64(r["db"]), db_ref)
+    rows = np.sort(rng.choice(N, size=2048, replace=False))
+    e_out = rel_fro(f64(r["out"][rows][:, co]), oracle_fwd_rows(nbr_ref, rows, co, f, W, b))
+    assert max(e_dw, e_db, e_out) <= TF32_TOL, (e_dw, e_db, e_out)
+    assert e_dw > 1e-6  # TF32 products, not the exact FFMA path
+

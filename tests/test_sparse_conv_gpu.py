@@ -111,11 +111,16 @@ def test_sparse_conv_tf32(K, s):
     m.fwd(0, f_in.cuda(), W.cuda(), b.cuda(), out, ws, flags=fl)
     dY = torch.randn(m.n_out, 32)
     dX = torch.empty(m.n_in, 64, device="cuda")
-    m.bwd(0, dY.cuda(), f_in.cuda(), W.cuda(), dX, None, None, ws, flags=fl)
+    dW = torch.empty_like(W).cuda()
+    db = torch.empty(32, device="cuda")
+    m.bwd(0, dY.cuda(), f_in.cuda(), W.cuda(), dX, dW, db, ws, flags=fl)
     torch.cuda.synchronize()
+    assert ops.vg_conv_status(ws) == ops.VG_OK
     W27 = _pad27(W)
     assert rel_fro(f64(out), oracle.fwd(down, f64(f_in), W27, f64(b))) <= TF32_TOL
     assert rel_fro(f64(dX), oracle.dgrad_scatter_to(down, f64(dY), W27, m.n_in)) <= TF32_TOL
+    dW_ref, db_ref = oracle.wgrad(down, f64(f_in), f64(dY))
+    assert rel_fro(f64(dW), dW_ref[: K ** 3]) <= TF32_TOL and rel_fro(f64(db), db_ref) <= TF32_TOL
 
 
 def test_sparse_map_rejects_bad_sites_and_arguments():

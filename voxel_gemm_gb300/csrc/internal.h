@@ -131,6 +131,9 @@ int tc_pack_weights(const void* W, int dtype, int Cin, int Cout, int mode, int t
                     const uint32_t* nbr_status, cudaStream_t s);
 int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
 int tc_wgrad(const WgradPass& p, cudaStream_t s);
+// TF32 weight gradient (fp32 features, Cin and Cout multiples of 32): split-K chunks and the pass.
+int tf32_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps = 27);
+int tf32_wgrad(const WgradPass& p, cudaStream_t s);
 // Scratch of the weight gradient: dY rows copied into processing order (zero rows
 // pad the last tile) when Cout takes the wide-N kernel, else 0 bytes.
 size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout);

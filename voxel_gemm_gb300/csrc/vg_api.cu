@@ -42,6 +42,7 @@ static int conv_plan2(int64_t n_fwd, int64_t n_dgrad, int taps, int Cin, int Cou
     const size_t gpart = std::max(p.ks_fwd > 1 ? (size_t)p.ks_fwd * rows_pad * Cout * 4 : 0,
                                   p.ks_dgrad > 1 ? (size_t)p.ks_dgrad * rows_pad_d * Cin * 4 : 0);
     p.splits = p.tensor_core ? tc_wgrad_splits(N, Cin, Cout, p.sms, taps)
+               : p.tf32      ? tf32_wgrad_splits(N, Cin, Cout, p.sms, taps)
                              : simt_wgrad_splits(N, Cin, Cout, p.sms, taps);
     const size_t wbytes = (size_t)kTaps * Cin * Cout * dtype_size(dtype);
     size_t o = 0;
@@ -136,7 +137,7 @@ static int run_wgrad(const ConvPlan& p, const Side& sd, int taps, int dtype, con
     w.sms = p.sms;
     w.taps = taps;
     w.err = err;
-    return p.tensor_core ? tc_wgrad(w, s) : simt_wgrad(w, s);
+    return p.tensor_core ? tc_wgrad(w, s) : (p.tf32 ? tf32_wgrad(w, s) : simt_wgrad(w, s));
 }
 
 static int check_common(const void* nbr_ws, const uint32_t* nbr, const uint32_t* mask, int64_t N,
@@ -221,6 +222,8 @@ int vg_conv_describe(int64_t N, int Cin, int Cout, int dtype, unsigned flags, in
     info[1] = p.splits;
     const int dgrad_launches = p.tensor_core || p.tf32 ? tc_fwd_launches(p.ks_dgrad) : 1;
     info[2] = N > 0 ? (p.tensor_core || p.tf32 ? tc_fwd_launches(p.ks_fwd) : 1) : 0;
+    // backward: input gradient, then dW (GEMM + split reduce; + the dY sort on the 16-bit
+    // path when Cout >= 128) and db (partials + reduce)
     info[3] = N > 0 ? (p.tensor_core ? dgrad_launches - 2 + tc_bwd_launches(Cout) : dgrad_launches + 2 + 2) : 0;
     return VG_OK;
 }
