@@ -148,3 +148,68 @@ def test_sparse_map_empty_input():
           device="cuda"), W, None, dW, db, ws)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dW) == 0 and torch.count_nonzero(db) == 0
+
+
+def test_sparse_map_large_grid_and_hilbert_order():
+    # a grid of more than 2^31 cells (64-bit hash and candidate keys) with the Hilbert
+    # row order: the map stays bit-exact and a bf16 strided pass stays within bound
+    grid = (3, 1100, 1000, 900)
+    coords = synth.random_coords(91, 3000, *grid)
+    # cluster half of the voxels so that windows hold several inputs
+    coords[:1500, 1:] = (coords[:1500, 1:] % 16) + 500
+    coords = np.unique(coords, axis=0)
+    coords = coords[np.random.default_rng(1).permutation(len(coords))].astype(np.int32)
+    co, down, up = oracle.sparse_map(coords, *grid, 3, 2)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, 3, 2, flags=ops.VG_ORDER_HILBERT)
+    assert m.n_out == co.shape[0]
+    assert np.array_equal(m.coords_out().cpu().numpy(), co)
+    assert np.array_equal(u32(m.down()), down) and np.array_equal(u32(m.up()), up)
+    g = torch.Generator().manual_seed(4)
+    f = torch.randn(coords.shape[0], 64, generator=g).bfloat16()
+    W = (torch.randn(27, 64, 64, generator=g) * 0.03).bfloat16()
+    ws = m.workspace(0, 64, 64, torch.bfloat16)
+    out = torch.empty(m.n_out, 64, dtype=torch.bfloat16, device="cuda")
+    m.fwd(0, f.cuda(), W.cuda(), None, out, ws)
+    torch.cuda.synchronize()
+    ref = oracle.fwd(down, f64(f), _pad27(W), None)
+    assert rel_fro(f64(out), ref) <= TOL["bf16"]
+
+
+def test_sparse_conv_16bit_cuda_core_channels_and_graph_capture():
+    # 16-bit channels that are not multiples of 64 take the CUDA-core kernels; the
+    # strided forward and backward replay from a CUDA graph with the same bits
+    grid = (1, 20, 20, 20)
+    coords, f_in, W, b = _problem(3, 2, 1500, grid, 40, 24, "f16", 5)
+    co, down, up = oracle.sparse_map(coords, *grid, 3, 2)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, 3, 2)
+    dt = torch.float16
+    fi, Wd, bd = f_in.cuda(), W.cuda(), b.cuda()
+    dY = torch.randn(m.n_out, 24, generator=torch.Generator().manual_seed(6)).half().cuda()
+    ws = m.workspace(0, 40, 24, dt)
+    out = torch.empty(m.n_out, 24, dtype=dt, device="cuda")
+    dX = torch.empty(m.n_in, 40, dtype=dt, device="cuda")
+    dW = torch.empty_like(Wd)
+    db = torch.empty_like(bd)
+    s = torch.cuda.Stream()
+
+    def step():
+        m.fwd(0, fi, Wd, bd, out, ws, stream=s)
+        m.bwd(0, dY, fi, Wd, dX, dW, db, ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    eager = [t.clone() for t in (out, dX, dW, db)]
+    W27 = _pad27(W)
+    assert rel_fro(f64(out), oracle.fwd(down, f64(f_in), W27, f64(b))) <= TOL["f16"]
+    assert rel_fro(f64(dX), oracle.dgrad_scatter_to(down, f64(dY), W27, m.n_in)) <= TOL["f16"]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for t in (out, dX, dW, db):
+        t.zero_()
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    for a_, b_ in zip(eager, (out, dX, dW, db)):
+        assert torch.equal(a_, b_)
