@@ -9,7 +9,8 @@
 // skipping taps no row of the tile uses.  The backward reuses the same
 // neighbour cache ("Contribution Tasks — JeffreyXiang/FlexGEMM", §二 call flow).
 //
-// GB300 design (one CTA per SM, persistent over (128-row tile, N block) units):
+// GB300 design (one CTA per SM, two for tiles up to 128 columns; persistent over
+// (128-row tile, N block) units):
 //   warps 0-3  gather: per tap and 128-byte K block (64 16-bit or 32 fp32
 //              channels), 128 rows x 128 B of the
 //              feature matrix via 16-byte cp.async with zero fill for missing
@@ -56,11 +57,20 @@ int choose_bn(int ndim) {
     return 32;  // TF32 only (channels multiples of 32)
 }
 
+// Tiles up to 128 columns are issue-bound at the single MMA thread (four short
+// MMAs per stage): two CTAs share each SM there, with 3 stages each at BN <= 64
+// and 2 stages + 2 accumulator buffers at BN = 128, so that two MMA threads feed
+// each tensor core (measured: forward 0.0389 -> 0.0305 ms at 25k voxels and
+// 1.734 -> 1.600 ms at 4.9M, C = 64; 0.258 -> 0.195 ms at 319k voxels, C = 128;
+// 4 stages with one CTA per SM: no gain).
+template <int BN>
+constexpr int ctas_per_sm() { return BN <= 128 ? 2 : 1; }
+
 template <int BN>
 struct Cfg {
-    static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 6 : 8);  // pipeline stages
+    static constexpr int S = BN == 256 ? 4 : (BN == 128 ? 2 : 3);  // pipeline stages
     static constexpr int kBBytes = BN * kKBytes;
-    static constexpr int NBUF = BN <= 128 ? 4 : 2;                  // TMEM accumulator buffers
+    static constexpr int NBUF = BN <= 64 ? 4 : 2;                   // TMEM accumulator buffers
     static constexpr int kTmemCols = NBUF * BN;                      // 128, 256 or 512 columns
     static constexpr size_t kSmemA = (size_t)S * kABytes;
     static constexpr size_t kSmemB = (size_t)S * kBBytes;
@@ -154,7 +164,7 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&acc)[
 }
 
 template <int BN, int DT>
-__global__ void __launch_bounds__(kThreads, 1) k_gather_gemm_tc(TcArgs a) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(TcArgs a) {
     using C = Cfg<BN>;
     constexpr int S = C::S;
     constexpr int ES = Elt<DT>::size;
@@ -499,7 +509,7 @@ int launch_tc(const TcArgs& a, cudaStream_t s) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
     const int64_t units = a.num_tiles * (a.Ndim / BN) * a.ksplit;
-    const int grid = (int)std::min<int64_t>(units, plan_sms(0));
+    const int grid = (int)std::min<int64_t>(units, (int64_t)ctas_per_sm<BN>() * plan_sms(0));
     kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
@@ -551,6 +561,9 @@ void launch_split_reduce(const TcArgs& a, int sms, cudaStream_t s) {
 
 }  // namespace
 
+// (Counted against the SM count, not the resident CTAs: at BN <= 128 two CTAs
+// share an SM, and splitting units that already fill the SMs once was measured
+// slower -- 25k voxels, C = 64: 0.0305 -> 0.045 ms.)
 int tc_gather_splits(int64_t n, int Ndim, int sms) {
     const int64_t units = (n + kBM - 1) / kBM * (Ndim / choose_bn(Ndim));
     if (units == 0 || units >= sms) return 1;

@@ -20,6 +20,7 @@
 // Each unit writes an fp32 partial [128 x BN] for its chunk; a second kernel sums
 // the chunks in a fixed order (bitwise deterministic).
 //
+// Persistent CTAs, one per SM (two at narrow tiles, see WCfg below).
 // Warp roles as in the forward kernel: warps 0-3 gather A with 16-byte cp.async
 // (zero fill; each thread's copies arrive on the stage barrier by themselves),
 // warp 4 issues tcgen05.mma, warps 5-8 store the partials.  B (dY) rows are
@@ -49,20 +50,26 @@ constexpr int kThreads = 288;
 // The larger MU, the fewer times dY is re-read (measured: 7 blocks at Cout = 64
 // cut DRAM reads from 7.0 to about 2 GB at 4.9 M voxels; 4 blocks at Cout = 128
 // were slower than 2).
-template <int BN>
+// TWO = two CTAs per SM, each with half the stages and one accumulator buffer, so
+// that one CTA's MMAs run while the other's epilogue or gather waits.  Always at
+// Cout = 128 (measured at 319k voxels: 0.447 -> 0.384 ms); at Cout = 64 only when
+// the MU = 7 units cannot fill the SMs, with MU = 3 (25k voxels: 0.061 -> 0.054 ms;
+// at 4.9 M voxels MU = 3 re-reads dY more often and took 2.96 instead of 2.48 ms).
+template <int BN, bool TWO>
 struct WCfg {
-    static constexpr int MU = BN == 64 ? 7 : 2;
+    static constexpr int MU = BN == 64 ? (TWO ? 3 : 7) : 2;
     static constexpr int R = BN == 64 ? 32 : 64;           // rows per stage (K of the MMA)
     static constexpr int RQ = R / 16;                       // rows per gather thread
     static constexpr int kAccCols = MU * BN;
-    static constexpr int NBUF = 2 * kAccCols <= 512 ? 2 : 1;
+    static constexpr int NBUF = TWO ? 1 : (2 * kAccCols <= 512 ? 2 : 1);
     static constexpr int kTmemCols = NBUF * kAccCols <= 256 ? 256 : 512;
     static constexpr int kABytes = 2 * R * 128;             // two 64-channel blocks x R rows
     static constexpr int kBBytes = (BN / 64) * R * 128;
     static constexpr int kStageBytes = MU * kABytes + kBBytes;
-    static constexpr int S = 196608 / kStageBytes;          // 192 KB of stages
+    static constexpr int S = (TWO ? 98304 : 196608) / kStageBytes;  // 96 or 192 KB of stages
     static constexpr int kNumBars = 2 * S + 5;
     static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 4 * S + 16;
+    static_assert(!TWO || (kTmemCols <= 256 && 2 * kSmem <= 232448), "two CTAs must fit one SM");
 };
 
 struct WgArgs {
@@ -186,11 +193,11 @@ k_sort_rows(const uint16_t* __restrict__ src, const uint32_t* __restrict__ sorte
     }
 }
 
-template <int BN, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
+template <int BN, bool BF16, bool TWO>
+__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
     // B by TMA from the sorted dY copy when the tile is wide (R = 64 rows, box 64 x 64)
     constexpr bool kTmaB = BN >= 128;
-    using C = WCfg<BN>;
+    using C = WCfg<BN, TWO>;
     constexpr int S = C::S;
     constexpr int MU = C::MU;
     constexpr int NBUF = C::NBUF;
@@ -472,10 +479,10 @@ EncodeTiled encode_tiled() {
     return fn;
 }
 
-template <int BN, bool BF16>
+template <int BN, bool BF16, bool TWO>
 int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream_t s) {
-    using C = WCfg<BN>;
-    auto kern = k_wgrad_tc<BN, BF16>;
+    using C = WCfg<BN, TWO>;
+    auto kern = k_wgrad_tc<BN, BF16, TWO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
     CUtensorMap tm;
@@ -495,20 +502,17 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream
     }
     const int MG = (num_munits(a.Cin, a.taps) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
-    const int grid = (int)std::min<int64_t>(units, sms);
+    const int grid = (int)std::min<int64_t>(units, (int64_t)(TWO ? 2 : 1) * sms);
     kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
     return VG_OK;
 }
 
-}  // namespace
-
-// Split-K chunk count: about four work units per SM and chunks of at most 256
-// tiles (the units running side by side then stream the same rows through L2;
-// measured at 602k voxels, C = 1024: 2 chunks 17.6 ms, 8 chunks 16.1 ms), at
-// least 4 tiles per chunk (every chunk non-empty), partial sums capped at 1 GiB.
-int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
-    const int bn = wg_bn(Cout);
-    const int mu = bn == 64 ? WCfg<64>::MU : (bn == 128 ? WCfg<128>::MU : WCfg<256>::MU);
+// Split-K chunk count for M blocks of mu: about four work units per SM and
+// chunks of at most 256 tiles (the units running side by side then stream the
+// same rows through L2; measured at 602k voxels, C = 1024: 2 chunks 17.6 ms,
+// 8 chunks 16.1 ms), at least 4 tiles per chunk (every chunk non-empty), partial
+// sums capped at 1 GiB.
+int64_t wgrad_splits_mu(int64_t n, int Cin, int Cout, int sms, int taps, int bn, int mu) {
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
     const int64_t MG = (num_munits(Cin, taps) + mu - 1) / mu;
     const int64_t per_split = MG * (Cout / bn);
@@ -518,7 +522,25 @@ int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
     const int64_t tpc = (T + S - 1) / S;
-    return (int)((T + tpc - 1) / tpc);
+    return (T + tpc - 1) / tpc;
+}
+
+// Two CTAs per SM: always at 128 columns; at 64 columns when the MU = 7 units
+// (M groups x chunks) number fewer than the SMs.
+bool wgrad_two_cta(int64_t n, int Cin, int Cout, int sms, int taps) {
+    const int bn = wg_bn(Cout);
+    if (bn != 64) return bn == 128;
+    const int64_t MG = (num_munits(Cin, taps) + WCfg<64, false>::MU - 1) / WCfg<64, false>::MU;
+    return MG * (Cout / bn) * wgrad_splits_mu(n, Cin, Cout, sms, taps, bn, WCfg<64, false>::MU) < sms;
+}
+
+}  // namespace
+
+int tc_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
+    const int bn = wg_bn(Cout);
+    const bool two = wgrad_two_cta(n, Cin, Cout, sms, taps);
+    const int mu = bn == 64 ? (two ? WCfg<64, true>::MU : WCfg<64, false>::MU) : WCfg<256, false>::MU;
+    return (int)wgrad_splits_mu(n, Cin, Cout, sms, taps, bn, mu);
 }
 
 size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout) {
@@ -559,9 +581,22 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         }
         int st;
         switch (bn) {
-            case 256: st = bf16 ? launch_wgrad<256, true>(a, dys, p.sms, s) : launch_wgrad<256, false>(a, dys, p.sms, s); break;
-            case 128: st = bf16 ? launch_wgrad<128, true>(a, dys, p.sms, s) : launch_wgrad<128, false>(a, dys, p.sms, s); break;
-            default: st = bf16 ? launch_wgrad<64, true>(a, dys, p.sms, s) : launch_wgrad<64, false>(a, dys, p.sms, s); break;
+            case 256:
+                st = bf16 ? launch_wgrad<256, true, false>(a, dys, p.sms, s)
+                          : launch_wgrad<256, false, false>(a, dys, p.sms, s);
+                break;
+            case 128:
+                st = bf16 ? launch_wgrad<128, true, true>(a, dys, p.sms, s)
+                          : launch_wgrad<128, false, true>(a, dys, p.sms, s);
+                break;
+            default:
+                if (wgrad_two_cta(p.n, p.Cin, p.Cout, p.sms, p.taps))
+                    st = bf16 ? launch_wgrad<64, true, true>(a, dys, p.sms, s)
+                              : launch_wgrad<64, false, true>(a, dys, p.sms, s);
+                else
+                    st = bf16 ? launch_wgrad<64, true, false>(a, dys, p.sms, s)
+                              : launch_wgrad<64, false, false>(a, dys, p.sms, s);
+                break;
         }
         if (st != VG_OK) return st;
         launch_reduce_splits(p.partial, p.splits, (int64_t)p.taps * p.Cin * p.Cout, (int64_t)kTaps * p.Cin * p.Cout,
