@@ -1,6 +1,6 @@
 """Benchmark: one step = the whole submanifold-conv hot path on one batch of
 seeded synthetic voxels, through the C ABI:
-    neighbour-map build (hash, probe, row-order sort, tile masks)
+    neighbour-map build (column index or hash table, probe, row-order sort, tile masks)
     -> forward, input gradient, weight and bias gradient (three streams after
        the map build, each call with its own conv workspace; --one-stream runs
        them one after the other)
@@ -490,7 +490,9 @@ def run_workload(args, wl, rank, world, dev, flush, full):
                                   "bwd": cplan["launches_bwd"],
                                   "gradient_sum": reducer.launches if reducer else 0},
         "path": {"tensor_core": bool(cplan["tensor_core"]), "wgrad_splits": splits,
-                 "hash_keys": 64 if nplan["key64"] else 32, "sort_passes": nplan["sort_passes"]},
+                 "map_index": nplan["index"],
+                 "hash_keys": (64 if nplan["key64"] else 32) if nplan["index"] == "hash" else None,
+                 "sort_passes": nplan["sort_passes"]},
         "launch": ("eager" if not use_graph else "CUDA graph replay of the step's C-ABI calls")
                   + ("" if one_stream else "; fwd, dgrad and wgrad+db on three streams after the map build"),
     })

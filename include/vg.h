@@ -71,6 +71,17 @@ extern "C" {
 #define VG_KEY32            0x1u   /* force 32-bit hash keys (needs B*X*Y*Z < 2^32)    */
 #define VG_KEY64            0x2u   /* force 64-bit hash keys                            */
 #define VG_ORDER_HILBERT    0x4u   /* row order from the Hilbert code instead of Morton  */
+/* Map-build flags: how the probe finds a voxel's neighbours.  The hash table
+ * is the pages' method.  The column index counts the voxels of every (b, x, y)
+ * column, prefix-sums the counts, stores each column's voxels sorted by z, and
+ * searches a voxel's 9 neighbouring columns for z - 1, z, z + 1; it needs
+ * B*X*Y <= 2^28.  By default the column index is used when the hash table would
+ * exceed 64 MiB (so would not stay in the GPU's L2) and B*X*Y <= 8 N + 2^20;
+ * VG_MAP_HASH or VG_MAP_COLUMNS forces one (both: VG_ERR_INVALID_ARG;
+ * VG_MAP_COLUMNS on a larger grid: VG_ERR_UNSUPPORTED).  The map, the row order
+ * and the tiles are identical either way. */
+#define VG_MAP_HASH         0x8u
+#define VG_MAP_COLUMNS      0x40u
 /* Testing aid: size the hash table below N so that the overflow path
  * (VG_ERR_HASH_FULL) can be exercised from the host. */
 #define VG_TEST_SMALL_HASH  0x100u
@@ -107,12 +118,13 @@ VG_API int vg_version(void);
  * module table rows kernels.cuda.hash and kernels.cuda.spconv; init_hashmap picks
  * uint32 or uint64 keys by grid volume).  Reading taken: 64-bit keys iff
  * B*X*Y*Z >= 2^30, unless VG_KEY32/VG_KEY64 forces the width; the map itself is
- * identical either way.
+ * identical either way, and identical again when a column index replaces the
+ * hash table (VG_MAP_HASH).
  * ====================================================================================== */
 
 /* Bytes of device workspace vg_nbrmap_build needs for these sizes and flags
  * (0 if the arguments are invalid).  The workspace is the neighbour cache: it
- * holds the hash table, the sorted row order and the per-tile masks, and must
+ * holds the hash table (or the column index), the sorted row order and the per-tile masks, and must
  * stay alive and unmodified while convolutions use the map. */
 VG_API size_t vg_nbrmap_workspace_bytes(int64_t N, int B, int X, int Y, int Z, unsigned flags);
 
@@ -157,7 +169,8 @@ VG_API const uint32_t* vg_nbrmap_tile_mask(const void* ws, int64_t N);
 VG_API const uint32_t* vg_nbrmap_sorted_nbr(const void* ws, int64_t N);
 
 /* Host-only description of the build plan (no device work):
- *   info[0] = 1 if the hash keys are 64-bit, info[1] = significant bits of the
+ *   info[0] = how neighbours are looked up: 0 hash table with 32-bit keys, 1 hash
+ *   table with 64-bit keys, 2 column index (see VG_MAP_HASH); info[1] = significant bits of the
  *   sort key above, info[2] = radix-sort passes, info[3] = kernels launched by
  *   vg_nbrmap_build (memsets not counted).
  *   sm_count: SMs of the device the plan is for; 0 = the current device's (the

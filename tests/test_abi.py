@@ -40,8 +40,8 @@ def test_host_only_queries(ops):
     assert ops.vg_version() >= 100
     assert ops.vg_strerror(ops.VG_ERR_DUPLICATE_COORD) == "duplicate coordinate"
     assert ops.vg_strerror(12345) == "unknown status"
-    n32 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, 0)
-    n64 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, ops.VG_KEY64)
+    n32 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, ops.VG_MAP_HASH)
+    n64 = ops.vg_nbrmap_workspace_bytes(1000, 1, 64, 64, 64, ops.VG_KEY64 | ops.VG_MAP_HASH)
     assert n64 > n32 > 0
     assert ops.vg_nbrmap_workspace_bytes(-1, 1, 8, 8, 8, 0) == 0
     assert ops.vg_nbrmap_workspace_bytes(10, 0, 8, 8, 8, 0) == 0
@@ -58,14 +58,50 @@ def test_host_only_queries(ops):
                          (1, 512, 0 + 27 + 5), (1, 1024, 0 + 27 + 5), (1, 2, 0 + 27 + 3)]:
         d = ops.vg_nbrmap_describe(1000, B, R, R, R)
         assert d["sort_bits"] == bits and d["sort_passes"] == (bits + 7) // 8, (B, R, d)
-    # kernels per build: insert, probe, keys, the radix passes, tile rows, and above
-    # 2^17 voxels one more pass ordering the tiles region by region
-    assert ops.vg_nbrmap_describe(1 << 17, 1, 512, 512, 512)["launches"] == 4 + 4
-    assert ops.vg_nbrmap_describe((1 << 17) + 1, 1, 512, 512, 512)["launches"] == 4 + 4 + 1
+    # kernels per build: (hash) insert, probe, keys or (column index) count, scan,
+    # scatter, rank, probe, keys; the radix passes, tile rows, and above 2^17
+    # voxels one more pass ordering the tiles region by region
+    H = ops.VG_MAP_HASH
+    assert ops.vg_nbrmap_describe(1 << 17, 1, 512, 512, 512, H)["launches"] == 4 + 4
+    assert ops.vg_nbrmap_describe((1 << 17) + 1, 1, 512, 512, 512, H)["launches"] == 4 + 4 + 1
+    C = ops.VG_MAP_COLUMNS
+    assert ops.vg_nbrmap_describe(1 << 17, 1, 512, 512, 512, C)["launches"] == 7 + 4
+    assert ops.vg_nbrmap_describe((1 << 17) + 1, 1, 512, 512, 512, C)["launches"] == 7 + 4 + 1
     # the 64-bit hash path leaves the plan otherwise unchanged
-    d32 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY32)
-    d64 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY64)
+    d32 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY32 | H)
+    d64 = ops.vg_nbrmap_describe(5000, 1, 512, 512, 512, ops.VG_KEY64 | H)
     assert (d32["key64"], d64["key64"]) == (0, 1) and d32["sort_passes"] == d64["sort_passes"]
+    assert d32["index"] == d64["index"] == "hash"
+
+
+def test_column_index_choice(ops):
+    """Column index by default when the hash table would exceed 64 MiB and the
+    (b, x, y) columns number at most 8 N + 2^20 (and at most 2^28); VG_MAP_HASH
+    and VG_MAP_COLUMNS force one or the other."""
+    d = ops.vg_nbrmap_describe
+    assert d(4_915_386, 1, 1024, 1024, 1024)["index"] == "columns"   # 268 MB table
+    assert d(602_492, 1, 512, 512, 512)["index"] == "hash"           # 16 MB table
+    assert d(25_179, 4, 64, 64, 64)["index"] == "hash"
+    assert d(4_915_386, 1, 4096, 1024, 1024)["index"] == "columns"    # 2^22 columns <= 8 N + 2^20
+    assert d(4_915_386, 16, 4096, 1024, 1024)["index"] == "hash"      # 2^26 columns > 8 N + 2^20
+    assert d(4_915_386, 1, 1024, 1024, 1024, ops.VG_MAP_HASH)["index"] == "hash"
+    assert d(25_179, 4, 64, 64, 64, ops.VG_MAP_COLUMNS)["index"] == "columns"
+    assert d(3000, 8, 1024, 1024, 1024, ops.VG_MAP_COLUMNS)["index"] == "columns"  # 2^23 columns allowed when forced
+    assert d(4000, 1, 32, 32, 32, ops.VG_TEST_SMALL_HASH)["index"] == "hash"
+    with pytest.raises(RuntimeError):
+        d(1000, 1, 8, 8, 8, ops.VG_MAP_HASH | ops.VG_MAP_COLUMNS)
+    with pytest.raises(RuntimeError):
+        d(1000, 1, 1 << 15, 1 << 14, 8, ops.VG_MAP_COLUMNS)           # above 2^28 columns
+    assert d(1 << 30, 1, 1 << 15, 1 << 14, 8)["index"] == "hash"
+    # the column layout keeps its arrays 256-byte aligned for any size (else the
+    # query would return 0)
+    for n in (1, 2, 3, 255, 4097, 100_003, 4_915_386):
+        for grid in ((1, 8, 8, 8), (3, 65, 33, 17), (1, 1024, 1024, 1024), (2, 700, 301, 5)):
+            assert d(n, *grid, ops.VG_MAP_COLUMNS)["index"] == "columns"
+            assert ops.vg_nbrmap_workspace_bytes(n, *grid, ops.VG_MAP_COLUMNS) > 0, (n, grid)
+    # both layouts are valid workspaces of their own size
+    assert ops.vg_nbrmap_workspace_bytes(4_915_386, 1, 1024, 1024, 1024) > 0
+    assert ops.vg_nbrmap_workspace_bytes(4_915_386, 1, 1024, 1024, 1024, ops.VG_MAP_HASH) > 0
 
 
 @pytest.mark.parametrize("sms", [152, 148, 76])

@@ -75,8 +75,8 @@ def test_key_width_does_not_change_the_map():
     name = "b2_r256_shapes_c128_bf16"
     wl = synth.WORKLOADS[name]
     coords = coords_of(name)
-    m32, s32 = gpu_map(coords, wl.grid, ops.VG_KEY32)
-    m64, s64 = gpu_map(coords, wl.grid, ops.VG_KEY64)
+    m32, s32 = gpu_map(coords, wl.grid, ops.VG_KEY32 | ops.VG_MAP_HASH)
+    m64, s64 = gpu_map(coords, wl.grid, ops.VG_KEY64 | ops.VG_MAP_HASH)
     assert s32 == s64 == ops.VG_OK
     assert torch.equal(m32.nbr, m64.nbr) and torch.equal(m32.mask, m64.mask)
     assert torch.equal(m32.sorted_idx(), m64.sorted_idx())
@@ -95,11 +95,49 @@ def test_large_grid_forces_64bit_keys_and_matches():
     assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
 
 
+@pytest.mark.parametrize("name", MAP_WORKLOADS)
+def test_column_index_equals_hash_table(name):
+    """The (b, x, y) column index and the hash table must give the same map, row
+    order and tiles (the bit-exact test above covers whichever is the default)."""
+    wl = synth.WORKLOADS[name]
+    coords = coords_of(name)
+    n = coords.shape[0]
+    assert ops.vg_nbrmap_describe(n, *wl.grid, wl.key_flag | ops.VG_MAP_COLUMNS)["index"] == "columns"
+    assert ops.vg_nbrmap_describe(n, *wl.grid, wl.key_flag | ops.VG_MAP_HASH)["index"] == "hash"
+    mc, sc = gpu_map(coords, wl.grid, wl.key_flag | ops.VG_MAP_COLUMNS)
+    mh, sh = gpu_map(coords, wl.grid, wl.key_flag | ops.VG_MAP_HASH)
+    assert sc == sh == ops.VG_OK
+    assert torch.equal(mc.nbr, mh.nbr) and torch.equal(mc.mask, mh.mask)
+    assert torch.equal(mc.sorted_idx(), mh.sorted_idx()) and torch.equal(mc.tile_mask(), mh.tile_mask())
+    assert torch.equal(mc.sorted_nbr(), mh.sorted_nbr())
+
+
+@pytest.mark.parametrize("flags", [ops.VG_MAP_COLUMNS, ops.VG_MAP_HASH])
 @pytest.mark.parametrize("n", [1, 127, 128, 129, 4097, 5000])
-def test_ragged_sizes(n):
+def test_ragged_sizes(n, flags):
     coords = synth.random_coords(n, n, 2, 12, 12, 12)
     nbr_ref, mask_ref = oracle.nbrmap(coords, 2, 12, 12, 12)
-    m, st = gpu_map(coords, (2, 12, 12, 12))
+    m, st = gpu_map(coords, (2, 12, 12, 12), flags)
+    assert st == ops.VG_OK
+    assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
+
+
+@pytest.mark.parametrize("flags", [ops.VG_MAP_COLUMNS, ops.VG_MAP_HASH])
+def test_solid_block_and_long_columns(flags):
+    """Dense input: a solid 14^3 block (every tap of its inner voxels valid) and
+    full z-columns of 600 voxels, long enough for the column index's binary search."""
+    g = np.stack(np.meshgrid(np.arange(1, 15), np.arange(2, 16), np.arange(3, 17), indexing="ij"), -1).reshape(-1, 3)
+    solid = np.concatenate([np.zeros((g.shape[0], 1), np.int64), g], 1)
+    zs = np.arange(600)
+    cols = [np.stack([np.full(600, b), np.full(600, x), np.full(600, y), zs], 1)
+            for b, x, y in [(0, 20, 20), (0, 20, 21), (0, 21, 21), (1, 0, 0), (1, 0, 1), (1, 23, 23)]]
+    coords = np.concatenate([solid] + cols).astype(np.int32)
+    coords = coords[np.random.default_rng(5).permutation(coords.shape[0])]
+    grid = (2, 24, 24, 600)
+    assert ops.vg_nbrmap_describe(coords.shape[0], *grid, flags)["index"] == (
+        "hash" if flags == ops.VG_MAP_HASH else "columns")
+    nbr_ref, mask_ref = oracle.nbrmap(coords, *grid)
+    m, st = gpu_map(coords, grid, flags)
     assert st == ops.VG_OK
     assert np.array_equal(u32(m.nbr), nbr_ref) and np.array_equal(u32(m.mask), mask_ref)
 
@@ -110,13 +148,18 @@ def test_empty_map():
     assert m.status() == ops.VG_OK
 
 
-def test_duplicate_and_out_of_range_are_reported():
+@pytest.mark.parametrize("flags", [ops.VG_MAP_COLUMNS, ops.VG_MAP_HASH])
+def test_duplicate_and_out_of_range_are_reported(flags):
     c = np.array([[0, 1, 1, 1], [0, 2, 2, 2], [0, 1, 1, 1]], dtype=np.int32)
-    _, st = gpu_map(c, (1, 8, 8, 8))
+    _, st = gpu_map(c, (1, 8, 8, 8), flags)
     assert st == ops.VG_ERR_DUPLICATE_COORD
-    for bad in ([1, 0, 0, 0], [0, 8, 0, 0], [0, 0, -1, 0], [0, 0, 0, 9]):
+    # a duplicate among many voxels, in a long column
+    c = np.array([[0, 3, 4, z] for z in range(40)] + [[0, 3, 4, 17]], dtype=np.int32)
+    _, st = gpu_map(c, (1, 8, 8, 64), flags)
+    assert st == ops.VG_ERR_DUPLICATE_COORD
+    for bad in ([1, 0, 0, 0], [0, 8, 0, 0], [0, 0, -1, 0], [0, 0, 0, 9], [-1, 0, 0, 0]):
         c = np.array([[0, 1, 1, 1], bad], dtype=np.int32)
-        _, st = gpu_map(c, (1, 8, 8, 8))
+        _, st = gpu_map(c, (1, 8, 8, 8), flags)
         assert st == ops.VG_ERR_COORD_OUT_OF_RANGE
 
 

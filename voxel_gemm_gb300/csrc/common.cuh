@@ -55,6 +55,12 @@ struct NbrLayout {
     int curve = 0;           // curve of the row order: 0 z-order (Morton), 1 Hilbert
     int tile_passes = 1;     // radix passes of the tile region sort
     int64_t tile_blocks = 1; // blocks of one tile-sort pass
+    // column index (instead of the hash table): B*X*Y columns, their counts and
+    // starts, the scan's published chunk sums, and the voxels as {z, row}
+    int cols = 0;
+    int64_t ncols = 0, cchunks = 0;
+    size_t off_ccnt = 0, off_cpart = 0, off_cticket = 0, off_cstart = 0, off_carr = 0, off_cent_a = 0,
+           off_cent_b = 0, off_ccol_a = 0, off_ccol_b = 0, off_cpos = 0, off_crec = 0;
 };
 
 // Workspace layout of a regular (strided / transposed) convolution map: a header

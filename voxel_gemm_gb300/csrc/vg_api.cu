@@ -205,11 +205,12 @@ int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned flags, in
     const int st = nbr_layout(N, B, X, Y, Z, flags, sm_count, &l);
     if (st != VG_OK || !info) return st != VG_OK ? st : VG_ERR_INVALID_ARG;
     const int passes = nbr_sort_passes(l);
-    info[0] = l.key64;
+    info[0] = l.cols ? 2 : l.key64;
     info[1] = l.sort_bits;
     info[2] = passes;
-    // insert, probe, keys + digit counts, passes, tile rows, tile-order passes
-    info[3] = N > 0 ? 4 + passes + l.tile_passes : 0;
+    // hash: insert, probe, keys + digit counts; columns: count, scan, scatter, rank,
+    // probe, keys + digit counts; then the passes, tile rows and the tile-order passes
+    info[3] = N > 0 ? (l.cols ? 6 : 3) + passes + 1 + l.tile_passes : 0;
     return VG_OK;
 }
 

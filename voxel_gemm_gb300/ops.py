@@ -22,7 +22,8 @@ VG_OK, VG_ERR_INVALID_ARG, VG_ERR_COORD_OUT_OF_RANGE, VG_ERR_DUPLICATE_COORD = 0
 VG_ERR_HASH_FULL, VG_ERR_UNSUPPORTED, VG_ERR_WORKSPACE_TOO_SMALL, VG_ERR_CUDA = 4, 5, 6, 7
 VG_ERR_DEVICE_TIMEOUT = 8
 VG_F32, VG_F16, VG_BF16 = 0, 1, 2
-VG_KEY32, VG_KEY64, VG_ORDER_HILBERT, VG_TEST_SMALL_HASH = 0x1, 0x2, 0x4, 0x100
+VG_KEY32, VG_KEY64, VG_ORDER_HILBERT, VG_MAP_HASH, VG_MAP_COLUMNS = 0x1, 0x2, 0x4, 0x8, 0x40
+VG_TEST_SMALL_HASH = 0x100
 VG_CURVE_ZORDER, VG_CURVE_HILBERT = 0, 1
 VG_ALLOW_TF32, VG_NO_SMALL_N_SPLIT = 0x10, 0x20
 VG_NONE = 0xFFFFFFFF
@@ -200,7 +201,8 @@ def vg_subm_conv3d_bwd(nbr_ws, nbr, mask, grad_out, feats, weight, grad_feats, g
 def vg_nbrmap_describe(N, B, X, Y, Z, flags=0, sm_count=0) -> dict:
     info = (ctypes.c_int * 4)()
     _check(lib().vg_nbrmap_describe(N, B, X, Y, Z, flags, sm_count, info), "vg_nbrmap_describe")
-    return {"key64": info[0], "sort_bits": info[1], "sort_passes": info[2], "launches": info[3]}
+    return {"key64": 1 if info[0] == 1 else 0, "index": "columns" if info[0] == 2 else "hash",
+            "sort_bits": info[1], "sort_passes": info[2], "launches": info[3]}
 
 
 def vg_conv_describe(N, Cin, Cout, dtype, flags=0, sm_count=0) -> dict:
