@@ -106,6 +106,19 @@ def test_ragged_and_shapes(dtype, cin, cout):
     full_check(coords, (2, 14, 14, 14), f, W, b, dY, TOL[dtype])
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("cin,cout,n", [(256, 256, 1111), (64, 256, 1280), (256, 512, 1400), (512, 64, 600)])
+def test_wide_blocks_one_unit_per_tile(dtype, cin, cout, n):
+    """256-column output blocks with one unit per (tile, block) (no tap groups),
+    odd and even tile counts, with and without bias: every element against the oracle."""
+    coords = synth.random_coords(cin + cout + n, n, 1, 18, 18, 18)
+    N = coords.shape[0]
+    wl = synth.Workload("t", 1, 18, 0, ("sphere",), cin, cout, dtype, 21, 2.0)
+    f, W, b, dY = synth.make_tensors(wl, N)
+    full_check(coords, (1, 18, 18, 18), f, W, b, dY, TOL[dtype], flags=ops.VG_NO_SMALL_N_SPLIT)
+    full_check(coords, (1, 18, 18, 18), f, W, None, dY, TOL[dtype], flags=ops.VG_NO_SMALL_N_SPLIT)
+
+
 def test_bias_none_and_closed_form():
     # all-ones features and weights: out[i] = popcount(mask_i) * Cin exactly (small integers)
     coords = coords_of("b4_r64_spheres_c64_f16")
