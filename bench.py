@@ -420,26 +420,29 @@ def run_workload(args, wl, rank, world, dev, flush, full):
     h_db = torch.empty(pb.db.shape, dtype=pb.dt).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (h_coords, h_f, h_W, h_b, h_dY))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_dX, h_dW, h_db))
-    # Copies run on two more streams where the data dependences allow: features and
-    # weights go up while the map (which needs only the coordinates) is built, dY while
-    # the forward runs; `out` comes back during the backward and dX during the weight
-    # gradient.  The conv passes use the same streams as the device-only step.
+    # Copies run on two more streams where the data dependences allow.  Uploads go in
+    # the order the passes can start: the coordinates (the map build needs nothing
+    # else), the weights and bias, dY (the input gradient needs only dY and W), then
+    # the features (the forward and the weight gradient need them).  Each result
+    # comes back as soon as its pass ends: dX during the forward, out during the
+    # weight gradient, dW and db last (57 MB at C = 1024, where dX and out are 1.2 GB
+    # each).  The conv passes use the same streams as the device-only step.
     up = torch.cuda.Stream(device=dev)
     down = torch.cuda.Stream(device=dev)
 
     def e2e_eager():
-        ev_fwd_in, ev_bwd_in, ev_fwd, ev_dx = (torch.cuda.Event() for _ in range(4))
+        ev_dy_in, ev_f_in, ev_fwd, ev_dx = (torch.cuda.Event() for _ in range(4))
         with torch.cuda.stream(stream):
             pb.coords.copy_(h_coords, non_blocking=True)
         up.wait_stream(stream)
         down.wait_stream(stream)
         with torch.cuda.stream(up):
-            pb.f.copy_(h_f, non_blocking=True)
             pb.W.copy_(h_W, non_blocking=True)
             pb.b.copy_(h_b, non_blocking=True)
-            ev_fwd_in.record(up)
             pb.dY.copy_(h_dY, non_blocking=True)
-            ev_bwd_in.record(up)
+            ev_dy_in.record(up)
+            pb.f.copy_(h_f, non_blocking=True)
+            ev_f_in.record(up)
         m.build(pb.coords, stream)
         dx_stream = stream if one_stream else pb.s_dx
         dw_stream = stream if one_stream else pb.s_dw
@@ -447,19 +450,19 @@ def run_workload(args, wl, rank, world, dev, flush, full):
         if not one_stream:
             pb.s_dx.wait_stream(stream)
             pb.s_dw.wait_stream(stream)
-        stream.wait_event(ev_fwd_in)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0], stream=stream)
-        ev_fwd.record(stream)
-        dx_stream.wait_event(ev_bwd_in)
+        dx_stream.wait_event(ev_dy_in)
         ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, pb.dX, None, None, dx_ws,
                                stream=dx_stream)
         ev_dx.record(dx_stream)
+        stream.wait_event(ev_f_in)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, pb.f, pb.W, pb.b, pb.out, pb.ws[0], stream=stream)
+        ev_fwd.record(stream)
         with torch.cuda.stream(down):
-            down.wait_event(ev_fwd)
-            h_out.copy_(pb.out, non_blocking=True)
             down.wait_event(ev_dx)
             h_dX.copy_(pb.dX, non_blocking=True)
-        dw_stream.wait_event(ev_bwd_in)
+            down.wait_event(ev_fwd)
+            h_out.copy_(pb.out, non_blocking=True)
+        dw_stream.wait_event(ev_fwd)  # after the forward, so that `out` comes back during it
         ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, pb.dY, pb.f, pb.W, None, pb.dW, pb.db, dw_ws,
                                stream=dw_stream)
         for st in (up, down) if one_stream else (up, down, pb.s_dx, pb.s_dw):

@@ -511,7 +511,8 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream
 // chunks of at most 256 tiles (the units running side by side then stream the
 // same rows through L2; measured at 602k voxels, C = 1024: 2 chunks 17.6 ms,
 // 8 chunks 16.1 ms), at least 4 tiles per chunk (every chunk non-empty), partial
-// sums capped at 1 GiB.
+// sums capped at 768 MiB (at C = 1024: 6 chunks 13.79 ms, 4 chunks 13.89 ms,
+// 9 chunks (1 GiB) 13.97 ms, 18 chunks 14.66 ms).
 int64_t wgrad_splits_mu(int64_t n, int Cin, int Cout, int sms, int taps, int bn, int mu) {
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
     const int64_t MG = (num_munits(Cin, taps) + mu - 1) / mu;
@@ -519,7 +520,7 @@ int64_t wgrad_splits_mu(int64_t n, int Cin, int Cout, int sms, int taps, int bn,
     int64_t S = std::max<int64_t>(1, (4 * (int64_t)sms + per_split - 1) / per_split);
     S = std::max<int64_t>(S, (T + 255) / 256);
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
-    S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
+    S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(3) << 28) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
     const int64_t tpc = (T + S - 1) / S;
     return (T + tpc - 1) / tpc;
