@@ -19,6 +19,11 @@ constexpr uint32_t kErrRange = 1u;
 constexpr uint32_t kErrDup = 2u;
 constexpr uint32_t kErrFull = 4u;
 constexpr uint32_t kErrTimeout = 8u;
+// A conv pass's error record is the first word of a 256-byte block; further
+// words of that block hold the unit counters of the dynamically scheduled
+// kernels (zeroed before each launch).
+constexpr int kWgradUnitCounter = 16;
+constexpr int kGatherUnitCounter = 32;
 
 // Bound on mbarrier polls before a kernel gives up (~seconds at GB300 clocks).
 constexpr uint32_t kSpinLimit = 1u << 26;

@@ -44,6 +44,15 @@ using namespace ptx;
 
 constexpr int kThreads = 288;
 
+// Work units are handed out dynamically: thread 0 of the gather warps claims the
+// next unit from a global counter and publishes it in a 4-slot ring that the
+// gather, MMA and epilogue roles read in order (-1 ends the sequence).  A CTA
+// whose units hold sparse taps (few active tiles) thus takes more units; with
+// the fixed round-robin the busiest CTA had 18 % more tap-tiles than the mean
+// (602k voxels, C = 1024).
+constexpr int kUnitRing = 4;
+constexpr int kUnitReaders = 4 + 1 + 4;  // gather warps, the MMA thread, epilogue warps
+
 // One CTA work unit holds MU M blocks (MU accumulators of 128 x BN side by side
 // in TMEM, all sharing every dY stage) and streams stages of R sorted rows:
 //   Cout = 64: MU = 7 (448 columns), R = 32;  Cout >= 128: MU = 2, R = 64.
@@ -67,8 +76,9 @@ struct WCfg {
     static constexpr int kBBytes = (BN / 64) * R * 128;
     static constexpr int kStageBytes = MU * kABytes + kBBytes;
     static constexpr int S = (TWO ? 98304 : 196608) / kStageBytes;  // 96 or 192 KB of stages
-    static constexpr int kNumBars = 2 * S + 5;
-    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 4 * S + 16;
+    // full[S], empty[S], tfull[2], tempty[2], done, unit ring full[4] and empty[4]
+    static constexpr int kNumBars = 2 * S + 13;
+    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 8 * kUnitRing + 4 * S + 16;
     static_assert(!TWO || (kTmemCols <= 256 && 2 * kSmem <= 232448), "two CTAs must fit one SM");
 };
 
@@ -88,6 +98,7 @@ struct WgArgs {
     int taps;        // taps of the kernel (27, or 8): (tap, channel block) slots of the M blocks
     float* partial;  // [splits][27][Cin][Cout]
     uint32_t* err;
+    uint32_t* unit_ctr;  // next unit to claim (zero before the launch)
 };
 
 // Taps and channel offsets of M block m.  The 27 * (Cin/64) (tap, 64-channel
@@ -193,6 +204,17 @@ k_sort_rows(const uint16_t* __restrict__ src, const uint32_t* __restrict__ sorte
     }
 }
 
+// Warp-wide read of unit-ring slot `slot` (phase parity uph); lane 0 then releases
+// the slot.  -1 when the sequence has ended or the wait gave up.
+__device__ __forceinline__ int64_t read_unit(const volatile int64_t* s_unit, uint32_t ufull0, uint32_t uempty0,
+                                             uint32_t slot, uint32_t uph, int lane, const volatile uint32_t* abort) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(ufull0 + 8 * slot, uph, abort));
+    const int64_t u = ok ? s_unit[slot] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(uempty0 + 8 * slot);
+    return u;
+}
+
 template <int BN, bool BF16, bool TWO>
 __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
     // B by TMA from the sorted dY copy when the tile is wide (R = 64 rows, box 64 x 64)
@@ -209,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;  // stage g: MU A tiles, then the B tile
     uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)S * C::kStageBytes);
-    uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
+    volatile int64_t* s_unit = reinterpret_cast<volatile int64_t*>(bars + C::kNumBars);  // unit ring
+    uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars + kUnitRing);  // per stage: bit0 first, bit1 last
     uint32_t* s_tmem = s_info + S;
     volatile uint32_t* s_abort = s_tmem + 1;
 
@@ -219,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 2);
     const uint32_t done_bar = smem_u32(bars + 2 * S + 4);
+    const uint32_t ufull0 = smem_u32(bars + 2 * S + 5), uempty0 = smem_u32(bars + 2 * S + 5 + kUnitRing);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, 128 + 1);  // 128 copy arrivals + thread 0's info arrival
@@ -229,6 +253,10 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
             mbar_init(tempty0 + 8 * i, 4);
         }
         mbar_init(done_bar, 1);
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(ufull0 + 8 * i, 1);             // thread 0's publication of the slot
+            mbar_init(uempty0 + 8 * i, kUnitReaders);  // every reader of the slot
+        }
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -252,7 +280,16 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
         const int ch = p & 7;
         uint32_t it = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (uint32_t q = 0; ok; ++q) {
+            const uint32_t slot = q % kUnitRing, uph = (q / kUnitRing) & 1u;
+            if (p == 0) {  // claim the next unit once every reader is done with the slot's last one
+                const bool free_slot = mbar_wait(uempty0 + 8 * slot, uph ^ 1u, s_abort);
+                const int64_t uu = free_slot ? (int64_t)atomicAdd(a.unit_ctr, 1u) : units;
+                s_unit[slot] = uu < units ? uu : -1;
+                mbar_arrive(ufull0 + 8 * slot);
+            }
+            const int64_t u = read_unit(s_unit, ufull0, uempty0, slot, uph, lane, s_abort);
+            if (u < 0) break;
             const int mg = (int)(u % MG);
             const int64_t rest = u / MG;
             const int nb = (int)(rest % NB);
@@ -366,7 +403,12 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
             constexpr uint32_t lbo = kBlk;  // distance between 64-channel blocks
             uint32_t it = 0, ua = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
+            for (uint32_t q = 0; ok; ++q, ++ua) {
+                const uint32_t slot = q % kUnitRing, uph = (q / kUnitRing) & 1u;
+                if (!mbar_wait(ufull0 + 8 * slot, uph, s_abort)) { ok = false; break; }
+                const int64_t u = s_unit[slot];
+                mbar_arrive(uempty0 + 8 * slot);
+                if (u < 0) break;
                 const uint32_t buf = ua % NBUF;
                 if (!mbar_wait(tempty0 + 8 * buf, ((ua / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
@@ -408,7 +450,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
         const int q = warp & 3;
         uint32_t ua = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
+        for (uint32_t qi = 0;; ++qi, ++ua) {
+            const int64_t u = read_unit(s_unit, ufull0, uempty0, qi % kUnitRing, (qi / kUnitRing) & 1u, lane, s_abort);
+            if (u < 0) break;
             const int mg = (int)(u % MG);
             const int64_t rest = u / MG;
             const int nb = (int)(rest % NB);
@@ -570,6 +614,8 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.taps = p.taps;
         a.partial = p.partial;
         a.err = p.err;
+        a.unit_ctr = p.err + kWgradUnitCounter;
+        cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
         const bool bf16 = p.dtype == VG_BF16;
         const int bn = wg_bn(p.Cout);
         uint16_t* dys = static_cast<uint16_t*>(p.dy_sorted);
