@@ -284,7 +284,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(
         auto claim_publish = [&](uint32_t qq, uint32_t nbuf) {
             const uint32_t slot = qq % kUnitRing;
             const bool free_slot = mbar_wait(uempty0 + 8 * slot, ((qq / kUnitRing) & 1u) ^ 1u, s_abort);
-            const int64_t uu = free_slot ? (int64_t)atomicAdd(a.unit_ctr, 1u) : units;
+            // the first unit of every CTA is blockIdx.x (grid <= units); later ones are claimed
+            const int64_t uu = !free_slot ? units
+                               : qq == 0 ? (int64_t)blockIdx.x
+                                         : (int64_t)gridDim.x + (int64_t)atomicAdd(a.unit_ctr, 1u);
             const int64_t pub = uu < units ? uu : -1;
             s_unit[slot] = pub;
             s_gu[qq & 1u] = pub;

@@ -287,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
             const uint32_t slot = q % kUnitRing, uph = (q / kUnitRing) & 1u;
             if (p == 0) {  // claim the next unit once every reader is done with the slot's last one
                 const bool free_slot = mbar_wait(uempty0 + 8 * slot, uph ^ 1u, s_abort);
-                const int64_t uu = free_slot ? (int64_t)atomicAdd(a.unit_ctr, 1u) : units;
+                // the first unit of every CTA is blockIdx.x (grid <= units); later ones are claimed
+                const int64_t uu = !free_slot ? units
+                                   : q == 0 ? (int64_t)blockIdx.x
+                                            : (int64_t)gridDim.x + (int64_t)atomicAdd(a.unit_ctr, 1u);
                 s_unit[slot] = uu < units ? uu : -1;
                 mbar_arrive(ufull0 + 8 * slot);
             }
