@@ -489,13 +489,99 @@ def run_workload(args, wl, rank, world, dev, flush, full):
     ev = []
     timed(e2e_step, ke, ev)
     stream.synchronize()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev) / ke, world, dev)
+    e2e_single_ms = max_over_ranks(sum(a.elapsed_time(b_) for a, b_ in ev) / ke, world, dev)
+
+    # ---- end to end, pipelined as a training loop with input prefetch runs it: two
+    # device slots (inputs, map, workspaces, outputs); step i's uploads go to slot i % 2
+    # while step i - 1 computes, and step i's results come back while step i + 1
+    # computes.  Every step still copies all of its inputs in and all of its results
+    # out inside the timed region (K steps between one pair of events; the inputs are
+    # larger than L2, so no flush between steps).
+    pbs = [pb, Problem(wl, rank, dev, stream)]
+    pbs[1].m.build(pbs[1].coords, stream)
+    red2 = [reducer, shard.GradientSum(world, pbs[1].dW, pbs[1].db, dev) if world > 1 else None]
+    stream.synchronize()
+
+    def e2e_pipelined(k):
+        done_compute, done_down = [None] * k, [None] * k
+        for i in range(k):
+            q = pbs[i % 2]
+            mq = q.m
+            ev_c, ev_dy, ev_f, ev_fwd, ev_dx, ev_end = (torch.cuda.Event() for _ in range(6))
+            if i >= 2:  # the slot's previous step has read its inputs
+                up.wait_event(done_compute[i - 2])
+            with torch.cuda.stream(up):
+                q.coords.copy_(h_coords, non_blocking=True)
+                ev_c.record(up)
+                q.W.copy_(h_W, non_blocking=True)
+                q.b.copy_(h_b, non_blocking=True)
+                q.dY.copy_(h_dY, non_blocking=True)
+                ev_dy.record(up)
+                q.f.copy_(h_f, non_blocking=True)
+                ev_f.record(up)
+            stream.wait_event(ev_c)
+            if i >= 2:  # and its results have been copied out
+                stream.wait_event(done_down[i - 2])
+            mq.build(q.coords, stream)
+            dxs = stream if one_stream else q.s_dx
+            dws = stream if one_stream else q.s_dw
+            dx_ws, dw_ws = (q.ws[0], q.ws[0]) if one_stream else (q.ws[1], q.ws[2])
+            if not one_stream:
+                q.s_dx.wait_stream(stream)
+                q.s_dw.wait_stream(stream)
+            dxs.wait_event(ev_dy)
+            ops.vg_subm_conv3d_bwd(mq.ws, mq.nbr, mq.mask, q.dY, q.f, q.W, q.dX, None, None, dx_ws, stream=dxs)
+            ev_dx.record(dxs)
+            stream.wait_event(ev_f)
+            ops.vg_subm_conv3d_fwd(mq.ws, mq.nbr, mq.mask, q.f, q.W, q.b, q.out, q.ws[0], stream=stream)
+            ev_fwd.record(stream)
+            dws.wait_event(ev_fwd)
+            ops.vg_subm_conv3d_bwd(mq.ws, mq.nbr, mq.mask, q.dY, q.f, q.W, None, q.dW, q.db, dw_ws, stream=dws)
+            if not one_stream:
+                stream.wait_stream(q.s_dx)
+                stream.wait_stream(q.s_dw)
+            if red2[i % 2] is not None:
+                red2[i % 2](stream)
+            ev_end.record(stream)
+            done_compute[i] = ev_end
+            with torch.cuda.stream(down):
+                down.wait_event(ev_dx)
+                h_dX.copy_(q.dX, non_blocking=True)
+                down.wait_event(ev_fwd)
+                h_out.copy_(q.out, non_blocking=True)
+                down.wait_event(ev_end)
+                h_dW.copy_(q.dW, non_blocking=True)
+                h_db.copy_(q.db, non_blocking=True)
+                done_down[i] = torch.cuda.Event()
+                done_down[i].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+
+    e2e_pipelined(2)
+    stream.synchronize()
+    kp = max(4, min(args.steps, 100))
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    e0p, e1p = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0p.record(stream)
+    up.wait_stream(stream)
+    e2e_pipelined(kp)
+    e1p.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(e0p.elapsed_time(e1p) / kp, world, dev)
+    del pbs, red2
 
     nb_launch = nplan["launches"] + cplan["launches_fwd"] + cplan["launches_bwd"]
     rec.update({
         "roofline": roof, "clocks": clocks, "wall_s_timed_region": t_wall,
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "voxels/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "steps": kp, "schedule": "pipelined: step i's uploads while step i-1 computes, its downloads "
+                                         "while step i+1 computes (two device slots; K steps between one "
+                                         "pair of events)",
+                "single_step": {"value": world * N / (e2e_single_ms * 1e-3), "ms_per_step": e2e_single_ms,
+                                "schedule": "one step at a time: uploads, passes and downloads overlapped "
+                                            "within the step only (CUDA-graph replay, L2 flushed between steps)"}},
         "gpu_launches": steps * (nb_launch + (reducer.launches if reducer else 0)),
         "gpu_launches_per_step": {"nbrmap": nplan["launches"], "fwd": cplan["launches_fwd"],
                                   "bwd": cplan["launches_bwd"],
