@@ -222,6 +222,7 @@ template <int BN, bool BF16, bool TWO>
 __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
     // B by TMA from the sorted dY copy when the tile is wide (R = 64 rows, box 64 x 64)
     constexpr bool kTmaB = BN >= 128;
+    constexpr bool kDeep = !TWO;  // row metadata two stages ahead
     using C = WCfg<BN, TWO>;
     constexpr int S = C::S;
     constexpr int MU = C::MU;
@@ -313,32 +314,51 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
             cur.base = t_first;
             cur.end = min(a.num_tiles, t_first + a.tiles_per_chunk);
             cur.bits = window_bits(a, cur.base, cur.end, t_first, umask, lane);
-            int64_t t = next_tile(a, cur, t_first, umask, lane);  // the first tile is always active
-            int h = 0;
-            Meta<MU, RQ> mc, mn;
-            bool null_stage = false;
-            if (t >= 0) {
-                load_meta<MU, RQ, !kTmaB>(a, mu, t * 128, p, mc);
-            } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
-                null_stage = true;
-                for (int q = 0; q < RQ; ++q) {
-                    mc.i[q] = kNone;
-                    for (int v = 0; v < MU; ++v) mc.j0[v][q] = mc.j1[v][q] = kNone;
-                }
-            }
-            bool first = true;
-            while (t >= 0 || null_stage) {
-                // next stage of this unit: the next R rows of the tile, or the next active tile
-                int64_t tn = t;
-                int hn = h + 1;
-                if (null_stage) {
-                    tn = -1;
-                    null_stage = false;
-                } else if (hn == 128 / R) {
+            // Row metadata is loaded two stages ahead of the copies that use it (one stage
+            // ahead, the loads' latency set the pace of the whole pipeline: the MMA thread
+            // waited for full stages 46 % of its time at C = 1024; two ahead: C = 1024
+            // 11.92 -> 10.95 ms, C = 256 1.30 -> 1.18 ms).  Two CTAs per SM have no
+            // registers for a third stage's metadata and load one stage ahead.
+            // (t0, h0): this stage's tile and R-row part; (t1, h1): the next stage's.
+            auto advance = [&](int64_t t, int h, int64_t& tn, int& hn) {
+                tn = t;
+                hn = h + 1;
+                if (hn == 128 / R) {
                     tn = next_tile(a, cur, t_first, umask, lane);
                     hn = 0;
                 }
-                if (tn >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, tn * 128 + hn * R, p, mn);
+            };
+            int64_t t0 = next_tile(a, cur, t_first, umask, lane);  // the first tile is always active
+            int h0 = 0;
+            Meta<MU, RQ> m0, m1, m2;
+            bool null_stage = false;
+            int64_t t1 = -1;
+            int h1 = 0;
+            if (t0 >= 0) {
+                load_meta<MU, RQ, !kTmaB>(a, mu, t0 * 128, p, m0);
+                advance(t0, h0, t1, h1);
+                if (kDeep && t1 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t1 * 128 + h1 * R, p, m1);
+            } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
+                null_stage = true;
+                for (int q = 0; q < RQ; ++q) {
+                    m0.i[q] = kNone;
+                    for (int v = 0; v < MU; ++v) m0.j0[v][q] = m0.j1[v][q] = kNone;
+                }
+            }
+            bool first = true;
+            while (t0 >= 0 || null_stage) {
+                null_stage = false;
+                int64_t t2 = -1;
+                int h2 = 0;
+                if (t1 >= 0) advance(t1, h1, t2, h2);
+                if constexpr (kDeep) {
+                    if (t2 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t2 * 128 + h2 * R, p, m2);
+                } else {
+                    if (t1 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t1 * 128 + h1 * R, p, m1);
+                }
+                const int64_t t = t0, tn = t1;
+                const int h = h0;
+                const Meta<MU, RQ>& mc = m0;
                 const uint32_t stage = it % S, ph = (it / S) & 1u;
                 // warp-uniform decision: the tile cursor uses warp-wide ballots
                 if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort))) {
@@ -395,9 +415,12 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
                 cp_async_arrive_noinc(full0 + 8 * stage);  // fires when this thread's copies land
                 ++it;
                 first = false;
-                t = tn;
-                h = hn;
-                mc = mn;
+                t0 = t1;
+                h0 = h1;
+                m0 = m1;
+                t1 = t2;
+                h1 = h2;
+                if constexpr (kDeep) m1 = m2;
             }
         }
         cp_async_wait_all();
