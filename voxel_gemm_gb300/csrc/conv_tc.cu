@@ -560,7 +560,9 @@ int launch_tc(const TcArgs& a, cudaStream_t s) {
     const int grid = (int)std::min<int64_t>(units, (int64_t)ctas_per_sm<BN>() * plan_sms(0));
     TcArgs b = a;
     b.unit_ctr = a.err + kGatherUnitCounter;
-    cudaMemsetAsync(b.unit_ctr, 0, sizeof(uint32_t), s);
+    // with no more units than CTAs every claim returns >= gridDim.x >= units (the end),
+    // whatever the counter holds: no reset needed
+    if (units > grid) cudaMemsetAsync(b.unit_ctr, 0, sizeof(uint32_t), s);
     kern<<<grid, kThreads, C::kSmem, s>>>(b);
     return VG_OK;
 }

@@ -576,6 +576,9 @@ int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream
     const int MG = (num_munits(a.Cin, a.taps) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, (int64_t)(TWO ? 2 : 1) * sms);
+    // with no more units than CTAs every claim returns >= gridDim.x >= units (the end),
+    // whatever the counter holds: no reset needed
+    if (units > grid) cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
     kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
     return VG_OK;
 }
@@ -644,7 +647,6 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.partial = p.partial;
         a.err = p.err;
         a.unit_ctr = p.err + kWgradUnitCounter;
-        cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
         const bool bf16 = p.dtype == VG_BF16;
         const int bn = wg_bn(p.Cout);
         uint16_t* dys = static_cast<uint16_t*>(p.dy_sorted);
