@@ -235,7 +235,18 @@ k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows, flo
         const int rl = tid / (256 / lanes), g = g0 + tid % (256 / lanes);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (g < cg8) {
-            for (int64_t r = r0 + rl; r < r1; r += lanes) {
+            // four rows per iteration, their loads issued together (the sums stay in row order)
+            int64_t r = r0 + rl;
+            for (; r + 3 * lanes < r1; r += 4 * lanes) {
+                float v[4][8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) load8(dy + (r + j * lanes) * Cout + g * 8, v[j]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] += v[j][q];
+            }
+            for (; r < r1; r += lanes) {
                 float v[8];
                 load8(dy + r * Cout + g * 8, v);
 #pragma unroll
@@ -254,6 +265,72 @@ k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows, flo
             partial_db[(int64_t)blockIdx.x * Cout + gg * 8 + (c & 7)] = sum;
         }
         __syncthreads();
+    }
+}
+
+// The same partial sums read through the processing order, fused with the copy of
+// dy into that order that the tensor-core weight gradient loads by TMA:
+// dst[r] = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad; block b sums
+// the sorted rows [b*rows, (b+1)*rows) into partial_db[b][:] (fixed order as above).
+// One read of dy serves both (16-bit types).
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_dbias_sorted(const T* __restrict__ dy, const uint32_t* __restrict__ sorted_idx, int64_t n, int64_t rows_pad,
+               int Cout, int64_t rows, float* __restrict__ partial_db, T* __restrict__ dst,
+               const uint32_t* __restrict__ nbr_status) {
+    static_assert(sizeof(T) == 2, "16-bit rows");
+    __shared__ float red[256 * 8];
+    if (*nbr_status) return;
+    const int cg8 = Cout / 8;
+    const int lanes = cg8 >= 256 ? 1 : 256 / cg8;
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * rows, r1 = min(n, r0 + rows);
+    for (int g0 = 0; g0 < cg8; g0 += 256 / lanes) {
+        const int rl = tid / (256 / lanes), g = g0 + tid % (256 / lanes);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (g < cg8) {
+            // four rows per iteration, their loads issued together (the sums stay in row order)
+            int64_t r = r0 + rl;
+            for (; r + 3 * lanes < r1; r += 4 * lanes) {
+                uint32_t src[4];
+                uint4 u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) src[j] = sorted_idx[r + j * lanes];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[j] = *reinterpret_cast<const uint4*>(dy + (int64_t)src[j] * Cout + g * 8);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    *reinterpret_cast<uint4*>(dst + (r + j * lanes) * Cout + g * 8) = u[j];
+                    const T* e = reinterpret_cast<const T*>(&u[j]);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[q] += to_f32(e[q]);
+                }
+            }
+            for (; r < r1; r += lanes) {
+                const uint4 u = *reinterpret_cast<const uint4*>(dy + (int64_t)sorted_idx[r] * Cout + g * 8);
+                *reinterpret_cast<uint4*>(dst + r * Cout + g * 8) = u;
+                const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += to_f32(e[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) red[tid * 8 + q] = acc[q];
+        __syncthreads();
+        const int width = 256 / lanes;
+        for (int c = tid; c < width * 8; c += 256) {
+            const int gg = g0 + c / 8;
+            if (gg >= cg8) continue;
+            float sum = 0.f;
+            for (int l = 0; l < lanes; ++l) sum += red[(l * width + c / 8) * 8 + (c & 7)];
+            partial_db[(int64_t)blockIdx.x * Cout + gg * 8 + (c & 7)] = sum;
+        }
+        __syncthreads();
+    }
+    if (blockIdx.x == gridDim.x - 1) {  // the padding rows of the sorted copy
+        const int64_t chunks = (rows_pad - n) * cg8;
+        for (int64_t e = tid; e < chunks; e += 256)
+            reinterpret_cast<uint4*>(dst + n * Cout)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -367,6 +444,25 @@ static void dbias_t(const void* dy, int64_t n, int Cout, int sms, void* db, floa
     k_dbias_partial<T><<<R, 256, 0, s>>>(static_cast<const T*>(dy), n, Cout, dbias_rows(n, sms), partial_db,
                                          nbr_status);
     k_reduce_db<T><<<(unsigned)((Cout + 31) / 32), 256, 0, s>>>(partial_db, R, Cout, static_cast<T*>(db), nbr_status);
+}
+
+void launch_dbias_sorted(const void* dy, const uint32_t* sorted_idx, int64_t n, int64_t rows_pad, int Cout,
+                         int sms, void* db, float* partial_db, void* dy_sorted, int dtype,
+                         const uint32_t* nbr_status, cudaStream_t s) {
+    const int R = dbias_blocks(n, sms);
+    const int64_t rows = dbias_rows(n, sms);
+    const unsigned cb = (unsigned)((Cout + 31) / 32);
+    if (dtype == VG_F16) {
+        k_dbias_sorted<__half><<<R, 256, 0, s>>>(static_cast<const __half*>(dy), sorted_idx, n, rows_pad, Cout, rows,
+                                                 partial_db, static_cast<__half*>(dy_sorted), nbr_status);
+        k_reduce_db<__half><<<cb, 256, 0, s>>>(partial_db, R, Cout, static_cast<__half*>(db), nbr_status);
+    } else {
+        k_dbias_sorted<__nv_bfloat16><<<R, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dy), sorted_idx, n,
+                                                        rows_pad, Cout, rows, partial_db,
+                                                        static_cast<__nv_bfloat16*>(dy_sorted), nbr_status);
+        k_reduce_db<__nv_bfloat16><<<cb, 256, 0, s>>>(partial_db, R, Cout, static_cast<__nv_bfloat16*>(db),
+                                                      nbr_status);
+    }
 }
 
 void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,

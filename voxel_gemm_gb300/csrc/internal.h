@@ -108,6 +108,11 @@ void launch_reduce_splits(const float* partial, int splits, int64_t total, int64
 // db = column sums of dy over dbias_blocks(n, sms) row blocks, reduced in a fixed order
 // (partial_db holds dbias_blocks(n, sms) x Cout floats).
 int dbias_blocks(int64_t n, int sms);
+// The same db, read through the processing order while copying dy into it:
+// dy_sorted[r] = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad (16-bit dtypes).
+void launch_dbias_sorted(const void* dy, const uint32_t* sorted_idx, int64_t n, int64_t rows_pad, int Cout,
+                         int sms, void* db, float* partial_db, void* dy_sorted, int dtype,
+                         const uint32_t* nbr_status, cudaStream_t s);
 void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s);
 

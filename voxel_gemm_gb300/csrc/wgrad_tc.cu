@@ -628,6 +628,7 @@ size_t tc_wgrad_sorted_dy_bytes(int64_t n, int Cout) {
 
 int tc_wgrad(const WgradPass& p, cudaStream_t s) {
     if (p.n == 0) return VG_OK;
+    bool db_done = false;
     if (p.dW) {
         WgArgs a;
         a.sorted_idx = p.sorted_idx;
@@ -653,9 +654,15 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         if (bn >= 128) {
             if (!dys) return VG_ERR_INVALID_ARG;
             const int64_t rows_pad = a.num_tiles * kTileRows;
-            const int64_t chunks = rows_pad * (p.Cout / 8);
-            const unsigned blocks = (unsigned)std::min<int64_t>((chunks + 255) / 256, 16 * (int64_t)p.sms);
-            k_sort_rows<<<blocks, 256, 0, s>>>(a.dy, p.sorted_idx, p.n, rows_pad, p.Cout, p.nbr_status, dys);
+            if (p.db) {  // one read of dY: the copy into processing order and db's partial sums
+                launch_dbias_sorted(p.dy, p.sorted_idx, p.n, rows_pad, p.Cout, p.sms, p.db, p.partial_db, dys,
+                                    p.dtype, p.nbr_status, s);
+                db_done = true;
+            } else {
+                const int64_t chunks = rows_pad * (p.Cout / 8);
+                const unsigned blocks = (unsigned)std::min<int64_t>((chunks + 255) / 256, 16 * (int64_t)p.sms);
+                k_sort_rows<<<blocks, 256, 0, s>>>(a.dy, p.sorted_idx, p.n, rows_pad, p.Cout, p.nbr_status, dys);
+            }
         }
         int st;
         switch (bn) {
@@ -680,11 +687,12 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         launch_reduce_splits(p.partial, p.splits, (int64_t)p.taps * p.Cin * p.Cout, (int64_t)kTaps * p.Cin * p.Cout,
                              p.dW, p.dtype, p.nbr_status, s);
     }
-    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    if (p.db && !db_done) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;
 }
 
-// dgrad (pack, gemm), wgrad (sorted dY copy when Cout >= 128, gemm, reduce), dbias (partial, reduce)
-int tc_bwd_launches(int Cout) { return 2 + (wg_bn(Cout) >= 128 ? 3 : 2) + 2; }
+// dgrad (pack, gemm); Cout >= 128: dY into processing order with db's partial sums, wgrad gemm,
+// split reduce, db reduce; Cout = 64: wgrad gemm, split reduce, db partials, db reduce
+int tc_bwd_launches(int Cout) { return 2 + (wg_bn(Cout) >= 128 ? 3 + 1 : 2 + 2); }
 
 }  // namespace vg
