@@ -648,6 +648,68 @@ def run_inference(args, wl, dev, flush):
     return rec
 
 
+def run_tf32(args, base, dev, flush):
+    """fp32 features on a workload's voxels (Cin = Cout = 256): the three passes with
+    VG_ALLOW_TF32 (tensor cores, TF32 inputs, fp32 accumulation) and without it (the
+    exact fp32 FFMA path), CUDA-event time of each pass call."""
+    import torch
+    from voxel_gemm_gb300 import ops, synth
+    stream = torch.cuda.Stream(device=dev)
+    wl = synth.Workload(base.name + "_f32", base.B, base.res, base.shapes_per_sample, base.kinds, 256, 256, "f32",
+                        base.seed, 2.0)
+    coords_np = synth.make_coords(base)
+    N = coords_np.shape[0]
+    with torch.cuda.stream(stream):
+        coords = torch.from_numpy(coords_np).to(dev)
+        f, W, b, dY = synth.make_tensors(wl, N, device=dev)
+        m = ops.NbrMap.alloc(N, base.grid, base.key_flag, device=dev)
+        out = torch.empty(N, wl.cout, dtype=torch.float32, device=dev)
+        dX = torch.empty(N, wl.cin, dtype=torch.float32, device=dev)
+        dW = torch.empty_like(W)
+        db = torch.empty_like(b)
+    m.build(coords, stream)
+    assert m.status(stream) == ops.VG_OK
+    P = count_pairs(m.mask.cpu().numpy().view("uint32"))
+    peaks = load_peaks()
+    tf32_peak = peaks["bf16_tflops"] / 2  # dense TF32 rate: half the 16-bit rate (nominal ratio)
+    rec = {"workload": wl.name, "N": N, "P": P, "cin": wl.cin, "cout": wl.cout,
+           "tf32_peak_tflops": tf32_peak, "tf32_peak_source": peaks["source"] + " bf16 burst / 2"}
+    for tag, flags in (("tf32", ops.VG_ALLOW_TF32), ("ffma", 0)):
+        with torch.cuda.stream(stream):
+            ws = ops.conv_workspace(N, wl.cin, wl.cout, torch.float32, device=dev, flags=flags)
+        calls = {
+            "fwd": lambda: ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, flags=flags, stream=stream),
+            "dgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, None, None, ws, flags=flags,
+                                                    stream=stream),
+            "wgrad": lambda: ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, None, dW, db, ws, flags=flags,
+                                                    stream=stream),
+        }
+        r = {}
+        for name, call in calls.items():
+            for _ in range(2):
+                call()
+            ts = []
+            for _ in range(max(3, min(args.steps, 10))):
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    call()
+                    e1.record(stream)
+                ts.append((e0, e1))
+            stream.synchronize()
+            ms = sum(a.elapsed_time(b_) for a, b_ in ts) / len(ts)
+            fl = 2.0 * P * wl.cin * wl.cout
+            r[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+            if tag == "tf32":
+                r[name]["frac_of_tf32_peak"] = r[name]["tflops"] / tf32_peak
+        assert ops.vg_conv_status(ws, stream) == ops.VG_OK
+        rec[tag] = r
+        del ws
+    rec["speedup_tf32"] = sum(v["ms"] for v in rec["ffma"].values()) / sum(v["ms"] for v in rec["tf32"].values())
+    return rec
+
+
 def run_row_orders(args, wl, dev, flush):
     """The two row orders of the neighbour map on one workload: Morton (the default)
     and Hilbert (VG_ORDER_HILBERT).  Per order: the useful fraction of the MMA rows
@@ -807,10 +869,16 @@ def run_ours(args, rank, world, local_rank):
         except Exception as e:  # noqa: BLE001
             regular = {"workload": REGULAR_WORKLOAD, "error": f"{type(e).__name__}: {e}"}
         torch.cuda.empty_cache()
+        try:
+            tf32 = run_tf32(args, synth.WORKLOADS[REGULAR_WORKLOAD], dev, flush)
+        except Exception as e:  # noqa: BLE001
+            tf32 = {"workload": REGULAR_WORKLOAD, "error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
     else:
         infer = None
         orders = None
         regular = None
+        tf32 = None
 
     res = {
         "metric": METRIC, "value": head["value"], "unit": "voxels/s", "n_gpus": world,
@@ -828,6 +896,7 @@ def run_ours(args, rank, world, local_rank):
         "inference_small_n": infer,
         "row_order_morton_vs_hilbert": orders,
         "regular_conv": regular,
+        "tf32": tf32,
     }
     return res
 
