@@ -150,57 +150,83 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             const int64_t end = min(a.num_tiles, first + a.tiles_per_chunk);
             int64_t pos = next_active(first, first, end, k);
             bool first_stage = true;
-            while (pos >= 0 && ok) {
-                const int64_t t = a.tile_order[pos];
-                const int64_t npos = next_active(pos + 1, first, end, k);
-                for (int h = 0; h < 128 / kRows && ok; ++h) {
-                    const uint32_t stage = it % S, ph = (it / S) & 1u;
-                    if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
-                        ok = false;
-                        *s_abort = 1;
-                        break;
-                    }
-                    uint8_t* img_a = stages + (size_t)stage * C::kStageBytes;
-                    uint8_t* img_b = img_a + C::kABytes;
-                    const int64_t r0 = t * 128 + h * kRows + 4 * rq;  // < num_tiles * 128 always
-                    // A: 128 input channels as 8 blocks of 16 (4 lanes x 4 channels), two per warp
+            // Software pipeline: the row indices of a stage are loaded one stage ahead, and
+            // a stage's data loads are all issued before its slot is waited for and before
+            // any store (loads of independent rows in flight together; with the loads and
+            // stores interleaved per 4x4 block the producers paced the pass, 0.03 of the
+            // TF32 peak at C = 256).
+            int64_t t = pos >= 0 ? a.tile_order[pos] : 0;
+            int64_t npos = pos >= 0 ? next_active(pos + 1, first, end, k) : -1;
+            int h = 0;
+            uint32_t jn[4], in[4];  // this stage's neighbour rows (tap k) and dY rows
+            auto load_idx = [&](int64_t tt, int hh, uint32_t (&jj)[4], uint32_t (&ii)[4]) {
+                const int64_t rr = tt * 128 + hh * kRows + 4 * rq;  // < num_tiles * 128 always
 #pragma unroll
-                    for (int P = warp; P < kBM / 16; P += 4) {
-                        const int cl = P * 16 + cg * 4;  // channel offset in the unit
-                        const int c = ci0 + cl;
-                        float4 v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t j = a.sorted_nbr[(r0 + e) * kTaps + k];
-                            v[e] = (j != kNone && c < a.Cin)
-                                       ? __ldg(reinterpret_cast<const float4*>(a.f + (int64_t)j * a.Cin + c))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                        store_t4(img_a, cl, rq, v);
-                    }
-                    // B: BN output channels as BN/16 blocks of 16 over the four warps
-#pragma unroll
-                    for (int P = warp; P < BN / 16; P += 4) {
-                        const int cl = P * 16 + cg * 4;
-                        float4 v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int64_t r = r0 + e;
-                            const uint32_t i = r < a.n ? a.sorted_idx[r] : kNone;
-                            v[e] = i != kNone
-                                       ? __ldg(reinterpret_cast<const float4*>(a.dy + (int64_t)i * a.Cout + co0 + cl))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                        store_t4(img_b, cl, rq, v);
-                    }
-                    if (p == 0)
-                        s_info[stage] = (first_stage ? 1u : 0u) | ((npos < 0 && h == 128 / kRows - 1) ? 2u : 0u);
-                    fence_proxy_async_smem();  // generic-proxy stores -> the MMA's async-proxy reads
-                    mbar_arrive(full0 + 8 * stage);
-                    ++it;
-                    first_stage = false;
+                for (int e = 0; e < 4; ++e) {
+                    jj[e] = a.sorted_nbr[(rr + e) * kTaps + k];
+                    ii[e] = rr + e < a.n ? a.sorted_idx[rr + e] : kNone;
                 }
-                pos = npos;
+            };
+            if (pos >= 0) load_idx(t, 0, jn, in);
+            while (pos >= 0 && ok) {
+                // data of this stage
+                constexpr int NBP = (BN / 16 + 3) / 4;  // B blocks of 16 channels per warp (at most)
+                float4 va[kBM / 64][4], vb[NBP][4];
+#pragma unroll
+                for (int P = 0; P < kBM / 64; ++P) {
+                    const int c = ci0 + (warp + 4 * P) * 16 + cg * 4;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        va[P][e] = (jn[e] != kNone && c < a.Cin)
+                                       ? __ldg(reinterpret_cast<const float4*>(a.f + (int64_t)jn[e] * a.Cin + c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int P = 0; P < NBP; ++P) {
+                    const int cl = (warp + 4 * P) * 16 + cg * 4;
+                    const bool blk = warp + 4 * P < BN / 16;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        vb[P][e] = blk && in[e] != kNone
+                                       ? __ldg(reinterpret_cast<const float4*>(a.dy + (int64_t)in[e] * a.Cout + co0 + cl))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                // the next stage's position and row indices
+                const bool last = npos < 0 && h == 128 / kRows - 1;
+                int64_t t_next = t, pos_next = pos, npos_next = npos;
+                int h_next = h + 1;
+                if (h_next == 128 / kRows) {
+                    h_next = 0;
+                    pos_next = npos;
+                    if (pos_next >= 0) {
+                        t_next = a.tile_order[pos_next];
+                        npos_next = next_active(pos_next + 1, first, end, k);
+                    }
+                }
+                if (!last) load_idx(t_next, h_next, jn, in);
+                const uint32_t stage = it % S, ph = (it / S) & 1u;
+                if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
+                    ok = false;
+                    *s_abort = 1;
+                    break;
+                }
+                uint8_t* img_a = stages + (size_t)stage * C::kStageBytes;
+                uint8_t* img_b = img_a + C::kABytes;
+#pragma unroll
+                for (int P = 0; P < kBM / 64; ++P) store_t4(img_a, (warp + 4 * P) * 16 + cg * 4, rq, va[P]);
+#pragma unroll
+                for (int P = 0; P < NBP; ++P)
+                    if (warp + 4 * P < BN / 16) store_t4(img_b, (warp + 4 * P) * 16 + cg * 4, rq, vb[P]);
+                if (p == 0) s_info[stage] = (first_stage ? 1u : 0u) | (last ? 2u : 0u);
+                fence_proxy_async_smem();  // generic-proxy stores -> the MMA's async-proxy reads
+                mbar_arrive(full0 + 8 * stage);
+                ++it;
+                first_stage = false;
+                if (last) break;
+                t = t_next;
+                h = h_next;
+                pos = pos_next;
+                npos = npos_next;
             }
         }
         if (!ok) atomicOr(a.err, kErrTimeout);
