@@ -16,8 +16,8 @@
 // hit distinct bank groups.
 //   A: M = 128 input channels of one tap (masked past Cin), K = 32 rows
 //   B: N = BN output channels,                                K = 32 rows
-// Warps 0-3 produce, warp 4 allocates TMEM and issues the MMAs (4 per stage,
-// K = 8 each), warps 5-8 write the fp32 partials.  Every wait is bounded.
+// Warps 0-7 produce, warp 8 allocates TMEM and issues the MMAs (4 per stage,
+// K = 8 each), warps 9-12 write the fp32 partials.  Every wait is bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -28,7 +28,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;
+constexpr int kProducerWarps = 8;  // (4 left one load latency per stage exposed: 2x slower)
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kRows = 32;  // voxel rows per stage (one 128-byte K block of fp32)
 constexpr int kBM = 128;   // input channels per unit
 
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     const uint32_t done_bar = smem_u32(bars + 2 * S + 2 * NBUF);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(full0 + 8 * i, 128);  // every producer thread
+            mbar_init(full0 + 8 * i, kProducerWarps * 32);  // every producer thread
             mbar_init(empty0 + 8 * i, 1);   // one tcgen05.commit
         }
         for (int i = 0; i < NBUF; ++i) {
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         *s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
         tmem_relinquish();
     }
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         return -1;
     };
 
-    if (warp < 4) {
+    if (warp < kProducerWarps) {
         // ------------------------------------------------------------ producers (transposing gather)
         const int p = threadIdx.x;
         const int rq = lane >> 2, cg = lane & 3;  // row quad (rows 4rq..4rq+3), channel group
@@ -170,11 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             if (pos >= 0) load_idx(t, 0, jn, in);
             while (pos >= 0 && ok) {
                 // data of this stage
-                constexpr int NBP = (BN / 16 + 3) / 4;  // B blocks of 16 channels per warp (at most)
-                float4 va[kBM / 64][4], vb[NBP][4];
+                constexpr int PW = kProducerWarps;
+                constexpr int NAP = (kBM / 16 + PW - 1) / PW;  // A blocks of 16 channels per warp
+                constexpr int NBP = (BN / 16 + PW - 1) / PW;   // B blocks per warp (at most)
+                float4 va[NAP][4], vb[NBP][4];
 #pragma unroll
-                for (int P = 0; P < kBM / 64; ++P) {
-                    const int c = ci0 + (warp + 4 * P) * 16 + cg * 4;
+                for (int P = 0; P < NAP; ++P) {
+                    const int c = ci0 + (warp + PW * P) * 16 + cg * 4;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         va[P][e] = (jn[e] != kNone && c < a.Cin)
@@ -183,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 }
 #pragma unroll
                 for (int P = 0; P < NBP; ++P) {
-                    const int cl = (warp + 4 * P) * 16 + cg * 4;
-                    const bool blk = warp + 4 * P < BN / 16;
+                    const int cl = (warp + PW * P) * 16 + cg * 4;
+                    const bool blk = warp + PW * P < BN / 16;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         vb[P][e] = blk && in[e] != kNone
@@ -213,12 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 uint8_t* img_a = stages + (size_t)stage * C::kStageBytes;
                 uint8_t* img_b = img_a + C::kABytes;
 #pragma unroll
-                for (int P = 0; P < kBM / 64; ++P) store_t4(img_a, (warp + 4 * P) * 16 + cg * 4, rq, va[P]);
+                for (int P = 0; P < NAP; ++P) store_t4(img_a, (warp + PW * P) * 16 + cg * 4, rq, va[P]);
 #pragma unroll
                 for (int P = 0; P < NBP; ++P)
-                    if (warp + 4 * P < BN / 16) store_t4(img_b, (warp + 4 * P) * 16 + cg * 4, rq, vb[P]);
+                    if (warp + PW * P < BN / 16) store_t4(img_b, (warp + PW * P) * 16 + cg * 4, rq, vb[P]);
                 if (p == 0) s_info[stage] = (first_stage ? 1u : 0u) | (last ? 2u : 0u);
-                fence_proxy_async_smem();  // generic-proxy stores -> the MMA's async-proxy reads
+                // (the MMA thread orders these generic-proxy stores before its async-proxy
+                // reads with one proxy fence after the stage barrier, as for cp.async data)
                 mbar_arrive(full0 + 8 * stage);
                 ++it;
                 first_stage = false;
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             }
         }
         if (!ok) atomicOr(a.err, kErrTimeout);
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_tf32(BN);
@@ -308,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 int tf32_bn(int cout) {
