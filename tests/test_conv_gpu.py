@@ -119,6 +119,48 @@ def test_wide_blocks_one_unit_per_tile(dtype, cin, cout, n):
     full_check(coords, (1, 18, 18, 18), f, W, None, dY, TOL[dtype], flags=ops.VG_NO_SMALL_N_SPLIT)
 
 
+@pytest.mark.parametrize("dtype,cout", [("bf16", 256), ("f16", 512), ("f32", 256)])
+def test_tile_pairs_rows_and_ragged_tail(dtype, cout):
+    """256-column output blocks with at least as many tile pairs as SMs run on the
+    kernel that feeds each weight tile to two consecutive tiles (each skipping its own
+    absent taps).  Surface voxels (tiles with different tap masks) and an odd tile
+    count whose last tile is partial: every column of 4096 sampled rows and of every
+    row of the last three tiles in processing order, for out and dX, and sampled
+    full-sum dW entries, against the oracle (fp32 runs as TF32)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = (2 * sms + 1) * 128 - 77
+    wl = synth.Workload("t", 4, 112, 4, ("sphere", "torus"), 256, cout, dtype, 41, 2.0)
+    coords_all = synth.make_coords(wl)
+    assert coords_all.shape[0] >= n
+    coords = coords_all[np.random.default_rng(41).permutation(coords_all.shape[0])[:n]]
+    flags = ops.VG_ALLOW_TF32 if dtype == "f32" else 0
+    f, W, b, dY = synth.make_tensors(wl, n)
+    c = torch.from_numpy(coords).cuda()
+    m = ops.NbrMap.alloc(n, wl.grid).build(c)
+    fd, Wd, bd, dYd = (t.cuda() for t in (f, W, b, dY))
+    ws = ops.conv_workspace(n, 256, cout, f.dtype, flags=flags)
+    out = torch.empty(n, cout, dtype=f.dtype, device="cuda")
+    dX = torch.empty(n, 256, dtype=f.dtype, device="cuda")
+    dW = torch.empty_like(Wd)
+    db = torch.empty_like(bd)
+    ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, fd, Wd, bd, out, ws, flags=flags)
+    ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dYd, fd, Wd, dX, dW, db, ws, flags=flags)
+    assert m.status() == ops.VG_OK and ops.vg_conv_status(ws) == ops.VG_OK
+    nbr_ref, _ = oracle.nbrmap(coords, *wl.grid)
+    assert np.array_equal(u32(m.nbr), nbr_ref)
+    order = m.sorted_idx().cpu().numpy().astype(np.int64)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([rng.choice(n, size=4096, replace=False), order[(n // 128 - 2) * 128:]]))
+    tol = 5e-3 if dtype == "f32" else TOL[dtype]
+    e_out = rel_fro(f64(out.cpu()[rows]), oracle_fwd_rows(nbr_ref, rows, np.arange(cout), f, W, b))
+    e_dx = rel_fro(f64(dX.cpu()[rows]), oracle_dgrad_rows(nbr_ref, rows, np.arange(256), dY, W))
+    ci = np.sort(rng.choice(256, size=16, replace=False))
+    co = np.sort(rng.choice(cout, size=16, replace=False))
+    dW_ref, _ = oracle_wgrad_cols(nbr_ref, f, dY, ci, co)
+    e_dw = rel_fro(f64(dW.cpu()[:, ci][:, :, co]), dW_ref)
+    assert max(e_out, e_dx, e_dw) <= tol, (e_out, e_dx, e_dw)
+
+
 @pytest.mark.parametrize("n", [3000, 60000])
 def test_workspace_contents_do_not_matter(n):
     """The GEMM kernels hand out work units through counters in the conv workspace

@@ -504,6 +504,351 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(
     if (warp == 4) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Tile pairs (256 output columns): one unit = two consecutive 128-row tiles x
+// one 256-column N block.  Each stage holds both tiles' gathered rows for one
+// (tap, K block) and ONE weight tile, which feeds two M = 128 MMAs (one per
+// tile, each into its own 256-column TMEM accumulator): per stage 64 KB of
+// shared memory for 8.4 MFLOP instead of 48 KB for 4.2 MFLOP, so the weight
+// tiles -- two thirds of the single-tile kernel's L2 reads -- are read once per
+// pair.  Each tile still skips its own absent taps: a stage carries the rows of
+// only the tiles whose mask has the tap, and the MMA thread issues only their
+// MMAs, so no MMA runs on rows of a tap its tile does not use; only the weight
+// tile is shared (read for the union of the two masks).
+//   warps 0-3    gather (both tiles: 16 rows of 16 B per thread per stage)
+//   warp 4       TMEM (all 512 columns) and the MMA-issuing thread
+//   warps 5-8    epilogue of the first tile; warps 10-13 that of the second
+//                (warp w reads TMEM lane quadrant w % 4), concurrently
+//   warp 9       weight-tile loader
+// The accumulators are not double-buffered (two tiles x 256 columns fill TMEM):
+// the MMA thread starts a unit once the first tile's accumulator has been read
+// out, and its first MMA into the second tile once that one has.
+constexpr int kPairThreads = 448;  // 14 warps
+constexpr int kPairReaders = 1 + 8 + 1;  // the MMA thread, 8 epilogue warps, the weight loader
+
+struct PairCfg {
+    static constexpr int S = 3;  // stages
+    static constexpr int BN = 256;
+    static constexpr int kBBytes = BN * kKBytes;                   // 32 KB
+    static constexpr int kStageBytes = 2 * kABytes + kBBytes;      // 64 KB: tile 0 rows, tile 1 rows, weights
+    static constexpr size_t kNbrBytes = (size_t)2 * kBM * kTaps * 4;
+    // full x S, empty x S, tfull, tempty x 2, done, nbr, unit ring full and empty
+    static constexpr int kNumBars = 2 * S + 5 + 2 * kUnitRing;
+    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + kNbrBytes + 8 * kNumBars + 8 * (kUnitRing + 2) +
+                                    16 + 2 * kMaxBiasCols;
+};
+static_assert(PairCfg::kSmem <= 232448, "tile-pair kernel exceeds the shared memory of one CTA");
+
+template <int DT>
+__global__ void __launch_bounds__(kPairThreads, 1) k_gather_gemm_pair(TcArgs a) {
+    using C = PairCfg;
+    constexpr int S = C::S, BN = C::BN;
+    constexpr int ES = Elt<DT>::size;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sStage = smem;                                                     // [S][rows 0 | rows 1 | weights]
+    uint32_t* s_nbr = reinterpret_cast<uint32_t*>(smem + (size_t)S * C::kStageBytes);  // [256][27]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_nbr + 2 * kBM * kTaps);
+    volatile int64_t* s_unit = reinterpret_cast<volatile int64_t*>(bars + C::kNumBars);
+    volatile int64_t* s_gu = s_unit + kUnitRing;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::kNumBars + kUnitRing + 2);
+    volatile uint32_t* s_abort = s_tmem + 1;
+    uint8_t* s_bias = reinterpret_cast<uint8_t*>(s_tmem + 4);
+
+    if (*a.nbr_status) return;  // bad neighbour map: write nothing (uniform over the block)
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t tfull = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + 1);
+    const uint32_t done_bar = smem_u32(bars + 2 * S + 3), nbar = smem_u32(bars + 2 * S + 4);
+    const uint32_t ufull0 = smem_u32(bars + 2 * S + 5), uempty0 = ufull0 + 8 * kUnitRing;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(ufull0 + 8 * i, 1);
+            mbar_init(uempty0 + 8 * i, kPairReaders);
+        }
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full0 + 8 * i, 128 + 1);  // 128 gather threads + the weight-tile expect_tx
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty0, 4);      // the four epilogue warps of tile 0
+        mbar_init(tempty0 + 8, 4);  // ... of tile 1
+        mbar_init(done_bar, 1);
+        mbar_init(nbar, 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(smem_u32(s_tmem), 2 * BN);
+        tmem_relinquish();
+    }
+    if (DT != kTF32 && a.bias) {
+        const uint32_t* bsrc = static_cast<const uint32_t*>(a.bias);
+        for (int c = threadIdx.x; c < a.Ndim / 2; c += kPairThreads) reinterpret_cast<uint32_t*>(s_bias)[c] = bsrc[c];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    const int NB = a.Ndim / BN;
+    const int64_t a_row_bytes = (int64_t)a.Kdim * ES;
+    const int KB = (int)(a_row_bytes / kKBytes);
+    // unit u = (tile pair tp, N block nb), u = tp * NB + nb; tiles 2tp and 2tp + 1
+    const int64_t units = (a.num_tiles + 1) / 2 * NB;
+    auto tile_taps = [&](int64_t t) { return t < a.num_tiles ? a.tile_mask[t] : 0u; };
+
+    if (warp < 4) {
+        // ------------------------------------------------------------ gather producer
+        // As in the single-tile kernel, with one neighbour-list buffer (both tiles,
+        // 27 KB): thread 0 copies the next unit's lists in once every gather thread
+        // has finished the current unit.
+        const int p = threadIdx.x;
+        uint32_t it = 0;
+        bool ok = true;
+        auto claim_publish = [&](uint32_t qq) {
+            const uint32_t slot = qq % kUnitRing;
+            const bool free_slot = mbar_wait(uempty0 + 8 * slot, ((qq / kUnitRing) & 1u) ^ 1u, s_abort);
+            const int64_t uu = !free_slot ? units
+                               : qq == 0 ? (int64_t)blockIdx.x
+                                         : (int64_t)gridDim.x + (int64_t)atomicAdd(a.unit_ctr, 1u);
+            const int64_t pub = uu < units ? uu : -1;
+            s_unit[slot] = pub;
+            s_gu[qq & 1u] = pub;
+            mbar_arrive(ufull0 + 8 * slot);
+        };
+        auto copy_nbr = [&](int64_t uu) {
+            const int64_t t0 = uu / NB * 2;
+            const uint32_t bytes = (uint32_t)((t0 + 1 < a.num_tiles ? 2 : 1) * kBM * kTaps * 4);
+            mbar_arrive_expect_tx(nbar, bytes);
+            bulk_g2s(smem_u32(s_nbr), a.sorted_nbr + t0 * kBM * kTaps, bytes, nbar);
+        };
+        if (p == 0) {
+            claim_publish(0);
+            if (s_gu[0] >= 0) copy_nbr(s_gu[0]);
+        }
+        named_bar_sync(1, 128);
+        const int ch = p & 7;
+        for (uint32_t idx = 0;; ++idx) {
+            const int64_t u = s_gu[idx & 1u];
+            if (u < 0) break;  // the same value in every gather thread
+            const int64_t t0 = u / NB * 2;
+            const uint32_t m0 = tile_taps(t0), m1 = tile_taps(t0 + 1);
+            if (p == 0) claim_publish(idx + 1);
+            // always wait for this unit's copy, so none is in flight when the block exits
+            if (!mbar_wait_timed(nbar, idx & 1u)) {
+                ok = false;
+                *s_abort = 1;
+            }
+            for (int k = 0; k < kTaps && ok; ++k) {
+                const bool h0 = (m0 >> k) & 1u, h1 = (m1 >> k) & 1u;
+                if (!h0 && !h1) continue;
+                // this thread's 8 source rows of each present tile for tap k
+                const uint8_t* src[16];
+                uint32_t src_bytes[16];
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const bool present = i2 < 8 ? h0 : h1;
+                    const uint32_t j = present ? s_nbr[((i2 >> 3) * kBM + (i2 & 7) * 16 + (p >> 3)) * kTaps + k] : kNone;
+                    src[i2] = a.A + (int64_t)(j != kNone ? j : 0u) * a_row_bytes + ch * 16;
+                    src_bytes[i2] = j != kNone ? 16u : 0u;
+                }
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t stage = it % S, ph = (it / S) & 1u;
+                    if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
+                        ok = false;
+                        *s_abort = 1;
+                        break;
+                    }
+                    const uint32_t base = smem_u32(sStage + (size_t)stage * C::kStageBytes);
+                    if (h0) {
+#pragma unroll
+                        for (int i2 = 0; i2 < 8; ++i2) {
+                            const int row = i2 * 16 + (p >> 3);
+                            cp_async16(base + row * 128 + ((ch ^ (row & 7)) << 4), src[i2] + kb * kKBytes,
+                                       src_bytes[i2]);
+                        }
+                    }
+                    if (h1) {
+#pragma unroll
+                        for (int i2 = 0; i2 < 8; ++i2) {
+                            const int row = i2 * 16 + (p >> 3);
+                            cp_async16(base + kABytes + row * 128 + ((ch ^ (row & 7)) << 4),
+                                       src[8 + i2] + kb * kKBytes, src_bytes[8 + i2]);
+                        }
+                    }
+                    cp_async_arrive_noinc(full0 + 8 * stage);
+                    ++it;
+                }
+            }
+            named_bar_sync(1, 128);  // every gather thread is done with the neighbour lists
+            if (p == 0) {
+                const int64_t nu = s_gu[(idx + 1) & 1u];
+                if (nu >= 0) copy_nbr(nu);
+            }
+        }
+        cp_async_wait_all();
+        if (!ok) atomicOr(a.err, kErrTimeout);
+        if (p == 0)
+            for (uint32_t i = 0; i < S && i < it; ++i) {
+                const uint32_t last = it - 1 - i;
+                if (!mbar_wait_timed(full0 + 8 * (last % S), (last / S) & 1u)) atomicOr(a.err, kErrTimeout);
+            }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = DT == kTF32 ? idesc_tf32(BN) : idesc_f16(DT == kBF16, BN);
+            uint32_t it = 0, uc = 0;
+            bool ok = true;
+            for (uint32_t qi = 0; ok; ++qi) {
+                const int64_t u = read_unit_one(s_unit, ufull0, uempty0, qi, s_abort);
+                if (u < 0) break;
+                const int64_t t0 = u / NB * 2;
+                const uint32_t m0 = tile_taps(t0), m1 = tile_taps(t0 + 1);
+                // accumulator h is free once the epilogue has read out unit uc - 1's tile h
+                const uint32_t par = (uc & 1u) ^ 1u;
+                if (!mbar_wait(tempty0, par, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                bool free1 = false;
+                uint32_t acc0 = 0, acc1 = 0;
+                for (int k = 0; k < kTaps && ok; ++k) {
+                    const bool h0 = (m0 >> k) & 1u, h1 = (m1 >> k) & 1u;
+                    if (!h0 && !h1) continue;
+                    if (h1 && !free1) {
+                        if (!mbar_wait(tempty0 + 8, par, s_abort)) { ok = false; break; }
+                        tc_fence_after();
+                        free1 = true;
+                    }
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t stage = it % S, ph = (it / S) & 1u;
+                        if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
+                        fence_proxy_async_smem();
+                        tc_fence_after();
+                        const uint32_t base = smem_u32(sStage + (size_t)stage * C::kStageBytes);
+                        const uint32_t b_base = base + 2 * kABytes;
+                        if (h0) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if constexpr (DT == kTF32)
+                                    mma_tf32(tmem, sw128_kmajor_desc(base + 32 * j), sw128_kmajor_desc(b_base + 32 * j),
+                                             idesc, acc0 | (uint32_t)j);
+                                else
+                                    mma_f16(tmem, sw128_kmajor_desc(base + 32 * j), sw128_kmajor_desc(b_base + 32 * j),
+                                            idesc, acc0 | (uint32_t)j);
+                            }
+                            acc0 = 1;
+                        }
+                        if (h1) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if constexpr (DT == kTF32)
+                                    mma_tf32(tmem + BN, sw128_kmajor_desc(base + kABytes + 32 * j),
+                                             sw128_kmajor_desc(b_base + 32 * j), idesc, acc1 | (uint32_t)j);
+                                else
+                                    mma_f16(tmem + BN, sw128_kmajor_desc(base + kABytes + 32 * j),
+                                            sw128_kmajor_desc(b_base + 32 * j), idesc, acc1 | (uint32_t)j);
+                            }
+                            acc1 = 1;
+                        }
+                        mma_commit(empty0 + 8 * stage);
+                        ++it;
+                    }
+                }
+                // tfull's next phase must not complete before the second tile's epilogue
+                // warps have seen this one: wait for their previous read-out here at the latest
+                if (ok && !free1 && !mbar_wait(tempty0 + 8, par, s_abort)) ok = false;
+                if (ok) mma_commit(tfull);
+                ++uc;
+            }
+            mma_commit(done_bar);
+            const bool drained = mbar_wait_timed(done_bar, 0);
+            if (!ok || !drained) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
+    } else if (warp != 9) {
+        // ------------------------------------------------------------ epilogue (tile h of the pair)
+        const int h = warp >= 10 ? 1 : 0;
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        uint32_t uc = 0;
+        bool ok = true;
+        for (uint32_t qi = 0;; ++qi) {
+            const int64_t u = read_unit_warp(s_unit, ufull0, uempty0, qi, lane, s_abort);
+            if (u < 0) break;
+            const int64_t t = u / NB * 2 + h;
+            const int col0 = (int)(u % NB) * BN;
+            const uint32_t mh = tile_taps(t);
+            const int64_t r_out = t * kBM + q * 32 + lane;
+            const uint32_t v = r_out < a.n ? a.sorted_idx[r_out] : kNone;
+            ok = __all_sync(0xffffffffu, mbar_wait(tfull, uc & 1u, s_abort));
+            ++uc;
+            if (!ok) break;  // warp-uniform
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t acc[32];
+                if (mh != 0u) {  // warp-uniform; a tile with no taps has a zero sum
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c0, acc);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[i] = 0u;
+                }
+                if (v != kNone) store_row32<DT>(a.out + ((int64_t)v * a.Ndim + col0 + c0) * ES, acc, s_bias, a.bias,
+                                                col0 + c0);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * h);
+        }
+        if (!ok) {
+            *s_abort = 1;
+            atomicOr(a.err, kErrTimeout);
+        }
+    } else {
+        // ------------------------------------------------------------ weight-tile loader
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t qi = 0; ok; ++qi) {
+                const int64_t u = read_unit_one(s_unit, ufull0, uempty0, qi, s_abort);
+                if (u < 0) break;
+                const int nb = (int)(u % NB);
+                const int64_t t0 = u / NB * 2;
+                const uint32_t mu = tile_taps(t0) | tile_taps(t0 + 1);
+                for (int k = 0; k < kTaps && ok; ++k) {
+                    if (!((mu >> k) & 1u)) continue;
+                    const uint8_t* bsrc = a.Bimg + ((int64_t)nb * kTaps + k) * KB * C::kBBytes;
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t stage = it % S, ph = (it / S) & 1u;
+                        if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full0 + 8 * stage, C::kBBytes);
+                        bulk_g2s(smem_u32(sStage + (size_t)stage * C::kStageBytes + 2 * kABytes), bsrc + kb * C::kBBytes,
+                                 C::kBBytes, full0 + 8 * stage);
+                        ++it;
+                    }
+                }
+            }
+            if (!ok) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, 2 * BN);
+}
+
 // Repack W into the B-operand tiles the MMA reads: for tap k, N block nb and
 // K block kb, a [BN rows][128 bytes of K] tile (64 16-bit or 32 fp32 K values),
 // rows in the 128-byte swizzled layout (row n at (n/8)*1024 + (n%8)*128,
@@ -564,6 +909,25 @@ int launch_tc(const TcArgs& a, cudaStream_t s) {
     // whatever the counter holds: no reset needed
     if (units > grid) cudaMemsetAsync(b.unit_ctr, 0, sizeof(uint32_t), s);
     kern<<<grid, kThreads, C::kSmem, s>>>(b);
+    return VG_OK;
+}
+
+// Tile pairs at 256 output columns whenever the pairs alone give every SM a unit.
+bool pair_tiles(int64_t num_tiles, int Ndim, int ksplit, int sms) {
+    return ksplit == 1 && choose_bn(Ndim) == PairCfg::BN && (num_tiles + 1) / 2 * (Ndim / PairCfg::BN) >= sms;
+}
+
+template <int DT>
+int launch_pair(const TcArgs& a, cudaStream_t s) {
+    auto kern = k_gather_gemm_pair<DT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PairCfg::kSmem) != cudaSuccess)
+        return VG_ERR_CUDA;
+    const int64_t units = (a.num_tiles + 1) / 2 * (a.Ndim / PairCfg::BN);
+    const int grid = (int)std::min<int64_t>(units, (int64_t)plan_sms(0));
+    TcArgs b = a;
+    b.unit_ctr = a.err + kGatherUnitCounter;
+    if (units > grid) cudaMemsetAsync(b.unit_ctr, 0, sizeof(uint32_t), s);
+    kern<<<grid, kPairThreads, PairCfg::kSmem, s>>>(b);
     return VG_OK;
 }
 
@@ -673,7 +1037,11 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s) {
     if (a.ksplit > 1 && !a.partial) return VG_ERR_INVALID_ARG;
     const int bn = choose_bn(p.Ndim);
     int st;
-    if (p.dtype == VG_F32) {
+    if (pair_tiles(a.num_tiles, p.Ndim, a.ksplit, plan_sms(0))) {
+        st = p.dtype == VG_F32    ? launch_pair<kTF32>(a, s)
+             : p.dtype == VG_BF16 ? launch_pair<kBF16>(a, s)
+                                  : launch_pair<kF16>(a, s);
+    } else if (p.dtype == VG_F32) {
         switch (bn) {
             case 256: st = launch_tc<256, kTF32>(a, s); break;
             case 128: st = launch_tc<128, kTF32>(a, s); break;
