@@ -140,27 +140,19 @@ __device__ __forceinline__ float bits_to_f32(uint16_t b) {
     else return __half2float(__ushort_as_half(b));
 }
 
-// Round 32 fp32 accumulators (+ bias) to the output type and store them: 64 B
-// (16-bit) or 128 B (fp32) of one output row.  The 16-bit bias comes from its
-// shared-memory copy, the fp32 bias straight from global memory (read-only path).
+// Add the bias to 32 fp32 accumulators of one row (columns col..col+31) and round
+// them to the output type: 16 words of two 16-bit values, or 32 fp32 words.
 template <int DT>
-__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&acc)[32], const void* s_bias,
-                                            const void* g_bias, int col) {
+__device__ __forceinline__ void pack_row32(uint32_t* dst, const uint32_t (&acc)[32], const void* s_bias,
+                                           const void* g_bias, int col) {
     const bool has_bias = g_bias != nullptr;
     if constexpr (DT == kTF32) {
-        const float* sb = static_cast<const float*>(g_bias);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        const float* gb = static_cast<const float*>(g_bias);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(acc[4 * i + e]) + (has_bias ? __ldg(sb + col + 4 * i + e) : 0.f);
-            d4[i] = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
-                               __float_as_uint(v[3]));
-        }
+        for (int i = 0; i < 32; ++i)
+            dst[i] = __float_as_uint(__uint_as_float(acc[i]) + (has_bias ? __ldg(gb + col + i) : 0.f));
     } else {
         const uint16_t* sb = static_cast<const uint16_t*>(s_bias);
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
@@ -168,11 +160,54 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&acc)[
                 lo += bits_to_f32<DT == kBF16>(sb[col + 2 * i]);
                 hi += bits_to_f32<DT == kBF16>(sb[col + 2 * i + 1]);
             }
-            pk[i] = pack2<DT == kBF16>(lo, hi);
+            dst[i] = pack2<DT == kBF16>(lo, hi);
         }
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+    }
+}
+
+// Store one 128-byte line of output per row for a warp's 32 rows: lane i holds
+// row i's line (32 words, output columns col.. of row v).  A 4 x 4 transpose of
+// 32-byte blocks inside each lane quad (two shuffle rounds) leaves lane 4g + d
+// with block d of rows 4g..4g+3, so that each of the four stores writes eight
+// whole lines -- eight requests per store instead of 32 scattered 16-byte
+// pieces.  v8ok: the output is 32-byte aligned (one 32-byte store per block).
+template <int ES>
+__device__ __forceinline__ void store_lines_quad(uint8_t* out, int Ndim, uint32_t v, uint32_t (&z)[32], int col,
+                                                 int lane, bool v8ok) {
+    const bool hi = (lane & 2) != 0, odd = (lane & 1) != 0;
+    // round 1 (lanes d and d ^ 2): swap the off-diagonal 2 x 2 groups of blocks
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    for (int sblk = 0; sblk < 2; ++sblk)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t send = hi ? z[8 * sblk + e] : z[8 * (2 + sblk) + e];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+            if (hi) z[8 * sblk + e] = recv;
+            else z[8 * (2 + sblk) + e] = recv;
+        }
+    // round 2 (lanes d and d ^ 1): transpose each 2 x 2 group
+#pragma unroll
+    for (int t = 0; t < 4; t += 2)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t send = odd ? z[8 * t + e] : z[8 * (t + 1) + e];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            if (odd) z[8 * t + e] = recv;
+            else z[8 * (t + 1) + e] = recv;
+        }
+    const int d = lane & 3;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t vk = __shfl_sync(0xffffffffu, v, (lane & ~3) | k);
+        if (vk == kNone) continue;  // the same for the four lanes of the quad
+        uint8_t* dst = out + ((int64_t)vk * Ndim + col) * ES + d * 32;
+        if (v8ok) {
+            st_global_v8(dst, z + 8 * k);
+        } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            d4[0] = make_uint4(z[8 * k], z[8 * k + 1], z[8 * k + 2], z[8 * k + 3]);
+            d4[1] = make_uint4(z[8 * k + 4], z[8 * k + 5], z[8 * k + 6], z[8 * k + 7]);
+        }
     }
 }
 
@@ -414,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(
     } else if (warp <= 8) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const bool v8ok = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
         uint32_t ua = 0;
         bool ok = true;
         const int64_t rows_pad = a.num_tiles * kBM;
@@ -440,19 +476,32 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(
             ++ua;
             if (!ok) break;  // warp-uniform
             tc_fence_after();
+            if (KS > 1) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t acc[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
-                tmem_ld_wait();
-                if (KS > 1) {
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t acc[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
+                    tmem_ld_wait();
                     float4* d4 = reinterpret_cast<float4*>(prow + c0);
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
                                             __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
-                } else if (v != kNone) {
-                    store_row32<DT>(a.out + ((int64_t)v * a.Ndim + col0 + c0) * ES, acc, s_bias, a.bias, col0 + c0);
+                }
+            } else {
+                // one 128-byte output line per row at a time: 64 16-bit or 32 fp32 columns
+                constexpr int kLine = 128 / ES;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += kLine) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int part = 0; part < kLine / 32; ++part) {
+                        uint32_t acc[32];
+                        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0 + 32 * part, acc);
+                        tmem_ld_wait();
+                        pack_row32<DT>(z + part * 16, acc, s_bias, a.bias, col0 + c0 + 32 * part);
+                    }
+                    store_lines_quad<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
                 }
             }
             tc_fence_before();
@@ -773,6 +822,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_gather_gemm_pair(TcArgs a) 
         // ------------------------------------------------------------ epilogue (tile h of the pair)
         const int h = warp >= 10 ? 1 : 0;
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const bool v8ok = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;
         uint32_t uc = 0;
         bool ok = true;
         for (uint32_t qi = 0;; ++qi) {
@@ -787,18 +837,24 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_gather_gemm_pair(TcArgs a) 
             ++uc;
             if (!ok) break;  // warp-uniform
             tc_fence_after();
+            // one 128-byte output line per row at a time: 64 16-bit or 32 fp32 columns
+            constexpr int kLine = 128 / ES;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t acc[32];
-                if (mh != 0u) {  // warp-uniform; a tile with no taps has a zero sum
-                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c0, acc);
-                    tmem_ld_wait();
-                } else {
+            for (int c0 = 0; c0 < BN; c0 += kLine) {
+                uint32_t z[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[i] = 0u;
+                for (int part = 0; part < kLine / 32; ++part) {
+                    uint32_t acc[32];
+                    if (mh != 0u) {  // warp-uniform; a tile with no taps has a zero sum
+                        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + h * BN + c0 + 32 * part, acc);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[i] = 0u;
+                    }
+                    pack_row32<DT>(z + part * 16, acc, s_bias, a.bias, col0 + c0 + 32 * part);
                 }
-                if (v != kNone) store_row32<DT>(a.out + ((int64_t)v * a.Ndim + col0 + c0) * ES, acc, s_bias, a.bias,
-                                                col0 + c0);
+                store_lines_quad<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
             }
             tc_fence_before();
             __syncwarp();
