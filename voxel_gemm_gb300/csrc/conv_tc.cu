@@ -165,50 +165,12 @@ __device__ __forceinline__ void pack_row32(uint32_t* dst, const uint32_t (&acc)[
     }
 }
 
-// Store one 128-byte line of output per row for a warp's 32 rows: lane i holds
-// row i's line (32 words, output columns col.. of row v).  A 4 x 4 transpose of
-// 32-byte blocks inside each lane quad (two shuffle rounds) leaves lane 4g + d
-// with block d of rows 4g..4g+3, so that each of the four stores writes eight
-// whole lines -- eight requests per store instead of 32 scattered 16-byte
-// pieces.  v8ok: the output is 32-byte aligned (one 32-byte store per block).
+// Store one 128-byte line of output per row for a warp's 32 rows (lane i holds
+// row i's line, output columns col.. of row v; kNone: no row).
 template <int ES>
-__device__ __forceinline__ void store_lines_quad(uint8_t* out, int Ndim, uint32_t v, uint32_t (&z)[32], int col,
-                                                 int lane, bool v8ok) {
-    const bool hi = (lane & 2) != 0, odd = (lane & 1) != 0;
-    // round 1 (lanes d and d ^ 2): swap the off-diagonal 2 x 2 groups of blocks
-#pragma unroll
-    for (int sblk = 0; sblk < 2; ++sblk)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t send = hi ? z[8 * sblk + e] : z[8 * (2 + sblk) + e];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
-            if (hi) z[8 * sblk + e] = recv;
-            else z[8 * (2 + sblk) + e] = recv;
-        }
-    // round 2 (lanes d and d ^ 1): transpose each 2 x 2 group
-#pragma unroll
-    for (int t = 0; t < 4; t += 2)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t send = odd ? z[8 * t + e] : z[8 * (t + 1) + e];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            if (odd) z[8 * t + e] = recv;
-            else z[8 * (t + 1) + e] = recv;
-        }
-    const int d = lane & 3;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t vk = __shfl_sync(0xffffffffu, v, (lane & ~3) | k);
-        if (vk == kNone) continue;  // the same for the four lanes of the quad
-        uint8_t* dst = out + ((int64_t)vk * Ndim + col) * ES + d * 32;
-        if (v8ok) {
-            st_global_v8(dst, z + 8 * k);
-        } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-            d4[0] = make_uint4(z[8 * k], z[8 * k + 1], z[8 * k + 2], z[8 * k + 3]);
-            d4[1] = make_uint4(z[8 * k + 4], z[8 * k + 5], z[8 * k + 6], z[8 * k + 7]);
-        }
-    }
+__device__ __forceinline__ void store_lines(uint8_t* out, int Ndim, uint32_t v, uint32_t (&z)[32], int col, int lane,
+                                            bool v8ok) {
+    store_lines_quad(v != kNone ? out + ((int64_t)v * Ndim + col) * ES : nullptr, z, lane, v8ok);
 }
 
 // Reads of unit-ring slot qi % R (phase parity (qi / R) & 1): by one thread, or
@@ -501,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<BN>()) k_gather_gemm_tc(
                         tmem_ld_wait();
                         pack_row32<DT>(z + part * 16, acc, s_bias, a.bias, col0 + c0 + 32 * part);
                     }
-                    store_lines_quad<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
+                    store_lines<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
                 }
             }
             tc_fence_before();
@@ -854,7 +816,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) k_gather_gemm_pair(TcArgs a) 
                     }
                     pack_row32<DT>(z + part * 16, acc, s_bias, a.bias, col0 + c0 + 32 * part);
                 }
-                store_lines_quad<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
+                store_lines<ES>(a.out, a.Ndim, v, z, col0 + c0, lane, v8ok);
             }
             tc_fence_before();
             __syncwarp();

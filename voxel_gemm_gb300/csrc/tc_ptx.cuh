@@ -99,6 +99,52 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
                  "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
 }
+// A warp stores one 128-byte line per lane: lane i holds its line as 32 words
+// and its destination (null: nothing to store).  A 4 x 4
+// transpose of 32-byte blocks inside each lane quad (two shuffle rounds) leaves
+// lane 4g + d with block d of the lines of lanes 4g..4g+3, so each of the four
+// stores writes eight whole lines -- eight requests per store instead of 32
+// scattered 16-byte pieces when every lane writes its own line.  v8ok: the
+// destinations are 32-byte aligned (one 32-byte store per block).
+__device__ __forceinline__ void store_lines_quad(uint8_t* dst, uint32_t (&z)[32], int lane, bool v8ok) {
+    const bool hi = (lane & 2) != 0, odd = (lane & 1) != 0;
+    // round 1 (lanes d and d ^ 2): swap the off-diagonal 2 x 2 groups of blocks
+#pragma unroll
+    for (int sblk = 0; sblk < 2; ++sblk)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t send = hi ? z[8 * sblk + e] : z[8 * (2 + sblk) + e];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+            if (hi) z[8 * sblk + e] = recv;
+            else z[8 * (2 + sblk) + e] = recv;
+        }
+    // round 2 (lanes d and d ^ 1): transpose each 2 x 2 group
+#pragma unroll
+    for (int t = 0; t < 4; t += 2)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t send = odd ? z[8 * t + e] : z[8 * (t + 1) + e];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            if (odd) z[8 * t + e] = recv;
+            else z[8 * (t + 1) + e] = recv;
+        }
+    const int d = lane & 3;
+    const uint64_t mine = reinterpret_cast<uint64_t>(dst);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint64_t pk = __shfl_sync(0xffffffffu, mine, (lane & ~3) | k);
+        if (pk == 0) continue;  // the same for the four lanes of the quad
+        uint8_t* p = reinterpret_cast<uint8_t*>(pk) + d * 32;
+        if (v8ok) {
+            st_global_v8(p, z + 8 * k);
+        } else {
+            uint4* d4 = reinterpret_cast<uint4*>(p);
+            d4[0] = make_uint4(z[8 * k], z[8 * k + 1], z[8 * k + 2], z[8 * k + 3]);
+            d4[1] = make_uint4(z[8 * k + 4], z[8 * k + 5], z[8 * k + 6], z[8 * k + 7]);
+        }
+    }
+}
+
 // Bring the 128-byte line holding p into L2 (no shared memory, no completion tracking).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

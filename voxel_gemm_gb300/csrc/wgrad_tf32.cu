@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     } else {
         // ------------------------------------------------------------ epilogue: fp32 partials
         const int q = warp & 3;
+        const bool v8ok = (reinterpret_cast<uintptr_t>(a.partial) & 31u) == 0;
         uint32_t ua = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
@@ -292,13 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 uint32_t acc[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c0, acc);
                 tmem_ld_wait();
-                if (ci < a.Cin) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + c0);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        d4[i] = make_float4(__uint_as_float(acc[4 * i]), __uint_as_float(acc[4 * i + 1]),
-                                            __uint_as_float(acc[4 * i + 2]), __uint_as_float(acc[4 * i + 3]));
-                }
+                // 32 fp32 columns: one 128-byte line of this lane's row
+                store_lines_quad(ci < a.Cin ? reinterpret_cast<uint8_t*>(dst + c0) : nullptr, acc, lane, v8ok);
             }
             tc_fence_before();
             __syncwarp();
