@@ -89,6 +89,18 @@ struct SparseLayout {
            off_cand_hist = 0, off_cand_status = 0, off_cand_tickets = 0, off_scan = 0, total = 0;
 };
 
+// dY in processing order as the weight gradient's B-operand image (Cout a
+// multiple of 128): 8 KB tiles of 64 sorted rows x 64 channels, ordered [row
+// group r / 64][channel block c / 64], each tile in the 128-byte-swizzled
+// MN-major layout the MMA reads (row rr at (rr / 8) * 1024 + (rr % 8) * 128
+// bytes, its 16-byte chunk cc stored at chunk cc ^ (rr % 8)); the B tile of one
+// stage (64 rows, BN channels) is then one contiguous bulk copy.  Offset, in
+// 16-bit elements, of chunk c8 (channels 8 * c8 .. 8 * c8 + 7) of sorted row r.
+__host__ __device__ __forceinline__ int64_t dy_image_offset(int64_t r, int c8, int Cout) {
+    const int rr = (int)(r & 63), cc = c8 & 7;
+    return ((r >> 6) * (Cout >> 6) + (c8 >> 3)) * 4096 + (rr >> 3) * 512 + (rr & 7) * 64 + ((cc ^ (rr & 7)) << 3);
+}
+
 constexpr int kSortThreads = 256;
 constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digits
 constexpr int kRadixBits = 8;

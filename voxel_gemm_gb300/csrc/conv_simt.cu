@@ -269,8 +269,9 @@ k_dbias_partial(const T* __restrict__ dy, int64_t n, int Cout, int64_t rows, flo
 }
 
 // The same partial sums read through the processing order, fused with the copy of
-// dy into that order that the tensor-core weight gradient loads by TMA:
-// dst[r] = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad; block b sums
+// dy into that order that the tensor-core weight gradient loads by bulk copies:
+// row r of dst = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad, stored
+// as the B-operand image (dy_image_offset); block b sums
 // the sorted rows [b*rows, (b+1)*rows) into partial_db[b][:] (fixed order as above).
 // One read of dy serves both (16-bit types).
 template <typename T>
@@ -300,7 +301,7 @@ k_dbias_sorted(const T* __restrict__ dy, const uint32_t* __restrict__ sorted_idx
                 for (int j = 0; j < 4; ++j) u[j] = *reinterpret_cast<const uint4*>(dy + (int64_t)src[j] * Cout + g * 8);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<uint4*>(dst + (r + j * lanes) * Cout + g * 8) = u[j];
+                    *reinterpret_cast<uint4*>(dst + dy_image_offset(r + j * lanes, g, Cout)) = u[j];
                     const T* e = reinterpret_cast<const T*>(&u[j]);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) acc[q] += to_f32(e[q]);
@@ -308,7 +309,7 @@ k_dbias_sorted(const T* __restrict__ dy, const uint32_t* __restrict__ sorted_idx
             }
             for (; r < r1; r += lanes) {
                 const uint4 u = *reinterpret_cast<const uint4*>(dy + (int64_t)sorted_idx[r] * Cout + g * 8);
-                *reinterpret_cast<uint4*>(dst + r * Cout + g * 8) = u;
+                *reinterpret_cast<uint4*>(dst + dy_image_offset(r, g, Cout)) = u;
                 const T* e = reinterpret_cast<const T*>(&u);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) acc[q] += to_f32(e[q]);
@@ -330,7 +331,8 @@ k_dbias_sorted(const T* __restrict__ dy, const uint32_t* __restrict__ sorted_idx
     if (blockIdx.x == gridDim.x - 1) {  // the padding rows of the sorted copy
         const int64_t chunks = (rows_pad - n) * cg8;
         for (int64_t e = tid; e < chunks; e += 256)
-            reinterpret_cast<uint4*>(dst + n * Cout)[e] = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dst + dy_image_offset(n + e / cg8, (int)(e % cg8), Cout)) =
+                make_uint4(0u, 0u, 0u, 0u);
     }
 }
 

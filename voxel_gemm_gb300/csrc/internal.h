@@ -108,8 +108,9 @@ void launch_reduce_splits(const float* partial, int splits, int64_t total, int64
 // db = column sums of dy over dbias_blocks(n, sms) row blocks, reduced in a fixed order
 // (partial_db holds dbias_blocks(n, sms) x Cout floats).
 int dbias_blocks(int64_t n, int sms);
-// The same db, read through the processing order while copying dy into it:
-// dy_sorted[r] = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad (16-bit dtypes).
+// The same db, read through the processing order while copying dy into it: row r
+// of dy_sorted = dy[sorted_idx[r]] for r < n, zero rows up to rows_pad, stored as
+// the weight gradient's B-operand image (dy_image_offset; 16-bit dtypes).
 void launch_dbias_sorted(const void* dy, const uint32_t* sorted_idx, int64_t n, int64_t rows_pad, int Cout,
                          int sms, void* db, float* partial_db, void* dy_sorted, int dtype,
                          const uint32_t* nbr_status, cudaStream_t s);

@@ -25,11 +25,10 @@
 // (zero fill; each thread's copies arrive on the stage barrier by themselves),
 // warp 4 issues tcgen05.mma, warps 5-8 store the partials.  B (dY) rows are
 // consecutive sorted rows: for Cout >= 128 they are first copied into
-// processing order (one streaming pass) and each stage's B tile is then one
-// TMA tile load per 64 columns, which halves the per-SM cp.async traffic;
-// for Cout = 64 the gather threads fetch them with cp.async as well.
-#include <cuda.h>
-
+// processing order as the B-operand image (one streaming pass, fused with the
+// bias gradient's partial sums), so that each stage's B tile is one contiguous
+// bulk copy (measured at C = 1024: 10.9 ms with four 2D tensor-map tile loads
+// per stage); for Cout = 64 the gather threads fetch them with cp.async as well.
 #include <cstring>
 
 #include "common.cuh"
@@ -97,6 +96,7 @@ struct WgArgs {
     int splits;
     const uint16_t* f;
     const uint16_t* dy;
+    const uint16_t* dy_img;  // dY in processing order as the B-operand image (Cout >= 128)
     int Cin, Cout;
     int taps;        // taps of the kernel (27, or 8): (tap, channel block) slots of the M blocks
     float* partial;  // [splits][27][Cin][Cout]
@@ -183,15 +183,8 @@ __device__ __forceinline__ int64_t next_tile(const WgArgs& a, TileCursor& c, int
     return (int64_t)a.tile_order[c.base + b];
 }
 
-// 2D TMA tile load (box of 64 columns x R rows, 128-byte swizzle) completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// dst[r] = src[sorted_idx[r]] for r < n, zero rows up to rows_pad (16-bit rows of C values).
+// Row r of dst = src[sorted_idx[r]] for r < n, zero rows up to rows_pad (16-bit
+// rows of C values), stored as the B-operand image (dy_image_offset).
 __global__ void __launch_bounds__(256)
 k_sort_rows(const uint16_t* __restrict__ src, const uint32_t* __restrict__ sorted_idx, int64_t n, int64_t rows_pad,
             int C, const uint32_t* __restrict__ nbr_status, uint16_t* __restrict__ dst) {
@@ -203,7 +196,7 @@ k_sort_rows(const uint16_t* __restrict__ src, const uint32_t* __restrict__ sorte
         const int c = (int)(e - r * cpr);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (r < n) v = reinterpret_cast<const uint4*>(src + (int64_t)sorted_idx[r] * C)[c];
-        reinterpret_cast<uint4*>(dst + r * C)[c] = v;
+        *reinterpret_cast<uint4*>(dst + dy_image_offset(r, c, C)) = v;
     }
 }
 
@@ -219,9 +212,10 @@ __device__ __forceinline__ int64_t read_unit(const volatile int64_t* s_unit, uin
 }
 
 template <int BN, bool BF16, bool TWO>
-__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, const __grid_constant__ CUtensorMap tmB) {
-    // B by TMA from the sorted dY copy when the tile is wide (R = 64 rows, box 64 x 64)
-    constexpr bool kTmaB = BN >= 128;
+__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
+    // B by one bulk copy from the dY image when the tile is wide (R = 64 rows)
+    constexpr bool kImgB = BN >= 128;
+    static_assert(!kImgB || WCfg<BN, TWO>::R == 64, "one image row group per stage");
     constexpr bool kDeep = !TWO;  // row metadata two stages ahead
     using C = WCfg<BN, TWO>;
     constexpr int S = C::S;
@@ -335,9 +329,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
             int64_t t1 = -1;
             int h1 = 0;
             if (t0 >= 0) {
-                load_meta<MU, RQ, !kTmaB>(a, mu, t0 * 128, p, m0);
+                load_meta<MU, RQ, !kImgB>(a, mu, t0 * 128, p, m0);
                 advance(t0, h0, t1, h1);
-                if (kDeep && t1 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t1 * 128 + h1 * R, p, m1);
+                if (kDeep && t1 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
             } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
                 null_stage = true;
                 for (int q = 0; q < RQ; ++q) {
@@ -352,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
                 int h2 = 0;
                 if (t1 >= 0) advance(t1, h1, t2, h2);
                 if constexpr (kDeep) {
-                    if (t2 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t2 * 128 + h2 * R, p, m2);
+                    if (t2 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t2 * 128 + h2 * R, p, m2);
                 } else {
-                    if (t1 >= 0) load_meta<MU, RQ, !kTmaB>(a, mu, t1 * 128 + h1 * R, p, m1);
+                    if (t1 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
                 }
                 const int64_t t = t0, tn = t1;
                 const int h = h0;
@@ -369,16 +363,13 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
                 uint8_t* st = stages + (size_t)stage * C::kStageBytes;
                 if (p == 0) {  // published by thread 0's own release arrival below
                     s_info[stage] = (first ? 1u : 0u) | (tn < 0 ? 2u : 0u);
-                    if constexpr (kTmaB) {
+                    if constexpr (kImgB) {
                         const uint32_t bytes = t >= 0 ? NBB * kBlk : 0u;
                         mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
-                        if (t >= 0) {
-                            const uint32_t b_base = smem_u32(st + MU * kABytes);
-#pragma unroll
-                            for (int blk = 0; blk < NBB; ++blk)
-                                tma_load_2d(b_base + blk * kBlk, &tmB, nb * BN + blk * 64, (int)(t * 128 + h * R),
-                                            full0 + 8 * stage);
-                        }
+                        if (t >= 0)  // rows t * 128 + h * 64 .. + 63: row group 2t + h; channel blocks nb * NBB ..
+                            bulk_g2s(smem_u32(st + MU * kABytes),
+                                     a.dy_img + ((2 * t + h) * (a.Cout / 64) + nb * NBB) * (int64_t)(kBlk / 2), bytes,
+                                     full0 + 8 * stage);
                     } else {
                         mbar_arrive(full0 + 8 * stage);
                     }
@@ -399,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a, co
                 }
                 const uint32_t b_base = smem_u32(st + MU * kABytes);
 #pragma unroll
-                for (int e = 0; e < (kTmaB ? 0 : NBB * RQ); ++e) {  // B: block e / RQ, the same rows
+                for (int e = 0; e < (kImgB ? 0 : NBB * RQ); ++e) {  // B: block e / RQ, the same rows
                     const int q = e % RQ, blk = e / RQ;
                     const int row = (p >> 3) + 16 * q;
                     const uint32_t i = mc.i[q];
@@ -531,51 +522,20 @@ int wg_bn(int cout) {
     return 64;
 }
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-// cuTensorMapEncodeTiled from the driver, looked up once (null if unavailable).
-EncodeTiled encode_tiled() {
-    static const EncodeTiled fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiled>(p);
-    }();
-    return fn;
-}
-
 template <int BN, bool BF16, bool TWO>
-int launch_wgrad(const WgArgs& a, const uint16_t* dy_sorted, int sms, cudaStream_t s) {
+int launch_wgrad(const WgArgs& a, int sms, cudaStream_t s) {
     using C = WCfg<BN, TWO>;
     auto kern = k_wgrad_tc<BN, BF16, TWO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
         return VG_ERR_CUDA;
-    CUtensorMap tm;
-    memset(&tm, 0, sizeof(tm));
-    if (BN >= 128) {
-        // [rows_pad][Cout] 16-bit, box = 64 columns x R rows, 128-byte swizzle (the MN-major B layout)
-        const EncodeTiled enc = encode_tiled();
-        if (!enc || !dy_sorted) return VG_ERR_CUDA;
-        const cuuint64_t dims[2] = {(cuuint64_t)a.Cout, (cuuint64_t)(a.num_tiles * kTileRows)};
-        const cuuint64_t strides[1] = {(cuuint64_t)a.Cout * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)C::R};
-        const cuuint32_t es[2] = {1, 1};
-        if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(dy_sorted), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return VG_ERR_CUDA;
-    }
+    if (BN >= 128 && !a.dy_img) return VG_ERR_INVALID_ARG;
     const int MG = (num_munits(a.Cin, a.taps) + C::MU - 1) / C::MU;
     const int64_t units = (int64_t)MG * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, (int64_t)(TWO ? 2 : 1) * sms);
     // with no more units than CTAs every claim returns >= gridDim.x >= units (the end),
     // whatever the counter holds: no reset needed
     if (units > grid) cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
-    kern<<<grid, kThreads, C::kSmem, s>>>(a, tm);
+    kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
 
@@ -591,6 +551,16 @@ int64_t wgrad_splits_mu(int64_t n, int Cin, int Cout, int sms, int taps, int bn,
     const int64_t per_split = MG * (Cout / bn);
     int64_t S = std::max<int64_t>(1, (4 * (int64_t)sms + per_split - 1) / per_split);
     S = std::max<int64_t>(S, (T + 255) / 256);
+    if (bn == 256) {
+        // Keep the rows of the chunks in flight (about sms / per_split of them side by
+        // side) within 64 MiB, so that a chunk's units find its feature and dY rows in
+        // L2 (measured at 602k voxels, C = 256: 23 chunks 1.13 ms with 32 % L2 hits and
+        // 4.0 GB of DRAM reads, 46 chunks 0.99 ms, 74 chunks 0.99 ms; C = 512: 19 chunks
+        // 2.98 ms, 27 chunks 2.92 ms)
+        const int64_t in_flight = (sms + per_split - 1) / per_split;
+        const int64_t chunk_bytes = in_flight * T * kTileRows * (int64_t)(Cin + Cout) * 2;
+        S = std::max<int64_t>(S, (chunk_bytes + (int64_t(64) << 20) - 1) / (int64_t(64) << 20));
+    }
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(3) << 28) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
@@ -638,6 +608,7 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         a.tiles_per_chunk = (a.num_tiles + p.splits - 1) / p.splits;
         a.f = static_cast<const uint16_t*>(p.f);
         a.dy = static_cast<const uint16_t*>(p.dy);
+        a.dy_img = static_cast<const uint16_t*>(p.dy_sorted);
         a.Cin = p.Cin;
         a.Cout = p.Cout;
         a.taps = p.taps;
@@ -663,20 +634,20 @@ int tc_wgrad(const WgradPass& p, cudaStream_t s) {
         int st;
         switch (bn) {
             case 256:
-                st = bf16 ? launch_wgrad<256, true, false>(a, dys, p.sms, s)
-                          : launch_wgrad<256, false, false>(a, dys, p.sms, s);
+                st = bf16 ? launch_wgrad<256, true, false>(a, p.sms, s)
+                          : launch_wgrad<256, false, false>(a, p.sms, s);
                 break;
             case 128:
-                st = bf16 ? launch_wgrad<128, true, true>(a, dys, p.sms, s)
-                          : launch_wgrad<128, false, true>(a, dys, p.sms, s);
+                st = bf16 ? launch_wgrad<128, true, true>(a, p.sms, s)
+                          : launch_wgrad<128, false, true>(a, p.sms, s);
                 break;
             default:
                 if (wgrad_two_cta(p.n, p.Cin, p.Cout, p.sms, p.taps))
-                    st = bf16 ? launch_wgrad<64, true, true>(a, dys, p.sms, s)
-                              : launch_wgrad<64, false, true>(a, dys, p.sms, s);
+                    st = bf16 ? launch_wgrad<64, true, true>(a, p.sms, s)
+                              : launch_wgrad<64, false, true>(a, p.sms, s);
                 else
-                    st = bf16 ? launch_wgrad<64, true, false>(a, dys, p.sms, s)
-                              : launch_wgrad<64, false, false>(a, dys, p.sms, s);
+                    st = bf16 ? launch_wgrad<64, true, false>(a, p.sms, s)
+                              : launch_wgrad<64, false, false>(a, p.sms, s);
                 break;
         }
         if (st != VG_OK) return st;
