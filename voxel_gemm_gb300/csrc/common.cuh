@@ -101,6 +101,18 @@ __host__ __device__ __forceinline__ int64_t dy_image_offset(int64_t r, int c8, i
     return ((r >> 6) * (Cout >> 6) + (c8 >> 3)) * 4096 + (rr >> 3) * 512 + (rr & 7) * 64 + ((cc ^ (rr & 7)) << 3);
 }
 
+// fp32 dY in processing order as the TF32 weight gradient's B-operand image
+// (K-major: the contraction runs over rows): per group of 32 sorted rows, each
+// channel's 32 values form a 128-byte row, channels in order, in the 128-byte
+// swizzle (channel c at (c / 8) * 1024 + (c % 8) * 128 bytes of its group, its
+// 16-byte chunk of rows 4kc..4kc+3 stored at chunk kc ^ (c % 8)); the B tile of
+// a stage (32 rows, BN channels) is then one contiguous bulk copy.  Offset, in
+// floats, of sorted row r, channel c.
+__host__ __device__ __forceinline__ int64_t tf32_dy_image_offset(int64_t r, int c, int Cout) {
+    const int kc = (int)((r & 31) >> 2);
+    return (r >> 5) * (int64_t)Cout * 32 + (c >> 3) * 256 + (c & 7) * 32 + ((kc ^ (c & 7)) << 2) + (int)(r & 3);
+}
+
 constexpr int kSortThreads = 256;
 constexpr int kMaxSortPasses = 8;                     // 64-bit keys, 8-bit digits
 constexpr int kRadixBits = 8;

@@ -336,6 +336,59 @@ k_dbias_sorted(const T* __restrict__ dy, const uint32_t* __restrict__ sorted_idx
     }
 }
 
+// fp32 dy in processing order as the TF32 weight gradient's B-operand image
+// (tf32_dy_image_offset), zero rows from n up to rows_pad.  Block b takes the
+// sorted rows [b*rows, (b+1)*rows) in groups of 32, 32 channels at a time: each
+// thread loads 4 channels of one row (a 32 x 32 tile through shared memory) and
+// writes 4 rows of one channel (16 bytes of a 128-byte image row).  With
+// partial_db, block b also sums its rows into partial_db[b][:] (fixed order: each
+// thread over its row of every group, then the 32 threads of a channel in order).
+__global__ void __launch_bounds__(256)
+k_dy_image_tf32(const float* __restrict__ dy, const uint32_t* __restrict__ sorted_idx, int64_t n, int64_t rows_pad,
+                int Cout, int64_t rows, float* __restrict__ partial_db, float* __restrict__ img,
+                const uint32_t* __restrict__ nbr_status) {
+    __shared__ float tile[32][33];
+    __shared__ float red[32][33];
+    if (*nbr_status) return;
+    const int tid = threadIdx.x;
+    const int lr = tid >> 3, lc = tid & 7;  // load: row lr of the group, channels 4lc..4lc+3
+    const int wc = tid >> 3, wk = tid & 7;  // store: channel wc of the block, rows 4wk..4wk+3
+    const int64_t r0 = (int64_t)blockIdx.x * rows, r1 = min(rows_pad, r0 + rows);
+    for (int c0 = 0; c0 < Cout; c0 += 32) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int64_t g0 = r0; g0 < r1; g0 += 32) {
+            const int64_t r = g0 + lr;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) v = *reinterpret_cast<const float4*>(dy + (int64_t)sorted_idx[r] * Cout + c0 + 4 * lc);
+            acc[0] += v.x;
+            acc[1] += v.y;
+            acc[2] += v.z;
+            acc[3] += v.w;
+            __syncthreads();  // the previous group's tile has been read
+            tile[lr][4 * lc] = v.x;
+            tile[lr][4 * lc + 1] = v.y;
+            tile[lr][4 * lc + 2] = v.z;
+            tile[lr][4 * lc + 3] = v.w;
+            __syncthreads();
+            const float4 o = make_float4(tile[4 * wk][wc], tile[4 * wk + 1][wc], tile[4 * wk + 2][wc], tile[4 * wk + 3][wc]);
+            *reinterpret_cast<float4*>(img + tf32_dy_image_offset(g0 + 4 * wk, c0 + wc, Cout)) = o;
+        }
+        if (partial_db) {
+            red[lr][4 * lc] = acc[0];
+            red[lr][4 * lc + 1] = acc[1];
+            red[lr][4 * lc + 2] = acc[2];
+            red[lr][4 * lc + 3] = acc[3];
+            __syncthreads();
+            if (tid < 32) {
+                float sum = 0.f;
+                for (int l = 0; l < 32; ++l) sum += red[l][tid];
+                partial_db[(int64_t)blockIdx.x * Cout + c0 + tid] = sum;
+            }
+            __syncthreads();
+        }
+    }
+}
+
 template <typename T>
 static int launch_gather(const GatherPass& p, cudaStream_t s) {
     const dim3 grid((unsigned)((p.n + BM - 1) / BM), (unsigned)((p.Ndim + BN - 1) / BN));
@@ -472,6 +525,17 @@ void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float*
     if (dtype == VG_F32) dbias_t<float>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
     else if (dtype == VG_F16) dbias_t<__half>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
     else dbias_t<__nv_bfloat16>(dy, n, Cout, sms, db, partial_db, nbr_status, s);
+}
+
+void launch_dy_image_tf32(const void* dy, const uint32_t* sorted_idx, int64_t n, int64_t rows_pad, int Cout, int sms,
+                          void* db, float* partial_db, void* img, const uint32_t* nbr_status, cudaStream_t s) {
+    const int R = dbias_blocks(n, sms);  // R * rows >= rows_pad (rows is a multiple of 256)
+    k_dy_image_tf32<<<R, 256, 0, s>>>(static_cast<const float*>(dy), sorted_idx, n, rows_pad, Cout,
+                                      dbias_rows(n, sms), db ? partial_db : nullptr, static_cast<float*>(img),
+                                      nbr_status);
+    if (db)
+        k_reduce_db<float><<<(unsigned)((Cout + 31) / 32), 256, 0, s>>>(partial_db, R, Cout, static_cast<float*>(db),
+                                                                       nbr_status);
 }
 
 // out[i] = sum over p = 0 .. nparts-1, in that order, of parts[p][i] (fp32 adds),

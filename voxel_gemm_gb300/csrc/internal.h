@@ -91,7 +91,7 @@ struct WgradPass {
     void* db;      // may be null
     float* partial;     // [S][27][Cin][Cout]
     float* partial_db;  // [S][Cout]
-    void* dy_sorted;    // tensor-core path: tc_wgrad_sorted_dy_bytes bytes of scratch (or null if 0)
+    void* dy_sorted;    // tc_wgrad_sorted_dy_bytes (16-bit) or tf32_dy_image_bytes (TF32) bytes of scratch
     int splits;
     int sms;            // SM count of the plan (grid sizes, db row blocks)
     int taps = 27;      // dW has taps x Cin x Cout entries (partials keep a 27-tap stride)
@@ -116,6 +116,11 @@ void launch_dbias_sorted(const void* dy, const uint32_t* sorted_idx, int64_t n, 
                          const uint32_t* nbr_status, cudaStream_t s);
 void launch_dbias(const void* dy, int64_t n, int Cout, int sms, void* db, float* partial_db,
                   int dtype, const uint32_t* nbr_status, cudaStream_t s);
+// fp32 dy in processing order as the TF32 weight gradient's B-operand image
+// (tf32_dy_image_offset), rows n..rows_pad zero; with db non-null, fused with
+// db's fixed-order partial sums over dbias_blocks(n, sms) row blocks and their reduce.
+void launch_dy_image_tf32(const void* dy, const uint32_t* sorted_idx, int64_t n, int64_t rows_pad, int Cout, int sms,
+                          void* db, float* partial_db, void* img, const uint32_t* nbr_status, cudaStream_t s);
 
 // Space-filling-curve codes (curve 0 = z-order, 1 = Hilbert) of (b,x,y,z) rows and back.
 int curve_encode(const int32_t* coords, int64_t n, int bits, int curve, uint64_t* codes, cudaStream_t s);
@@ -139,6 +144,7 @@ int tc_gather_pass(const GatherPass& p, const void* packed, cudaStream_t s);
 int tc_wgrad(const WgradPass& p, cudaStream_t s);
 // TF32 weight gradient (fp32 features, Cin and Cout multiples of 32): split-K chunks and the pass.
 int tf32_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps = 27);
+size_t tf32_dy_image_bytes(int64_t n, int Cout);  // scratch for the TF32 weight gradient's dY image
 int tf32_wgrad(const WgradPass& p, cudaStream_t s);
 // Scratch of the weight gradient: dY rows copied into processing order (zero rows
 // pad the last tile) when Cout takes the wide-N kernel, else 0 bytes.

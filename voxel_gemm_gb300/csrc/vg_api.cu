@@ -51,7 +51,9 @@ static int conv_plan2(int64_t n_fwd, int64_t n_dgrad, int taps, int Cin, int Cou
     p.off_wbwd = o;        o += packed ? align_up(tc_packed_weight_bytes(dtype, Cout, Cin), 256) : 0;
     p.off_partial = o;     o += align_up((size_t)p.splits * kTaps * Cin * Cout * 4, 256);
     p.off_partial_db = o;  o += align_up((size_t)dbias_blocks(N, p.sms) * Cout * 4, 256);
-    p.off_dys = o;         o += p.tensor_core ? align_up(tc_wgrad_sorted_dy_bytes(N, Cout), 256) : 0;
+    p.off_dys = o;         o += p.tensor_core ? align_up(tc_wgrad_sorted_dy_bytes(N, Cout), 256)
+                                : p.tf32      ? align_up(tf32_dy_image_bytes(N, Cout), 256)
+                                              : 0;
     p.off_gpart = o;       o += align_up(gpart, 256);
     (void)wbytes;
     p.total = o;

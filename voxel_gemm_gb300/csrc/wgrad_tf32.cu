@@ -8,16 +8,23 @@
 // in a fixed order by k_reduce_splits (bitwise deterministic).
 //
 // Both MMA operands are kept K-major (K = voxel rows): the contraction runs over
-// rows, while features and gradients are stored row-major, so the producer warps
-// transpose on the way into shared memory.  Per stage of 32 rows, a lane loads
-// four 16-byte pieces (4 channels) of four consecutive rows, transposes the 4x4
-// block in registers and stores four 16-byte pieces (4 rows of one channel) into
-// the 128-byte-swizzled K-major image; lanes are laid out so that those stores
-// hit distinct bank groups.
+// rows, while features and gradients are stored row-major.
+//   B (dY): before the kernel, one streaming pass copies dY into processing order
+//   as the B-operand image (tf32_dy_image_offset: per 32 sorted rows, each
+//   channel's 32 values in a 128-byte swizzled row), fused with the bias
+//   gradient's partial sums; a stage's B tile is then one contiguous bulk copy,
+//   issued by a loader warp as soon as the stage's slot is free.
+//   A (gathered features of one tap, 128 channels): the producer warps copy each
+//   stage's 32 neighbour rows row-major into a staging ring with cp.async, several
+//   stages ahead, then transpose each landed stage from shared memory into the
+//   K-major image (4x4 blocks through registers; the staging rows are XOR-swizzled
+//   so that both the copies and the transposing reads are free of bank conflicts).
 //   A: M = 128 input channels of one tap (masked past Cin), K = 32 rows
 //   B: N = BN output channels,                                K = 32 rows
-// Warps 0-7 produce, warp 8 allocates TMEM and issues the MMAs (4 per stage,
-// K = 8 each), warps 9-12 write the fp32 partials.  Every wait is bounded.
+// Warps 0-7 produce A, warp 8 allocates TMEM and issues the MMAs (4 per stage,
+// K = 8 each), warps 9-12 write the fp32 partials, warp 13 loads B.  Units are
+// taken N block first, so that the CTAs working side by side gather the same
+// neighbour rows.  Every wait is bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -28,22 +35,29 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kProducerWarps = 8;  // (4 left one load latency per stage exposed: 2x slower)
-constexpr int kMmaWarp = kProducerWarps;
-constexpr int kThreads = (kProducerWarps + 1 + 4) * 32;
+
+constexpr int kProducerWarps = 8;
+constexpr int kMmaWarp = kProducerWarps;       // warp 8
+constexpr int kEpiWarp0 = kProducerWarps + 1;  // warps 9-12
+constexpr int kLoaderWarp = kEpiWarp0 + 4;     // warp 13
+constexpr int kThreads = (kLoaderWarp + 1) * 32;
+constexpr int kProducers = kProducerWarps * 32;
 constexpr int kRows = 32;  // voxel rows per stage (one 128-byte K block of fp32)
 constexpr int kBM = 128;   // input channels per unit
+constexpr int kStgBytes = kRows * kBM * 4;  // one staging slot: 32 rows x 128 channels, row-major (512 B rows)
 
 template <int BN>
 struct TCfg {
     static constexpr int kABytes = kBM * 128;
     static constexpr int kBBytes = BN * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int S = 196608 / kStageBytes < 8 ? 196608 / kStageBytes : 8;
+    static constexpr int S = BN == 256 ? 3 : (BN == 128 ? 4 : 5);  // MMA operand stages
+    static constexpr int D = BN == 256 ? 4 : 5;                     // staging slots (copies D - 1 stages ahead)
     static constexpr int NBUF = 2;
     static constexpr int kTmemCols = NBUF * BN;
-    static constexpr int kNumBars = 2 * S + 2 * NBUF + 1;
-    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + 8 * kNumBars + 4 * S + 16;
+    static constexpr int kNumBars = 3 * S + 2 * NBUF + 1;  // full, empty, bfull; tfull, tempty; done
+    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + (size_t)D * kStgBytes + 8 * kNumBars + 4 * S + 16;
+    static_assert(kSmem <= 232448, "TF32 weight-gradient stages exceed one CTA's shared memory");
 };
 
 struct T32Args {
@@ -55,7 +69,7 @@ struct T32Args {
     int64_t n, num_tiles, tiles_per_chunk;
     int splits, taps;
     const float* f;
-    const float* dy;
+    const float* dy_img;  // dY in processing order as the B-operand image (tf32_dy_image_offset)
     int Cin, Cout;
     float* partial;  // [splits][27][Cin][Cout]
     uint32_t* err;
@@ -76,15 +90,85 @@ __device__ __forceinline__ void store_t4(uint8_t* img, int m0, int kc, const flo
     }
 }
 
+// Byte offset, in a staging slot, of 16-byte chunk c (channels 4c..4c+3) of row r:
+// chunk c ^ (r & 4), so that eight lanes reading one chunk from each of rows
+// 4q..4q+3 (two row quads) cover all eight bank groups.
+__device__ __forceinline__ uint32_t stg_off(int r, int c) { return (uint32_t)(r * 512 + ((c ^ (r & 4)) << 4)); }
+
+// Walk over the stages of the CTA's units: unit u = nb + NB * (mb + MB * (k + taps * s))
+// (N blocks of one (M block, tap, chunk) next to each other), each unit the
+// positions [first, end) of the tile visiting order whose tile mask has tap k (the
+// first position always counts, so no unit is empty), four 32-row stages per tile.
+struct StageWalk {
+    int64_t u, s, first, end, pos, npos, t;
+    int mb, k, nb, h;
+    bool valid, first_stage;
+};
+
+__device__ __forceinline__ int64_t next_active(const T32Args& a, int64_t pos, int64_t first, int64_t end, int k) {
+    for (; pos < end; ++pos)
+        if (pos == first || ((a.tile_mask[a.tile_order[pos]] >> k) & 1u)) return pos;
+    return -1;
+}
+
+__device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units) {
+    w.valid = w.u < units;
+    if (!w.valid) return;
+    w.nb = (int)(w.u % NB);
+    int64_t r = w.u / NB;
+    w.mb = (int)(r % MB);
+    r /= MB;
+    w.k = (int)(r % a.taps);
+    w.s = r / a.taps;
+    w.first = w.s * a.tiles_per_chunk;
+    w.end = min(a.num_tiles, w.first + a.tiles_per_chunk);
+    w.pos = w.first;
+    w.t = a.tile_order[w.pos];
+    w.npos = next_active(a, w.pos + 1, w.first, w.end, w.k);
+    w.h = 0;
+    w.first_stage = true;
+}
+
+__device__ __forceinline__ bool walk_last(const StageWalk& w) { return w.h == 128 / kRows - 1 && w.npos < 0; }
+
+__device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units) {
+    w.first_stage = false;
+    if (w.h + 1 < 128 / kRows) {
+        ++w.h;
+    } else if (w.npos >= 0) {
+        w.pos = w.npos;
+        w.t = a.tile_order[w.pos];
+        w.npos = next_active(a, w.pos + 1, w.first, w.end, w.k);
+        w.h = 0;
+    } else {
+        w.u += gridDim.x;
+        walk_unit(w, a, MB, NB, units);
+    }
+}
+
+// bar.red.or over the named barrier: every participant gets the OR of the predicates.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     using C = TCfg<BN>;
-    constexpr int S = C::S;
-    constexpr int NBUF = C::NBUF;
+    constexpr int S = C::S, D = C::D, NBUF = C::NBUF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)S * C::kStageBytes);
+    uint8_t* stages = smem;                                     // [S][A image | B image]
+    uint8_t* stg = smem + (size_t)S * C::kStageBytes;           // [D][32 rows x 512 B], row-major
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stg + (size_t)D * kStgBytes);
     uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
     uint32_t* s_tmem = s_info + S;
     volatile uint32_t* s_abort = s_tmem + 1;
@@ -92,13 +176,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     if (*a.nbr_status) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-    const uint32_t tfull0 = smem_u32(bars + 2 * S), tempty0 = smem_u32(bars + 2 * S + NBUF);
-    const uint32_t done_bar = smem_u32(bars + 2 * S + 2 * NBUF);
+    // full: the producers' A image; bfull: the loader's B tile (transaction bytes)
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), bfull0 = smem_u32(bars + 2 * S);
+    const uint32_t tfull0 = smem_u32(bars + 3 * S), tempty0 = smem_u32(bars + 3 * S + NBUF);
+    const uint32_t done_bar = smem_u32(bars + 3 * S + 2 * NBUF);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(full0 + 8 * i, kProducerWarps * 32);  // every producer thread
-            mbar_init(empty0 + 8 * i, 1);   // one tcgen05.commit
+            mbar_init(full0 + 8 * i, kProducers);  // every producer thread
+            mbar_init(empty0 + 8 * i, 1);          // one tcgen05.commit
+            mbar_init(bfull0 + 8 * i, 1);          // the loader's expect_tx
         }
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(tfull0 + 8 * i, 1);
@@ -120,120 +206,73 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     const int MB = (a.Cin + kBM - 1) / kBM;
     const int NB = a.Cout / BN;
     const int64_t units = (int64_t)MB * a.taps * NB * a.splits;
-    // unit u = mb + MB * (k + taps * (nb + NB * s))
-    auto decode = [&](int64_t u, int& mb, int& k, int& nb, int64_t& s) {
-        mb = (int)(u % MB);
-        int64_t r = u / MB;
-        k = (int)(r % a.taps);
-        r /= a.taps;
-        nb = (int)(r % NB);
-        s = r / NB;
-    };
-    // the unit's tiles: positions [first, end) of the visiting order whose mask has
-    // tap k; the first position always counts (so no unit is empty)
-    auto next_active = [&](int64_t pos, int64_t first, int64_t end, int k) -> int64_t {
-        for (; pos < end; ++pos)
-            if (pos == first || ((a.tile_mask[a.tile_order[pos]] >> k) & 1u)) return pos;
-        return -1;
-    };
 
     if (warp < kProducerWarps) {
-        // ------------------------------------------------------------ producers (transposing gather)
+        // ------------------------------------------------------------ producers: copy, then transpose
+        // Stage i: (1) this thread's copies of stage i have landed (cp.async groups
+        // are committed one per stage, D - 1 stages ahead) and a barrier over the
+        // producers makes everyone's visible -- and tells that everyone has finished
+        // transposing stage i - 1, whose staging slot the copies of stage i + D - 1
+        // then reuse; (2) transpose stage i into its operand slot once the MMAs of
+        // stage i - S are done.  All producers walk the same stages and meet at the
+        // same barriers; a failed wait ends the loop for all of them at the next one.
         const int p = threadIdx.x;
-        const int rq = lane >> 2, cg = lane & 3;  // row quad (rows 4rq..4rq+3), channel group
-        uint32_t it = 0;
+        const int rq = lane >> 2, cg = lane & 3;  // transpose: rows 4rq..4rq+3, channels 16 * warp + 4cg..
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int mb, k, nb;
-            int64_t s;
-            decode(u, mb, k, nb, s);
-            const int ci0 = mb * kBM, co0 = nb * BN;
-            const int64_t first = s * a.tiles_per_chunk;
-            const int64_t end = min(a.num_tiles, first + a.tiles_per_chunk);
-            int64_t pos = next_active(first, first, end, k);
-            bool first_stage = true;
-            // Software pipeline: the row indices of a stage are loaded one stage ahead, and
-            // a stage's data loads are all issued before its slot is waited for and before
-            // any store (loads of independent rows in flight together; with the loads and
-            // stores interleaved per 4x4 block the producers paced the pass, 0.03 of the
-            // TF32 peak at C = 256).
-            int64_t t = pos >= 0 ? a.tile_order[pos] : 0;
-            int64_t npos = pos >= 0 ? next_active(pos + 1, first, end, k) : -1;
-            int h = 0;
-            uint32_t jn[4], in[4];  // this stage's neighbour rows (tap k) and dY rows
-            auto load_idx = [&](int64_t tt, int hh, uint32_t (&jj)[4], uint32_t (&ii)[4]) {
-                const int64_t rr = tt * 128 + hh * kRows + 4 * rq;  // < num_tiles * 128 always
+        StageWalk wc, wt;  // copy walker (D - 1 stages ahead) and transpose walker
+        wc.u = blockIdx.x;
+        walk_unit(wc, a, MB, NB, units);
+        wt = wc;
+        uint32_t jn[4];  // neighbour rows (tap k) of this warp's rows warp + 8q of the copy walker's stage
+        auto load_idx = [&]() {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    jj[e] = a.sorted_nbr[(rr + e) * kTaps + k];
-                    ii[e] = rr + e < a.n ? a.sorted_idx[rr + e] : kNone;
-                }
-            };
-            if (pos >= 0) load_idx(t, 0, jn, in);
-            while (pos >= 0 && ok) {
-                // data of this stage
-                constexpr int PW = kProducerWarps;
-                constexpr int NAP = (kBM / 16 + PW - 1) / PW;  // A blocks of 16 channels per warp
-                constexpr int NBP = (BN / 16 + PW - 1) / PW;   // B blocks per warp (at most)
-                float4 va[NAP][4], vb[NBP][4];
-#pragma unroll
-                for (int P = 0; P < NAP; ++P) {
-                    const int c = ci0 + (warp + PW * P) * 16 + cg * 4;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        va[P][e] = (jn[e] != kNone && c < a.Cin)
-                                       ? __ldg(reinterpret_cast<const float4*>(a.f + (int64_t)jn[e] * a.Cin + c))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int P = 0; P < NBP; ++P) {
-                    const int cl = (warp + PW * P) * 16 + cg * 4;
-                    const bool blk = warp + PW * P < BN / 16;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        vb[P][e] = blk && in[e] != kNone
-                                       ? __ldg(reinterpret_cast<const float4*>(a.dy + (int64_t)in[e] * a.Cout + co0 + cl))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                // the next stage's position and row indices
-                const bool last = npos < 0 && h == 128 / kRows - 1;
-                int64_t t_next = t, pos_next = pos, npos_next = npos;
-                int h_next = h + 1;
-                if (h_next == 128 / kRows) {
-                    h_next = 0;
-                    pos_next = npos;
-                    if (pos_next >= 0) {
-                        t_next = a.tile_order[pos_next];
-                        npos_next = next_active(pos_next + 1, first, end, k);
-                    }
-                }
-                if (!last) load_idx(t_next, h_next, jn, in);
-                const uint32_t stage = it % S, ph = (it / S) & 1u;
-                if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, s_abort)) {
-                    ok = false;
-                    *s_abort = 1;
-                    break;
-                }
-                uint8_t* img_a = stages + (size_t)stage * C::kStageBytes;
-                uint8_t* img_b = img_a + C::kABytes;
-#pragma unroll
-                for (int P = 0; P < NAP; ++P) store_t4(img_a, (warp + PW * P) * 16 + cg * 4, rq, va[P]);
-#pragma unroll
-                for (int P = 0; P < NBP; ++P)
-                    if (warp + PW * P < BN / 16) store_t4(img_b, (warp + PW * P) * 16 + cg * 4, rq, vb[P]);
-                if (p == 0) s_info[stage] = (first_stage ? 1u : 0u) | (last ? 2u : 0u);
-                // (the MMA thread orders these generic-proxy stores before its async-proxy
-                // reads with one proxy fence after the stage barrier, as for cp.async data)
-                mbar_arrive(full0 + 8 * stage);
-                ++it;
-                first_stage = false;
-                if (last) break;
-                t = t_next;
-                h = h_next;
-                pos = pos_next;
-                npos = npos_next;
+            for (int q = 0; q < 4; ++q) {
+                const int64_t r = wc.t * 128 + wc.h * kRows + warp + 8 * q;  // < num_tiles * 128 always
+                jn[q] = wc.valid ? a.sorted_nbr[r * kTaps + wc.k] : kNone;
             }
+        };
+        auto issue = [&](uint32_t j) {  // the copies of stage j (the copy walker's), then advance it
+            if (wc.valid) {
+                const uint32_t base = smem_u32(stg + (size_t)(j % D) * kStgBytes);
+                const int ch = wc.mb * kBM + 4 * lane;
+                const bool cv = ch < a.Cin;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool v = cv && jn[q] != kNone;
+                    const float* src = a.f + (int64_t)(v ? jn[q] : 0u) * a.Cin + (cv ? ch : 0);
+                    cp_async16(base + stg_off(warp + 8 * q, lane), src, v ? 16u : 0u);
+                }
+                walk_next(wc, a, MB, NB, units);
+                load_idx();
+            }
+            cp_async_commit();
+        };
+        load_idx();
+#pragma unroll 1
+        for (uint32_t j = 0; j + 1 < D; ++j) issue(j);
+        for (uint32_t i = 0; wt.valid; ++i) {
+            cp_async_wait<D - 2>();
+            if (named_bar_any(1, kProducers, !ok)) break;  // the same decision in every producer
+            issue(i + D - 1);
+            const uint32_t st = i % S, ph = (i / S) & 1u;
+            if (mbar_wait(empty0 + 8 * st, ph ^ 1u, s_abort)) {
+                const uint8_t* slot = stg + (size_t)(i % D) * kStgBytes;
+                float4 v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[e] = *reinterpret_cast<const float4*>(slot + stg_off(4 * rq + e, 4 * warp + cg));
+                store_t4(stages + (size_t)st * C::kStageBytes, 16 * warp + 4 * cg, rq, v);
+                if (p == 0) s_info[st] = (wt.first_stage ? 1u : 0u) | (walk_last(wt) ? 2u : 0u);
+                // (the MMA thread orders these generic-proxy stores before its async-proxy
+                // reads with one proxy fence after the stage barrier)
+                mbar_arrive(full0 + 8 * st);
+            } else {  // leave at the next barrier, with the others (the walkers stay in step)
+                ok = false;
+                *s_abort = 1;
+            }
+            walk_next(wt, a, MB, NB, units);
         }
+        cp_async_wait_all();  // no copy of this thread is still writing shared memory
         if (!ok) atomicOr(a.err, kErrTimeout);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -248,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 const uint32_t d_tmem = tmem + buf * BN;
                 while (true) {
                     const uint32_t stage = it % S, ph = (it / S) & 1u;
-                    if (!mbar_wait(full0 + 8 * stage, ph, s_abort)) { ok = false; break; }
+                    if (!mbar_wait(full0 + 8 * stage, ph, s_abort) || !mbar_wait(bfull0 + 8 * stage, ph, s_abort)) {
+                        ok = false;
+                        break;
+                    }
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t info = s_info[stage];
@@ -272,16 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < kLoaderWarp) {
         // ------------------------------------------------------------ epilogue: fp32 partials
         const int q = warp & 3;
         const bool v8ok = (reinterpret_cast<uintptr_t>(a.partial) & 31u) == 0;
         uint32_t ua = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
-            int mb, k, nb;
-            int64_t s;
-            decode(u, mb, k, nb, s);
+            const int nb = (int)(u % NB);
+            int64_t r = u / NB;
+            const int mb = (int)(r % MB);
+            r /= MB;
+            const int k = (int)(r % a.taps);
+            const int64_t s = r / a.taps;
             const uint32_t buf = ua % NBUF;
             ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * buf, (ua / NBUF) & 1u, s_abort));
             if (!ok) break;
@@ -304,6 +349,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             *s_abort = 1;
             atomicOr(a.err, kErrTimeout);
         }
+    } else {
+        // ------------------------------------------------------------ B loader: one bulk copy per stage
+        if (lane == 0) {
+            StageWalk wl;
+            wl.u = blockIdx.x;
+            walk_unit(wl, a, MB, NB, units);
+            uint32_t i = 0;
+            bool ok = true;
+            for (; wl.valid; ++i) {
+                const uint32_t st = i % S, ph = (i / S) & 1u;
+                if (!mbar_wait(empty0 + 8 * st, ph ^ 1u, s_abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bfull0 + 8 * st, C::kBBytes);
+                bulk_g2s(smem_u32(stages + (size_t)st * C::kStageBytes + C::kABytes),
+                         a.dy_img + tf32_dy_image_offset(wl.t * 128 + wl.h * kRows, wl.nb * BN, a.Cout), C::kBBytes,
+                         bfull0 + 8 * st);
+                walk_next(wl, a, MB, NB, units);
+            }
+            // before the block may exit, every issued copy must have landed
+            for (uint32_t d = 0; d < S && d < i; ++d) {
+                const uint32_t last = i - 1 - d;
+                if (!mbar_wait_timed(bfull0 + 8 * (last % S), (last / S) & 1u)) ok = false;
+            }
+            if (!ok) {
+                *s_abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -334,17 +410,28 @@ int launch_tf32(const T32Args& a, int sms, cudaStream_t s) {
 }  // namespace
 
 // Split-K chunks: about four units per SM, chunks of at most 256 tiles, at least
-// 4 tiles per chunk, partial sums capped at 1 GiB (as the 16-bit kernel).
+// 4 tiles per chunk, the rows of the chunks in flight (about sms / per_split of
+// them side by side) within 64 MiB so that a chunk's units find its feature and
+// dY rows in L2 (602k voxels, C = 256: 19 chunks 7.9 ms, 55 chunks 7.0 ms, with
+// the earlier register-staged producers), partial sums capped at 1 GiB.
 int tf32_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
     const int64_t per_split = (int64_t)((Cin + kBM - 1) / kBM) * taps * (Cout / tf32_bn(Cout));
     int64_t S = std::max<int64_t>(1, (4 * (int64_t)sms + per_split - 1) / per_split);
     S = std::max<int64_t>(S, (T + 255) / 256);
+    const int64_t in_flight = (sms + per_split - 1) / per_split;
+    const int64_t chunk_bytes = in_flight * T * kTileRows * (int64_t)(Cin + Cout) * 4;
+    S = std::max<int64_t>(S, (chunk_bytes + (int64_t(64) << 20) - 1) / (int64_t(64) << 20));
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
     const int64_t tpc = (T + S - 1) / S;
     return (int)((T + tpc - 1) / tpc);
+}
+
+size_t tf32_dy_image_bytes(int64_t n, int Cout) {
+    const int64_t rows = (n + kTileRows - 1) / kTileRows * kTileRows;
+    return (size_t)rows * Cout * 4;
 }
 
 int tf32_wgrad(const WgradPass& p, cudaStream_t s) {
@@ -362,11 +449,15 @@ int tf32_wgrad(const WgradPass& p, cudaStream_t s) {
         a.tiles_per_chunk = (a.num_tiles + p.splits - 1) / p.splits;
         a.taps = p.taps;
         a.f = static_cast<const float*>(p.f);
-        a.dy = static_cast<const float*>(p.dy);
+        a.dy_img = static_cast<const float*>(p.dy_sorted);
         a.Cin = p.Cin;
         a.Cout = p.Cout;
         a.partial = p.partial;
         a.err = p.err;
+        if (!a.dy_img) return VG_ERR_INVALID_ARG;
+        // one read of dY: its B-operand image in processing order, and db's partial sums
+        launch_dy_image_tf32(p.dy, p.sorted_idx, p.n, a.num_tiles * kTileRows, p.Cout, p.sms, p.db, p.partial_db,
+                             p.dy_sorted, p.nbr_status, s);
         int st;
         switch (tf32_bn(p.Cout)) {
             case 256: st = launch_tf32<256>(a, p.sms, s); break;
@@ -378,7 +469,8 @@ int tf32_wgrad(const WgradPass& p, cudaStream_t s) {
         launch_reduce_splits(p.partial, p.splits, (int64_t)p.taps * p.Cin * p.Cout, (int64_t)kTaps * p.Cin * p.Cout,
                              p.dW, p.dtype, p.nbr_status, s);
     }
-    if (p.db) launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
+    else if (p.db)
+        launch_dbias(p.dy, p.n, p.Cout, p.sms, p.db, p.partial_db, p.dtype, p.nbr_status, s);
     return VG_OK;
 }
 
