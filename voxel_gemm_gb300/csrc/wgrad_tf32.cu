@@ -99,19 +99,42 @@ __device__ __forceinline__ uint32_t stg_off(int r, int c) { return (uint32_t)(r 
 // (N blocks of one (M block, tap, chunk) next to each other), each unit the
 // positions [first, end) of the tile visiting order whose tile mask has tap k (the
 // first position always counts, so no unit is empty), four 32-row stages per tile.
+// A whole warp walks together: the active positions are found 32 at a time (one
+// load of tile id and mask per lane and a ballot), and the next active tile is
+// looked up one tile ahead so that the last stage of a unit is known.
 struct StageWalk {
-    int64_t u, s, first, end, pos, npos, t;
+    int64_t u, s, first, end, base;
+    int64_t t, nt;      // this stage's tile; the unit's next active tile (-1: none)
+    uint32_t bits;      // active positions in [base, base + 32) not yet taken
+    uint32_t lane_tile; // tile id at position base + lane
     int mb, k, nb, h;
     bool valid, first_stage;
 };
 
-__device__ __forceinline__ int64_t next_active(const T32Args& a, int64_t pos, int64_t first, int64_t end, int k) {
-    for (; pos < end; ++pos)
-        if (pos == first || ((a.tile_mask[a.tile_order[pos]] >> k) & 1u)) return pos;
-    return -1;
+__device__ __forceinline__ void walk_window(StageWalk& w, const T32Args& a, int lane) {
+    const int64_t pos = w.base + lane;
+    bool act = false;
+    w.lane_tile = 0;
+    if (pos < w.end) {
+        w.lane_tile = a.tile_order[pos];
+        act = pos == w.first || ((a.tile_mask[w.lane_tile] >> w.k) & 1u);
+    }
+    w.bits = __ballot_sync(0xffffffffu, act);
 }
 
-__device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units) {
+// The unit's next active tile, or -1 (warp-uniform).
+__device__ __forceinline__ int64_t walk_take(StageWalk& w, const T32Args& a, int lane) {
+    while (w.bits == 0u) {
+        w.base += 32;
+        if (w.base >= w.end) return -1;
+        walk_window(w, a, lane);
+    }
+    const int b = __ffs(w.bits) - 1;
+    w.bits &= w.bits - 1u;
+    return (int64_t)__shfl_sync(0xffffffffu, w.lane_tile, b);
+}
+
+__device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units, int lane) {
     w.valid = w.u < units;
     if (!w.valid) return;
     w.nb = (int)(w.u % NB);
@@ -122,27 +145,27 @@ __device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB
     w.s = r / a.taps;
     w.first = w.s * a.tiles_per_chunk;
     w.end = min(a.num_tiles, w.first + a.tiles_per_chunk);
-    w.pos = w.first;
-    w.t = a.tile_order[w.pos];
-    w.npos = next_active(a, w.pos + 1, w.first, w.end, w.k);
+    w.base = w.first;
+    walk_window(w, a, lane);
+    w.t = walk_take(w, a, lane);  // the first position always counts
+    w.nt = walk_take(w, a, lane);
     w.h = 0;
     w.first_stage = true;
 }
 
-__device__ __forceinline__ bool walk_last(const StageWalk& w) { return w.h == 128 / kRows - 1 && w.npos < 0; }
+__device__ __forceinline__ bool walk_last(const StageWalk& w) { return w.h == 128 / kRows - 1 && w.nt < 0; }
 
-__device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units) {
+__device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units, int lane) {
     w.first_stage = false;
     if (w.h + 1 < 128 / kRows) {
         ++w.h;
-    } else if (w.npos >= 0) {
-        w.pos = w.npos;
-        w.t = a.tile_order[w.pos];
-        w.npos = next_active(a, w.pos + 1, w.first, w.end, w.k);
+    } else if (w.nt >= 0) {
+        w.t = w.nt;
+        w.nt = walk_take(w, a, lane);
         w.h = 0;
     } else {
         w.u += gridDim.x;
-        walk_unit(w, a, MB, NB, units);
+        walk_unit(w, a, MB, NB, units, lane);
     }
 }
 
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         bool ok = true;
         StageWalk wc, wt;  // copy walker (D - 1 stages ahead) and transpose walker
         wc.u = blockIdx.x;
-        walk_unit(wc, a, MB, NB, units);
+        walk_unit(wc, a, MB, NB, units, lane);
         wt = wc;
         uint32_t jn[4];  // neighbour rows (tap k) of this warp's rows warp + 8q of the copy walker's stage
         auto load_idx = [&]() {
@@ -242,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                     const float* src = a.f + (int64_t)(v ? jn[q] : 0u) * a.Cin + (cv ? ch : 0);
                     cp_async16(base + stg_off(warp + 8 * q, lane), src, v ? 16u : 0u);
                 }
-                walk_next(wc, a, MB, NB, units);
+                walk_next(wc, a, MB, NB, units, lane);
                 load_idx();
             }
             cp_async_commit();
@@ -270,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 ok = false;
                 *s_abort = 1;
             }
-            walk_next(wt, a, MB, NB, units);
+            walk_next(wt, a, MB, NB, units, lane);
         }
         cp_async_wait_all();  // no copy of this thread is still writing shared memory
         if (!ok) atomicOr(a.err, kErrTimeout);
@@ -351,24 +374,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         }
     } else {
         // ------------------------------------------------------------ B loader: one bulk copy per stage
-        if (lane == 0) {
-            StageWalk wl;
-            wl.u = blockIdx.x;
-            walk_unit(wl, a, MB, NB, units);
-            uint32_t i = 0;
-            bool ok = true;
-            for (; wl.valid; ++i) {
-                const uint32_t st = i % S, ph = (i / S) & 1u;
-                if (!mbar_wait(empty0 + 8 * st, ph ^ 1u, s_abort)) {
-                    ok = false;
-                    break;
-                }
+        // (the whole warp walks the stages; lane 0 issues the copies)
+        StageWalk wl;
+        wl.u = blockIdx.x;
+        walk_unit(wl, a, MB, NB, units, lane);
+        uint32_t i = 0;
+        bool ok = true;
+        for (; wl.valid; ++i) {
+            const uint32_t st = i % S, ph = (i / S) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * st, ph ^ 1u, s_abort))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
                 mbar_arrive_expect_tx(bfull0 + 8 * st, C::kBBytes);
                 bulk_g2s(smem_u32(stages + (size_t)st * C::kStageBytes + C::kABytes),
                          a.dy_img + tf32_dy_image_offset(wl.t * 128 + wl.h * kRows, wl.nb * BN, a.Cout), C::kBBytes,
                          bfull0 + 8 * st);
-                walk_next(wl, a, MB, NB, units);
             }
+            walk_next(wl, a, MB, NB, units, lane);
+        }
+        if (lane == 0) {
             // before the block may exit, every issued copy must have landed
             for (uint32_t d = 0; d < S && d < i; ++d) {
                 const uint32_t last = i - 1 - d;
