@@ -45,6 +45,7 @@ constexpr int kProducers = kProducerWarps * 32;
 constexpr int kRows = 32;  // voxel rows per stage (one 128-byte K block of fp32)
 constexpr int kBM = 128;   // input channels per unit
 constexpr int kStgBytes = kRows * kBM * 4;  // one staging slot: 32 rows x 128 channels, row-major (512 B rows)
+constexpr int kUnitRingSlots = 4;
 
 template <int BN>
 struct TCfg {
@@ -55,8 +56,10 @@ struct TCfg {
     static constexpr int D = BN == 256 ? 4 : 5;                     // staging slots (copies D - 1 stages ahead)
     static constexpr int NBUF = 2;
     static constexpr int kTmemCols = NBUF * BN;
-    static constexpr int kNumBars = 3 * S + 2 * NBUF + 1;  // full, empty, bfull; tfull, tempty; done
-    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + (size_t)D * kStgBytes + 8 * kNumBars + 4 * S + 16;
+    // full, empty, bfull; tfull, tempty; done; unit ring full and empty
+    static constexpr int kNumBars = 3 * S + 2 * NBUF + 1 + 2 * kUnitRingSlots;
+    static constexpr size_t kSmem = 1024 + (size_t)S * kStageBytes + (size_t)D * kStgBytes + 8 * kNumBars +
+                                    8 * kUnitRingSlots + 4 * S + 16;
     static_assert(kSmem <= 232448, "TF32 weight-gradient stages exceed one CTA's shared memory");
 };
 
@@ -73,6 +76,7 @@ struct T32Args {
     int Cin, Cout;
     float* partial;  // [splits][27][Cin][Cout]
     uint32_t* err;
+    uint32_t* unit_ctr;  // next unit to claim (zero before the launch when units > grid)
 };
 
 // Store the transpose of a 4x4 block: v[e] holds channels c..c+3 of row e; the
@@ -91,9 +95,57 @@ __device__ __forceinline__ void store_t4(uint8_t* img, int m0, int kc, const flo
 }
 
 // Byte offset, in a staging slot, of 16-byte chunk c (channels 4c..4c+3) of row r:
-// chunk c ^ (r & 4), so that eight lanes reading one chunk from each of rows
-// 4q..4q+3 (two row quads) cover all eight bank groups.
-__device__ __forceinline__ uint32_t stg_off(int r, int c) { return (uint32_t)(r * 512 + ((c ^ (r & 4)) << 4)); }
+// chunk c ^ ((r / 4) % 8), so that the eight lanes of a transposing read (one
+// chunk of row 4rq + e for rq = 0..7) cover all eight bank groups; a warp's copy
+// of one row permutes the row's chunks.
+__device__ __forceinline__ uint32_t stg_off(int r, int c) { return (uint32_t)(r * 512 + ((c ^ ((r >> 2) & 7)) << 4)); }
+
+// Work units are handed out dynamically: the copy walker of producer warp 0
+// claims the next unit from a global counter when it starts a unit and publishes
+// it in a 4-slot ring (the CTA's first unit is blockIdx.x); every walker, the MMA
+// thread and the epilogue warps read the ring in order (-1 ends the sequence).
+// With the fixed round-robin the CTAs drifted apart over the chunks and L2 kept
+// 22 % of the reads.
+constexpr int kUnitRing = kUnitRingSlots;
+constexpr int kUnitReaders = 2 * kProducerWarps + 1 + 1 + 4;  // producer walkers, loader, MMA thread, epilogue
+
+struct Ring {
+    volatile int64_t* slot;
+    uint32_t full0, empty0;
+    const volatile uint32_t* abort;
+    uint32_t* ctr;
+    int64_t units;
+};
+
+// Warp-wide read of ring entry qi (the whole warp calls it; lane 0 releases the
+// slot).  timed: wait without looking at the abort flag (the producer warps must
+// all see the same sequence; the claimer always publishes, -1 after a failure).
+__device__ __forceinline__ int64_t ring_read(const Ring& R, uint32_t qi, int lane, bool timed) {
+    const uint32_t slot = qi % kUnitRing, ph = (qi / kUnitRing) & 1u;
+    const bool got = timed ? mbar_wait_timed(R.full0 + 8 * slot, ph) : mbar_wait(R.full0 + 8 * slot, ph, R.abort);
+    const bool ok = __all_sync(0xffffffffu, got);
+    const int64_t u = ok ? R.slot[slot] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(R.empty0 + 8 * slot);
+    return u;
+}
+
+// Single-thread read of ring entry qi (releases the slot).
+__device__ __forceinline__ int64_t ring_read_one(const Ring& R, uint32_t qi) {
+    const uint32_t slot = qi % kUnitRing;
+    const int64_t u = mbar_wait(R.full0 + 8 * slot, (qi / kUnitRing) & 1u, R.abort) ? R.slot[slot] : -1;
+    mbar_arrive(R.empty0 + 8 * slot);
+    return u;
+}
+
+// Claim and publish ring entry qi (one thread).
+__device__ __forceinline__ void ring_publish(const Ring& R, uint32_t qi) {
+    const uint32_t slot = qi % kUnitRing;
+    const bool free_slot = mbar_wait(R.empty0 + 8 * slot, ((qi / kUnitRing) & 1u) ^ 1u, R.abort);
+    const int64_t uu = free_slot ? (int64_t)gridDim.x + (int64_t)atomicAdd(R.ctr, 1u) : R.units;
+    R.slot[slot] = uu < R.units ? uu : -1;
+    mbar_arrive(R.full0 + 8 * slot);
+}
 
 // Walk over the stages of the CTA's units: unit u = nb + NB * (mb + MB * (k + taps * s))
 // (N blocks of one (M block, tap, chunk) next to each other), each unit the
@@ -107,8 +159,9 @@ struct StageWalk {
     int64_t t, nt;      // this stage's tile; the unit's next active tile (-1: none)
     uint32_t bits;      // active positions in [base, base + 32) not yet taken
     uint32_t lane_tile; // tile id at position base + lane
+    uint32_t qi;        // ring entry of the current unit
     int mb, k, nb, h;
-    bool valid, first_stage;
+    bool valid, first_stage, claims;
 };
 
 __device__ __forceinline__ void walk_window(StageWalk& w, const T32Args& a, int lane) {
@@ -134,9 +187,13 @@ __device__ __forceinline__ int64_t walk_take(StageWalk& w, const T32Args& a, int
     return (int64_t)__shfl_sync(0xffffffffu, w.lane_tile, b);
 }
 
-__device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units, int lane) {
-    w.valid = w.u < units;
+// Start the unit of ring entry w.qi (the claiming walker first publishes the next one).
+__device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, const Ring& R, int MB, int NB, int lane,
+                                          bool timed) {
+    w.u = ring_read(R, w.qi, lane, timed);
+    w.valid = w.u >= 0;
     if (!w.valid) return;
+    if (w.claims && lane == 0) ring_publish(R, w.qi + 1);
     w.nb = (int)(w.u % NB);
     int64_t r = w.u / NB;
     w.mb = (int)(r % MB);
@@ -155,7 +212,8 @@ __device__ __forceinline__ void walk_unit(StageWalk& w, const T32Args& a, int MB
 
 __device__ __forceinline__ bool walk_last(const StageWalk& w) { return w.h == 128 / kRows - 1 && w.nt < 0; }
 
-__device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, int MB, int NB, int64_t units, int lane) {
+__device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, const Ring& R, int MB, int NB, int lane,
+                                          bool timed) {
     w.first_stage = false;
     if (w.h + 1 < 128 / kRows) {
         ++w.h;
@@ -164,8 +222,8 @@ __device__ __forceinline__ void walk_next(StageWalk& w, const T32Args& a, int MB
         w.nt = walk_take(w, a, lane);
         w.h = 0;
     } else {
-        w.u += gridDim.x;
-        walk_unit(w, a, MB, NB, units, lane);
+        ++w.qi;
+        walk_unit(w, a, R, MB, NB, lane, timed);
     }
 }
 
@@ -192,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     uint8_t* stages = smem;                                     // [S][A image | B image]
     uint8_t* stg = smem + (size_t)S * C::kStageBytes;           // [D][32 rows x 512 B], row-major
     uint64_t* bars = reinterpret_cast<uint64_t*>(stg + (size_t)D * kStgBytes);
-    uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars);  // per stage: bit0 first, bit1 last
+    volatile int64_t* s_unit = reinterpret_cast<volatile int64_t*>(bars + C::kNumBars);  // unit ring
+    uint32_t* s_info = reinterpret_cast<uint32_t*>(bars + C::kNumBars + kUnitRing);  // per stage: bit0 first, bit1 last
     uint32_t* s_tmem = s_info + S;
     volatile uint32_t* s_abort = s_tmem + 1;
 
@@ -203,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), bfull0 = smem_u32(bars + 2 * S);
     const uint32_t tfull0 = smem_u32(bars + 3 * S), tempty0 = smem_u32(bars + 3 * S + NBUF);
     const uint32_t done_bar = smem_u32(bars + 3 * S + 2 * NBUF);
+    const uint32_t ufull0 = smem_u32(bars + 3 * S + 2 * NBUF + 1), uempty0 = ufull0 + 8 * kUnitRing;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(full0 + 8 * i, kProducers);  // every producer thread
@@ -214,8 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
             mbar_init(tempty0 + 8 * i, 4);
         }
         mbar_init(done_bar, 1);
+        for (int i = 0; i < kUnitRing; ++i) {
+            mbar_init(ufull0 + 8 * i, 1);
+            mbar_init(uempty0 + 8 * i, kUnitReaders);
+        }
         *s_abort = 0;
         fence_mbar_init();
+        s_unit[0] = (int64_t)blockIdx.x;  // the first unit of every CTA (grid <= units)
+        mbar_arrive(ufull0);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
@@ -229,6 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
     const int MB = (a.Cin + kBM - 1) / kBM;
     const int NB = a.Cout / BN;
     const int64_t units = (int64_t)MB * a.taps * NB * a.splits;
+    Ring R;
+    R.slot = s_unit;
+    R.full0 = ufull0;
+    R.empty0 = uempty0;
+    R.abort = s_abort;
+    R.ctr = a.unit_ctr;
+    R.units = units;
 
     if (warp < kProducerWarps) {
         // ------------------------------------------------------------ producers: copy, then transpose
@@ -240,12 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         // stage i - S are done.  All producers walk the same stages and meet at the
         // same barriers; a failed wait ends the loop for all of them at the next one.
         const int p = threadIdx.x;
-        const int rq = lane >> 2, cg = lane & 3;  // transpose: rows 4rq..4rq+3, channels 16 * warp + 4cg..
+        const int rq = lane & 7, cg = lane >> 3;  // transpose: rows 4rq..4rq+3, channels 16 * warp + 4cg..
         bool ok = true;
-        StageWalk wc, wt;  // copy walker (D - 1 stages ahead) and transpose walker
-        wc.u = blockIdx.x;
-        walk_unit(wc, a, MB, NB, units, lane);
-        wt = wc;
+        StageWalk wc, wt;  // copy walker (D - 1 stages ahead; warp 0's claims the units) and transpose walker
+        wc.qi = wt.qi = 0;
+        wc.claims = warp == 0;
+        wt.claims = false;
+        walk_unit(wc, a, R, MB, NB, lane, true);
+        walk_unit(wt, a, R, MB, NB, lane, true);
         uint32_t jn[4];  // neighbour rows (tap k) of this warp's rows warp + 8q of the copy walker's stage
         auto load_idx = [&]() {
 #pragma unroll
@@ -265,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                     const float* src = a.f + (int64_t)(v ? jn[q] : 0u) * a.Cin + (cv ? ch : 0);
                     cp_async16(base + stg_off(warp + 8 * q, lane), src, v ? 16u : 0u);
                 }
-                walk_next(wc, a, MB, NB, units, lane);
+                walk_next(wc, a, R, MB, NB, lane, true);
                 load_idx();
             }
             cp_async_commit();
@@ -293,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                 ok = false;
                 *s_abort = 1;
             }
-            walk_next(wt, a, MB, NB, units, lane);
+            walk_next(wt, a, R, MB, NB, lane, true);
         }
         cp_async_wait_all();  // no copy of this thread is still writing shared memory
         if (!ok) atomicOr(a.err, kErrTimeout);
@@ -301,9 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_tf32(BN);
-            uint32_t it = 0, ua = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; u < units && ok; u += gridDim.x, ++ua) {
+            for (uint32_t ua = 0; ok; ++ua) {
+                if (ring_read_one(R, ua) < 0) break;
                 const uint32_t buf = ua % NBUF;
                 if (!mbar_wait(tempty0 + 8 * buf, ((ua / NBUF) & 1u) ^ 1u, s_abort)) { ok = false; break; }
                 tc_fence_after();
@@ -341,9 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         // ------------------------------------------------------------ epilogue: fp32 partials
         const int q = warp & 3;
         const bool v8ok = (reinterpret_cast<uintptr_t>(a.partial) & 31u) == 0;
-        uint32_t ua = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++ua) {
+        for (uint32_t ua = 0;; ++ua) {
+            const int64_t u = ring_read(R, ua, lane, false);
+            if (u < 0) break;
             const int nb = (int)(u % NB);
             int64_t r = u / NB;
             const int mb = (int)(r % MB);
@@ -376,8 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
         // ------------------------------------------------------------ B loader: one bulk copy per stage
         // (the whole warp walks the stages; lane 0 issues the copies)
         StageWalk wl;
-        wl.u = blockIdx.x;
-        walk_unit(wl, a, MB, NB, units, lane);
+        wl.qi = 0;
+        wl.claims = false;
+        walk_unit(wl, a, R, MB, NB, lane, false);
         uint32_t i = 0;
         bool ok = true;
         for (; wl.valid; ++i) {
@@ -392,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_wgrad_tf32(T32Args a) {
                          a.dy_img + tf32_dy_image_offset(wl.t * 128 + wl.h * kRows, wl.nb * BN, a.Cout), C::kBBytes,
                          bfull0 + 8 * st);
             }
-            walk_next(wl, a, MB, NB, units, lane);
+            walk_next(wl, a, R, MB, NB, lane, false);
         }
         if (lane == 0) {
             // before the block may exit, every issued copy must have landed
@@ -429,6 +507,9 @@ int launch_tf32(const T32Args& a, int sms, cudaStream_t s) {
         return VG_ERR_CUDA;
     const int64_t units = (int64_t)((a.Cin + kBM - 1) / kBM) * a.taps * (a.Cout / BN) * a.splits;
     const int grid = (int)std::min<int64_t>(units, sms);
+    // with no more units than CTAs every claim returns >= gridDim.x >= units (the end),
+    // whatever the counter holds: no reset needed
+    if (units > grid) cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
     kern<<<grid, kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
@@ -480,6 +561,7 @@ int tf32_wgrad(const WgradPass& p, cudaStream_t s) {
         a.Cout = p.Cout;
         a.partial = p.partial;
         a.err = p.err;
+        a.unit_ctr = p.err + kWgradUnitCounter;
         if (!a.dy_img) return VG_ERR_INVALID_ARG;
         // one read of dY: its B-operand image in processing order, and db's partial sums
         launch_dy_image_tf32(p.dy, p.sorted_idx, p.n, a.num_tiles * kTileRows, p.Cout, p.sms, p.db, p.partial_db,
