@@ -518,9 +518,10 @@ int launch_tf32(const T32Args& a, int sms, cudaStream_t s) {
 
 // Split-K chunks: about four units per SM, chunks of at most 256 tiles, at least
 // 4 tiles per chunk, the rows of the chunks in flight (about sms / per_split of
-// them side by side) within 64 MiB so that a chunk's units find its feature and
-// dY rows in L2 (602k voxels, C = 256: 19 chunks 7.9 ms, 55 chunks 7.0 ms, with
-// the earlier register-staged producers), partial sums capped at 1 GiB.
+// them side by side) within 32 MiB so that a chunk's units find its feature and
+// dY rows in L2 (602k voxels, C = 256: 19 chunks 7.9 ms, 55 chunks 7.0 ms with
+// the earlier register-staged producers; now 56 chunks 3.48 ms, 111 chunks
+// 3.36 ms, 222 chunks 3.44 ms), partial sums capped at 1 GiB.
 int tf32_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
     const int64_t T = std::max<int64_t>(1, (n + kTileRows - 1) / kTileRows);
     const int64_t per_split = (int64_t)((Cin + kBM - 1) / kBM) * taps * (Cout / tf32_bn(Cout));
@@ -528,7 +529,7 @@ int tf32_wgrad_splits(int64_t n, int Cin, int Cout, int sms, int taps) {
     S = std::max<int64_t>(S, (T + 255) / 256);
     const int64_t in_flight = (sms + per_split - 1) / per_split;
     const int64_t chunk_bytes = in_flight * T * kTileRows * (int64_t)(Cin + Cout) * 4;
-    S = std::max<int64_t>(S, (chunk_bytes + (int64_t(64) << 20) - 1) / (int64_t(64) << 20));
+    S = std::max<int64_t>(S, (chunk_bytes + (int64_t(32) << 20) - 1) / (int64_t(32) << 20));
     const int64_t bytes_per_split = (int64_t)kTaps * Cin * Cout * 4;
     S = std::min<int64_t>(S, std::max<int64_t>(1, (int64_t(1) << 30) / bytes_per_split));
     S = std::min<int64_t>(S, std::max<int64_t>(1, T / 4));
