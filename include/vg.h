@@ -197,8 +197,8 @@ VG_API int vg_nbrmap_describe(int64_t N, int B, int X, int Y, int Z, unsigned fl
  *   all of `dtype`, 16-byte aligned.
  *   nbr_ws/nbr/mask: a map built by vg_nbrmap_build for the same N.
  *   conv_ws: >= vg_conv_workspace_bytes(...) bytes, 256-byte aligned; holds the
- *   repacked weights, split-K partial sums, dY in processing order (tensor-core
- *   path, Cout >= 128) and a device error record.  Calls that may overlap on
+ *   repacked weights, split-K partial sums, dY in processing order (16-bit
+ *   tensor-core path with Cout >= 128, and TF32) and a device error record.  Calls that may overlap on
  *   the GPU (different streams) need their own conv_ws each; they may share
  *   nbr_ws/nbr/mask, which conv calls only read.
  * ====================================================================================== */
