@@ -161,27 +161,29 @@ def test_tile_pairs_rows_and_ragged_tail(dtype, cout):
     assert max(e_out, e_dx, e_dw) <= tol, (e_out, e_dx, e_dw)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("n", [3000, 60000])
-def test_workspace_contents_do_not_matter(n):
+def test_workspace_contents_do_not_matter(n, dtype):
     """The GEMM kernels hand out work units through counters in the conv workspace
     (reset before a launch with more units than CTAs; with fewer, every claim ends
     the sequence whatever the counter holds).  A workspace full of 0xFF bytes and a
-    zeroed one must give the same bits, in both regimes."""
+    zeroed one must give the same bits, in both regimes (bf16, and fp32 as TF32)."""
     coords = synth.random_coords(n, n, 1, 64, 64, 64)
     N = coords.shape[0]
-    wl = synth.Workload("t", 1, 64, 0, ("sphere",), 256, 256, "bf16", 31, 2.0)
+    wl = synth.Workload("t", 1, 64, 0, ("sphere",), 256, 256, dtype, 31, 2.0)
     f, W, b, dY = (t.cuda() for t in synth.make_tensors(wl, N))
+    flags = ops.VG_NO_SMALL_N_SPLIT | (ops.VG_ALLOW_TF32 if dtype == "f32" else 0)
     m = ops.NbrMap.alloc(N, (1, 64, 64, 64)).build(torch.from_numpy(coords).cuda())
     res = []
     for fill in (0x00, 0xFF):
-        ws = ops.conv_workspace(N, 256, 256, torch.bfloat16)
+        ws = ops.conv_workspace(N, 256, 256, f.dtype, flags=flags)
         ws.view(torch.uint8).fill_(fill)
-        out = torch.empty(N, 256, dtype=torch.bfloat16, device="cuda")
+        out = torch.empty(N, 256, dtype=f.dtype, device="cuda")
         dX = torch.empty_like(out)
         dW = torch.empty_like(W)
         db = torch.empty_like(b)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, flags=ops.VG_NO_SMALL_N_SPLIT)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, flags=ops.VG_NO_SMALL_N_SPLIT)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, flags=flags)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, flags=flags)
         assert ops.vg_conv_status(ws) == ops.VG_OK
         res.append((out, dX, dW, db))
     for a, b_ in zip(*res):

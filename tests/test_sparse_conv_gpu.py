@@ -213,3 +213,36 @@ def test_sparse_conv_16bit_cuda_core_channels_and_graph_capture():
     s.synchronize()
     for a_, b_ in zip(eager, (out, dX, dW, db)):
         assert torch.equal(a_, b_)
+
+
+@pytest.mark.parametrize("cin,cout", [(64, 256), (256, 64)])
+def test_regular_conv_tile_pairs_match_oracle(cin, cout):
+    """Enough output (or input) sites that the 256-column gather passes run on the
+    tile-pair kernel (at least two 128-row tiles per SM): the forward at Cout = 256 and
+    the input gradient at Cin = 256, strided and transposed, every element against the
+    oracle (bf16)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = (1, 96, 96, 96)
+    coords, f_in, W, b = _problem(2, 2, 80000, grid, cin, cout, "bf16", 77 + cin)
+    co, down, up = oracle.sparse_map(coords, *grid, 2, 2)
+    m = ops.SparseMap(torch.from_numpy(coords).cuda(), grid, 2, 2)
+    assert m.n_out == co.shape[0] and min(m.n_in, m.n_out) >= 2 * sms * 128
+    dt, tol = f_in.dtype, TOL["bf16"]
+    W27, Wd, bd = _pad27(W), W.cuda(), b.cuda()
+    for transposed, nbr, n_src, n_dst in ((0, down, m.n_in, m.n_out), (1, up, m.n_out, m.n_in)):
+        x = torch.randn(n_src, cin, generator=torch.Generator().manual_seed(5 + transposed)).to(dt)
+        dY = torch.randn(n_dst, cout, generator=torch.Generator().manual_seed(7 + transposed)).to(dt)
+        ws = m.workspace(transposed, cin, cout, dt)
+        out = torch.empty(n_dst, cout, dtype=dt, device="cuda")
+        dX = torch.empty(n_src, cin, dtype=dt, device="cuda")
+        dW, db = torch.empty_like(Wd), torch.empty_like(bd)
+        m.fwd(transposed, x.cuda(), Wd, bd, out, ws)
+        m.bwd(transposed, dY.cuda(), x.cuda(), Wd, dX, dW, db, ws)
+        torch.cuda.synchronize()
+        assert ops.vg_conv_status(ws) == ops.VG_OK
+        out_ref = oracle.fwd(nbr, f64(x), W27, f64(b))
+        dX_ref = oracle.dgrad_scatter_to(nbr, f64(dY), W27, n_src)
+        dW_ref, db_ref = oracle.wgrad(nbr, f64(x), f64(dY))
+        errs = {"out": rel_fro(f64(out), out_ref), "dX": rel_fro(f64(dX), dX_ref),
+                "dW": rel_fro(f64(dW), dW_ref[:8]), "db": rel_fro(f64(db), db_ref)}
+        assert all(e <= tol for e in errs.values()), (transposed, errs)
