@@ -41,7 +41,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;
 
 // Work units are handed out dynamically: thread 0 of the gather warps claims the
 // next unit from a global counter and publishes it in a 4-slot ring that the
@@ -53,7 +52,7 @@ constexpr int kThreads = 288;
 // the same A rows while they are in L2 (measured at C = 1024: 11.77 ms, against
 // 13.65 ms with the M groups of one N block next to each other).
 constexpr int kUnitRing = 4;
-constexpr int kUnitReaders = 4 + 1 + 4;  // gather warps, the MMA thread, epilogue warps
+// readers of each unit-ring slot: the gather warps, the MMA thread, the epilogue warps
 
 // One CTA work unit holds MU M blocks (MU accumulators of 128 x BN side by side
 // in TMEM, all sharing every dY stage) and streams stages of R sorted rows:
@@ -70,7 +69,11 @@ template <int BN, bool TWO>
 struct WCfg {
     static constexpr int MU = BN == 64 ? (TWO ? 3 : 7) : 2;
     static constexpr int R = BN == 64 ? 32 : 64;           // rows per stage (K of the MMA)
-    static constexpr int RQ = R / 16;                       // rows per gather thread
+    static constexpr int GW = BN == 256 && !TWO ? 8 : 4;    // gather warps
+    static constexpr int kThreads = (GW + 1 + 4) * 32;      // gather, MMA, epilogue warps
+    static constexpr int kUnitReaders = GW + 1 + 4;
+    static constexpr int RSTEP = GW * 4;                    // rows between one gather thread's rows
+    static constexpr int RQ = R / RSTEP;                    // rows per gather thread
     static constexpr int kAccCols = MU * BN;
     static constexpr int NBUF = TWO ? 1 : (2 * kAccCols <= 512 ? 2 : 1);
     static constexpr int kTmemCols = NBUF * kAccCols <= 256 ? 256 : 512;
@@ -142,12 +145,12 @@ struct Meta {
 };
 
 // The dY row index is needed only when the gather threads fetch B themselves (WANT_I).
-template <int MU, int RQ, bool WANT_I>
+template <int MU, int RQ, int RSTEP, bool WANT_I>
 __device__ __forceinline__ void load_meta(const WgArgs& a, const MUnit (&mu)[MU], int64_t row0, int p,
                                           Meta<MU, RQ>& m) {
 #pragma unroll
     for (int q = 0; q < RQ; ++q) {
-        const int64_t r = row0 + (p >> 3) + 16 * q;  // r < num_tiles * 128 always
+        const int64_t r = row0 + (p >> 3) + RSTEP * q;  // r < num_tiles * 128 always
         if (WANT_I) m.i[q] = r < a.n ? a.sorted_idx[r] : kNone;
 #pragma unroll
         for (int u = 0; u < MU; ++u) {
@@ -212,7 +215,7 @@ __device__ __forceinline__ int64_t read_unit(const volatile int64_t* s_unit, uin
 }
 
 template <int BN, bool BF16, bool TWO>
-__global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
+__global__ void __launch_bounds__(WCfg<BN, TWO>::kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
     // B by one bulk copy from the dY image when the tile is wide (R = 64 rows)
     constexpr bool kImgB = BN >= 128;
     static_assert(!kImgB || WCfg<BN, TWO>::R == 64, "one image row group per stage");
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
     using C = WCfg<BN, TWO>;
     constexpr int S = C::S;
     constexpr int MU = C::MU;
+    constexpr int GW = C::GW;  // gather warps; then the MMA warp, then four epilogue warps
     constexpr int NBUF = C::NBUF;
     constexpr int R = C::R, RQ = C::RQ;
     constexpr int NBB = BN / 64;  // 64-column blocks of B
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
     const uint32_t ufull0 = smem_u32(bars + 2 * S + 5), uempty0 = smem_u32(bars + 2 * S + 5 + kUnitRing);
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(full0 + 8 * i, 128 + 1);  // 128 copy arrivals + thread 0's info arrival
+            mbar_init(full0 + 8 * i, GW * 32 + 1);  // the gather threads' copy arrivals + thread 0's info arrival
             mbar_init(empty0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -253,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
         mbar_init(done_bar, 1);
         for (int i = 0; i < kUnitRing; ++i) {
             mbar_init(ufull0 + 8 * i, 1);             // thread 0's publication of the slot
-            mbar_init(uempty0 + 8 * i, kUnitReaders);  // every reader of the slot
+            mbar_init(uempty0 + 8 * i, C::kUnitReaders);  // every reader of the slot
         }
         *s_abort = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == GW) {
         tmem_alloc(smem_u32(s_tmem), C::kTmemCols);
         tmem_relinquish();
     }
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
     const int NB = a.Cout / BN;
     const int64_t units = (int64_t)MG * NB * a.splits;
 
-    if (warp < 4) {
+    if (warp < GW) {
         // ------------------------------------------------------------ gather producer
         const int p = threadIdx.x;
         const int ch = p & 7;
@@ -329,9 +333,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
             int64_t t1 = -1;
             int h1 = 0;
             if (t0 >= 0) {
-                load_meta<MU, RQ, !kImgB>(a, mu, t0 * 128, p, m0);
+                load_meta<MU, RQ, C::RSTEP, !kImgB>(a, mu, t0 * 128, p, m0);
                 advance(t0, h0, t1, h1);
-                if (kDeep && t1 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
+                if (kDeep && t1 >= 0) load_meta<MU, RQ, C::RSTEP, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
             } else {  // empty chunk (the host never makes one): one all-zero stage keeps roles in step
                 null_stage = true;
                 for (int q = 0; q < RQ; ++q) {
@@ -346,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
                 int h2 = 0;
                 if (t1 >= 0) advance(t1, h1, t2, h2);
                 if constexpr (kDeep) {
-                    if (t2 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t2 * 128 + h2 * R, p, m2);
+                    if (t2 >= 0) load_meta<MU, RQ, C::RSTEP, !kImgB>(a, mu, t2 * 128 + h2 * R, p, m2);
                 } else {
-                    if (t1 >= 0) load_meta<MU, RQ, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
+                    if (t1 >= 0) load_meta<MU, RQ, C::RSTEP, !kImgB>(a, mu, t1 * 128 + h1 * R, p, m1);
                 }
                 const int64_t t = t0, tn = t1;
                 const int h = h0;
@@ -378,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
                 for (int v = 0; v < MU; ++v) {
                     const uint32_t a_base = smem_u32(st + v * kABytes);
 #pragma unroll
-                    for (int e = 0; e < 2 * RQ; ++e) {  // A: block e / RQ, row (p>>3) + 16*(e % RQ)
+                    for (int e = 0; e < 2 * RQ; ++e) {  // A: block e / RQ, row (p>>3) + RSTEP*(e % RQ)
                         const int q = e % RQ, blk = e / RQ;
-                        const int row = (p >> 3) + 16 * q;
+                        const int row = (p >> 3) + C::RSTEP * q;
                         const uint32_t j = blk ? mc.j1[v][q] : mc.j0[v][q];
                         const int c = blk ? mu[v].c1 : mu[v].c0;
                         const uint16_t* src = a.f + (int64_t)(j != kNone ? j : 0u) * a.Cin + c + ch * 8;
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
 #pragma unroll
                 for (int e = 0; e < (kImgB ? 0 : NBB * RQ); ++e) {  // B: block e / RQ, the same rows
                     const int q = e % RQ, blk = e / RQ;
-                    const int row = (p >> 3) + 16 * q;
+                    const int row = (p >> 3) + C::RSTEP * q;
                     const uint32_t i = mc.i[q];
                     // rows with none of the unit's taps contribute nothing: skip their dY bytes
                     bool use = false;
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
         }
         cp_async_wait_all();
         if (!ok) atomicOr(a.err, kErrTimeout);
-    } else if (warp == 4) {
+    } else if (warp == GW) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_mn(BF16, BN);
@@ -513,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, TWO ? 2 : 1) k_wgrad_tc(WgArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == GW) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 int wg_bn(int cout) {
@@ -535,7 +539,7 @@ int launch_wgrad(const WgArgs& a, int sms, cudaStream_t s) {
     // with no more units than CTAs every claim returns >= gridDim.x >= units (the end),
     // whatever the counter holds: no reset needed
     if (units > grid) cudaMemsetAsync(a.unit_ctr, 0, sizeof(uint32_t), s);
-    kern<<<grid, kThreads, C::kSmem, s>>>(a);
+    kern<<<grid, C::kThreads, C::kSmem, s>>>(a);
     return VG_OK;
 }
 
