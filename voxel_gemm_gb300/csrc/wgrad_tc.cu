@@ -69,7 +69,10 @@ template <int BN, bool TWO>
 struct WCfg {
     static constexpr int MU = BN == 64 ? (TWO ? 3 : 7) : 2;
     static constexpr int R = BN == 64 ? 32 : 64;           // rows per stage (K of the MMA)
-    static constexpr int GW = BN == 256 && !TWO ? 8 : 4;    // gather warps
+    // gather warps: eight at 256 columns, where two M blocks share each 32 KB dY tile
+    // (602k voxels, C = 1024: 10.62 ms with four, 10.35 with eight, 11.06 with
+    // sixteen); four elsewhere (eight at C = 64, 4.9 M voxels: 2.17 -> 2.49 ms)
+    static constexpr int GW = BN == 256 && !TWO ? 8 : 4;
     static constexpr int kThreads = (GW + 1 + 4) * 32;      // gather, MMA, epilogue warps
     static constexpr int kUnitReaders = GW + 1 + 4;
     static constexpr int RSTEP = GW * 4;                    // rows between one gather thread's rows
@@ -219,8 +222,13 @@ __global__ void __launch_bounds__(WCfg<BN, TWO>::kThreads, TWO ? 2 : 1) k_wgrad_
     // B by one bulk copy from the dY image when the tile is wide (R = 64 rows)
     constexpr bool kImgB = BN >= 128;
     static_assert(!kImgB || WCfg<BN, TWO>::R == 64, "one image row group per stage");
-    constexpr bool kDeep = !TWO;  // row metadata two stages ahead
+    // row metadata two stages ahead with four gather warps (their threads carry twice
+    // the rows), one stage ahead with two CTAs per SM (no registers for a third) and
+    // with eight gather warps (measured at 602k voxels: C = 1024 10.44 -> 10.33 ms,
+    // C = 256 0.970 -> 0.959 ms against two ahead; C = 64 at 4.9 M voxels with four
+    // warps: 2.17 ms two ahead, 2.55 ms one ahead)
     using C = WCfg<BN, TWO>;
+    constexpr bool kDeep = !TWO && C::GW == 4;
     constexpr int S = C::S;
     constexpr int MU = C::MU;
     constexpr int GW = C::GW;  // gather warps; then the MMA warp, then four epilogue warps
@@ -312,11 +320,10 @@ __global__ void __launch_bounds__(WCfg<BN, TWO>::kThreads, TWO ? 2 : 1) k_wgrad_
             cur.base = t_first;
             cur.end = min(a.num_tiles, t_first + a.tiles_per_chunk);
             cur.bits = window_bits(a, cur.base, cur.end, t_first, umask, lane);
-            // Row metadata is loaded two stages ahead of the copies that use it (one stage
-            // ahead, the loads' latency set the pace of the whole pipeline: the MMA thread
-            // waited for full stages 46 % of its time at C = 1024; two ahead: C = 1024
-            // 11.92 -> 10.95 ms, C = 256 1.30 -> 1.18 ms).  Two CTAs per SM have no
-            // registers for a third stage's metadata and load one stage ahead.
+            // Row metadata is loaded ahead of the copies that use it (kDeep: two stages;
+            // with four gather warps and one stage ahead the loads' latency set the pace:
+            // the MMA thread waited for full stages 46 % of its time at C = 1024; two
+            // ahead: C = 1024 11.92 -> 10.95 ms, C = 256 1.30 -> 1.18 ms).
             // (t0, h0): this stage's tile and R-row part; (t1, h1): the next stage's.
             auto advance = [&](int64_t t, int h, int64_t& tn, int& hn) {
                 tn = t;
