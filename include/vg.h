@@ -352,10 +352,9 @@ VG_API int vg_sum_ordered(const void* parts, int nparts, int64_t count, int dtyp
 /* ======================================================================================
  * Forward pass without a caller-provided workspace.
  * The paper has no counterpart to this call.  It is for callers that cannot
- * allocate device memory: code running inside a stream capture (a cudaMalloc there
- * is not part of the graph and can break the capture), plug-ins hosted by a runtime
- * that owns all device memory and forbids allocation after start-up, and hot paths
- * that cannot afford the device-wide synchronisation of cudaMalloc/cudaFree.
+ * allocate device memory: plug-ins hosted by a runtime that owns all device memory
+ * and forbids allocation after start-up, and hot paths that cannot afford the
+ * device-wide synchronisation of cudaMalloc/cudaFree.
  * Arguments and output are those of vg_subm_conv3d_fwd without conv_ws: the scratch
  * (repacked weight tiles and the error word) is a fixed __device__ array of
  * 8 MiB + 256 B inside the library, which every GPU that loads the library holds
@@ -368,7 +367,7 @@ VG_API int vg_sum_ordered(const void* parts, int nparts, int64_t count, int dtyp
  *    bytes on the tensor-core path: 16-bit dtype, Cin and Cout multiples of 64)
  *    exceed 8 MiB, e.g. Cin = Cout = 512.
  *  - Allocates nothing.  The first call on each device looks up the array's device
- *    address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    address (cudaGetSymbolAddress) and keeps it once the lookup succeeds.
  *  - Every call uses the same array, which keeps the previous call's contents: calls
  *    that can overlap on the GPU (other streams, other host threads) race on it and
  *    must be serialised by the caller.

@@ -1,8 +1,8 @@
 """vg_subm_conv3d_fwd_noalloc against vg_subm_conv3d_fwd and the oracle (GPU).
 
 The no-allocation forward serves callers that cannot allocate device memory
-(code inside a stream capture, plug-ins under a runtime that owns all device
-memory, paths that cannot pay for cudaMalloc's synchronisation): its scratch
+(plug-ins under a runtime that owns all device memory, paths that cannot pay
+for cudaMalloc's synchronisation): its scratch
 is a fixed array inside the library instead of a caller workspace.  It runs the
 same kernels as the workspace forward, so its output must be bit-identical to
 it; a second call must not see stale state from the first, because every call

@@ -2,10 +2,9 @@
 //
 // vg_subm_conv3d_fwd needs a caller-provided conv workspace (for the repacked
 // weight tiles of the tensor-core path and a device error word).  Some callers
-// cannot obtain one: code that runs inside a stream capture (a cudaMalloc there
-// is not captured and may break the capture), plug-ins hosted by a runtime that
-// owns all device memory and forbids allocation after start-up, and hot paths
-// that cannot afford the device-wide synchronisation cudaMalloc/cudaFree imply.
+// cannot obtain one: plug-ins hosted by a runtime that owns all device memory and
+// forbids allocation after start-up, and hot paths that cannot afford the
+// device-wide synchronisation cudaMalloc/cudaFree imply.
 // This entry point keeps its scratch in a fixed, file-scope __device__ array
 // instead, so the caller passes only inputs and outputs.
 #include <mutex>
@@ -31,8 +30,8 @@ std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices];  // null until a lookup on that device succeeded
 
 // Device address of the scratch array on the current device.  Only a successful
-// lookup is kept; a failed one (for example during a stream capture, or under a
-// sticky error) returns VG_ERR_CUDA and is retried by the next call.
+// lookup is kept; a failed one (for example under a sticky error) returns
+// VG_ERR_CUDA and is retried by the next call.
 int scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VG_ERR_CUDA;
