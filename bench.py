@@ -579,12 +579,16 @@ def run_workload(args, wl, rank, world, dev, flush, full):
     kp = max(4, min(args.steps, 100))
     up.wait_stream(stream)
     down.wait_stream(stream)
+    e2e_sampler = ClockSampler(dev.index)  # the clocks while copies and compute overlap
+    e2e_sampler.start()
+    e2e_sampler.begin_region()
     e0p, e1p = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0p.record(stream)
     up.wait_stream(stream)
     e2e_pipelined(kp)
     e1p.record(stream)
     stream.synchronize()
+    e2e_clocks = e2e_sampler.stop()
     e2e_ms = max_over_ranks(e0p.elapsed_time(e1p) / kp, world, dev)
     del pbs, red2
 
@@ -596,6 +600,7 @@ def run_workload(args, wl, rank, world, dev, flush, full):
                 "steps": kp, "schedule": "pipelined: step i's uploads while step i-1 computes, its downloads "
                                          "while step i+1 computes (two device slots; K steps between one "
                                          "pair of events)",
+                "clocks": e2e_clocks,
                 "single_step": {"value": world * N / (e2e_single_ms * 1e-3), "ms_per_step": e2e_single_ms,
                                 "schedule": "one step at a time: uploads, passes and downloads overlapped "
                                             "within the step only (CUDA-graph replay, L2 flushed between steps)"}},
