@@ -10,6 +10,7 @@ seeded synthetic voxels, through the C ABI:
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                 [--no-graph] [--one-stream] [--no-cpu-baseline] [--no-sweep]
+python bench.py --ncu-step [--tf32] [--workload NAME] [--warmup W]   (a command for profilers)
 
 Prints ONE JSON line (rank 0).  The headline workload (default: batch 1, 512^3
 grid, Cin = Cout = 1024, bf16) gets the full record: step time, per-pass
@@ -1002,10 +1003,17 @@ def rows_budget(wl):
 def run_ncu_step(args):
     """The command a profiler attaches to: --warmup eager steps, then one more, of the
     workload's map build + forward + input gradient + weight/bias gradient on one
-    stream with one conv workspace (per step the kernels launch in that order)."""
+    stream with one conv workspace (per step the kernels launch in that order).
+    With --tf32: fp32 features at Cin = Cout = 256 on the workload's voxels, under
+    VG_ALLOW_TF32 (the bench's TF32 record)."""
     import torch
     from voxel_gemm_gb300 import ops, synth
     wl = synth.WORKLOADS[args.workload]
+    flags = 0
+    if args.tf32:
+        wl = synth.Workload(wl.name + "_f32", wl.B, wl.res, wl.shapes_per_sample, wl.kinds, 256, 256, "f32",
+                            wl.seed, 2.0, key_flag=wl.key_flag)
+        flags = ops.VG_ALLOW_TF32
     dev = torch.device("cuda", 0)
     s = torch.cuda.Stream()
     coords = torch.from_numpy(synth.make_coords(wl)).to(dev)
@@ -1013,15 +1021,15 @@ def run_ncu_step(args):
     f, W, b, dY = synth.make_tensors(wl, N, device=dev)
     dt = f.dtype
     m = ops.NbrMap.alloc(N, wl.grid, wl.key_flag)
-    ws = ops.conv_workspace(N, wl.cin, wl.cout, dt)
+    ws = ops.conv_workspace(N, wl.cin, wl.cout, dt, flags=flags)
     out = torch.empty(N, wl.cout, dtype=dt, device=dev)
     dX = torch.empty(N, wl.cin, dtype=dt, device=dev)
     dW = torch.empty_like(W)
     db = torch.empty_like(b)
     for _ in range(args.warmup + 1):
         m.build(coords, s)
-        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, stream=s)
-        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, stream=s)
+        ops.vg_subm_conv3d_fwd(m.ws, m.nbr, m.mask, f, W, b, out, ws, flags=flags, stream=s)
+        ops.vg_subm_conv3d_bwd(m.ws, m.nbr, m.mask, dY, f, W, dX, dW, db, ws, flags=flags, stream=s)
     s.synchronize()
     assert m.status(s) == ops.VG_OK and ops.vg_conv_status(ws, s) == ops.VG_OK
     print(json.dumps({"ncu_step": wl.name, "N": N}))
@@ -1041,6 +1049,8 @@ def main():
                     help="issue the step's conv passes one after the other on one stream")
     ap.add_argument("--ncu-step", action="store_true",
                     help="run --warmup + 1 eager steps on one stream and exit (for profilers)")
+    ap.add_argument("--tf32", action="store_true",
+                    help="with --ncu-step: fp32 features (C = 256) under VG_ALLOW_TF32")
     args = ap.parse_args()
     if args.ncu_step:
         run_ncu_step(args)
