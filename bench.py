@@ -866,7 +866,9 @@ def run_ours(args, rank, world, local_rank):
     head = run_workload(args, wl, rank, world, dev, flush, full=True)
     torch.cuda.empty_cache()
     sweep = []
-    if not args.no_sweep:
+    # with N ranks only the headline runs: the other records are single-GPU measurements,
+    # and a rank that failed one of them would leave the others waiting in a collective
+    if not args.no_sweep and world == 1:
         for name in SWEEP:
             if name == wl.name:
                 continue
