@@ -767,9 +767,11 @@ int nbr_layout(int64_t N, int B, int X, int Y, int Z, unsigned flags, int sms, N
               ncols <= 8.0 * (double)N + (double)(1 << 20));
     l.num_tiles = (N + kTileRows - 1) / kTileRows;
     // keys per thread in the radix sort: enough blocks to fill the GPU (about
-    // 2 per SM), at most 16 keys per thread
+    // 2 per SM), 4 to 16 keys per thread (below 4, the blocks' look-back chain
+    // costs more than their parallelism gives: map build at 25k voxels 0.112 ms
+    // with 1 key per thread, 0.107 ms with 4, 0.139 ms with 16)
     const int64_t per_block_target = std::max<int64_t>(1, N / (2 * (int64_t)l.sms));
-    l.sort_items = (int)std::min<int64_t>(16, std::max<int64_t>(1, (per_block_target + kSortThreads - 1) / kSortThreads));
+    l.sort_items = (int)std::min<int64_t>(16, std::max<int64_t>(4, (per_block_target + kSortThreads - 1) / kSortThreads));
     int64_t tile = (int64_t)kSortThreads * l.sort_items;
     l.sort_blocks = std::max<int64_t>(1, (N + tile - 1) / tile);
     (void)tile;
