@@ -859,7 +859,9 @@ static void launch_layout(const int4* coords, const NbrLayout& l, int L, char* w
     const int64_t sblocks = std::max(l.sort_blocks, l.tile_blocks);
     if (!keys_ready) {
         layout_memset(l, ws, s);
-        const int gh_blocks = (int)std::min<int64_t>(l.sort_blocks, 4 * (int64_t)l.sms);
+        // (a grid-stride loop: one key per thread up to four blocks per SM)
+        const int gh_blocks =
+            (int)std::max<int64_t>(1, std::min<int64_t>((n + kSortThreads - 1) / kSortThreads, 4 * (int64_t)l.sms));
         k_key_globalhist<SK><<<gh_blocks, kSortThreads, 0, s>>>(coords, nbr, n, L, l.fine_keep, l.curve, passes,
                                                                 mask, ka, hist);
     }
