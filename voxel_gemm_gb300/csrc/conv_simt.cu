@@ -202,9 +202,12 @@ __global__ void k_reduce_splits(const float* __restrict__ partial, int splits, i
 // db partial sums: block b sums rows [b*rows, (b+1)*rows) of dy into
 // partial_db[b][:].  Thread = (row lane, 8-column group); each thread sums its
 // rows in order, then row lanes are combined in order: a fixed summation order.
-// rows = n / (2 * SMs) rounded up to a multiple of 256, within [256, 4096].
+// rows = n / (4 * SMs) rounded up to a multiple of 256, within [256, 4096]: about
+// four blocks per SM keep enough rows in flight for the dY image copy (602k
+// voxels: weight-gradient pass at C = 256 0.952 -> 0.909 ms, C = 1024 10.06-10.29
+// -> 9.96 ms, TF32 C = 256 3.44 -> 3.19 ms against two blocks per SM).
 inline int64_t dbias_rows(int64_t n, int sms) {
-    int64_t r = (n / (2 * (int64_t)sms) + 255) / 256 * 256;
+    int64_t r = (n / (4 * (int64_t)sms) + 255) / 256 * 256;
     return r < 256 ? 256 : (r > 4096 ? 4096 : r);
 }
 
